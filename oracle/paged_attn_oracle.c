@@ -1,0 +1,212 @@
+/*
+ * Reference oracle for single-token decode attention over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain CPU definition that
+ * the CUDA library is checked against.  Only the test suite, the smoke check
+ * and the CPU-baseline leg of the benchmark load it.  The product path never
+ * links, calls or falls back to it, and it shares no code, header, table or
+ * constant with the CUDA sources.
+ *
+ * What it computes (issue "ROCm gfx1200: PagedAttnOnline is 8.1x slower per
+ * call ...", section "Where to look": a decode kernel that does online
+ * softmax over a KV cache read in NHD layout through strides, after a
+ * per-request lookup of the sequence's pages; PR "perf(cuda): head_dim-128
+ * arm for the warp-split-KV decode kernel", commit message: 32-token pages,
+ * GQA-fused query heads, an optional sliding window):
+ *
+ *   for every sequence b and every query head i (kv head h = i / g,
+ *   g = num_q_heads / num_kv_heads):
+ *     L  = context_lens[b]
+ *     t0 = window > 0 ? max(0, L - window) : 0
+ *     for every token t in [t0, L):
+ *        page = block_tables[b][t / block_size], slot = t % block_size
+ *        k_t  = k_cache[page][slot][h][:],  v_t = v_cache[page][slot][h][:]
+ *        s_t  = scale * sum_d q[b][i][d] * k_t[d]
+ *     out[b][i][:] = sum_t softmax(s)_t * v_t
+ *
+ * Online softmax (what the kernels on those pages use) is an exact
+ * reformulation of this; the oracle takes the plain two-pass form instead:
+ * pass 1 finds M = max_t s_t, pass 2 forms Z = sum_t exp(s_t - M) and
+ * sum_t exp(s_t - M) v_t, and the row is their ratio.  Every stored element is
+ * widened exactly to double first (bf16 and binary32 are both subsets of
+ * binary64) and all arithmetic is double.
+ *
+ * Readings taken where the pages are silent:
+ *   - kv head of query head i is i / g (contiguous query groups);
+ *   - cache layout [num_blocks][block_size][num_kv_heads][head_dim], head_dim
+ *     contiguous ("NHD");
+ *   - block table [num_seqs][max_blocks_per_seq] int32, row-major;
+ *   - window W > 0 keeps the keys t with L - W <= t < L; W <= 0 keeps all;
+ *   - a sequence with L == 0 yields a zero row.
+ *
+ * Error behaviour: returns ORACLE_OK (0) or a negative code, and writes
+ * nothing for the offending row, when a context length is negative or longer
+ * than the block-table row, or a page id lies outside [0, num_blocks).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG (-1)
+#define ORACLE_BAD_CONTEXT (-2)
+#define ORACLE_BAD_PAGE (-3)
+#define ORACLE_NO_MEMORY (-4)
+
+/* Storage codes for q / k_cache / v_cache elements. */
+#define ORACLE_ELEM_BF16 0 /* uint16 bit patterns of bfloat16 */
+#define ORACLE_ELEM_F32 1
+#define ORACLE_ELEM_F64 2
+
+/* bfloat16 is the upper half of an IEEE binary32 word: shifting the 16 stored
+ * bits into the top of a 32-bit word gives that binary32 value exactly. */
+static double widen_bf16(uint16_t bits) {
+  uint32_t word = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &word, sizeof f);
+  return (double)f;
+}
+
+/* Element e of an array stored with code `elem`, widened to double. */
+static double element(const void* base, int elem, size_t e) {
+  switch (elem) {
+    case ORACLE_ELEM_BF16:
+      return widen_bf16(((const uint16_t*)base)[e]);
+    case ORACLE_ELEM_F32:
+      return (double)((const float*)base)[e];
+    default:
+      return ((const double*)base)[e];
+  }
+}
+
+/* Flat index of element d of token slot `slot`, kv head h, in page `page`
+ * of a cache laid out [num_blocks][block_size][num_kv_heads][head_dim]. */
+static size_t cache_index(int page, int slot, int h, int d, int block_size,
+                          int num_kv_heads, int head_dim) {
+  return (((size_t)page * block_size + slot) * num_kv_heads + h) * head_dim + d;
+}
+
+/* One output row: sequence b, query head i.  out_row has head_dim doubles. */
+int oracle_decode_row(double* out_row, const void* q, const void* k_cache,
+                      const void* v_cache, int elem,
+                      const int32_t* block_tables, const int32_t* context_lens,
+                      int num_seqs, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int max_blocks_per_seq,
+                      int num_blocks, double scale, int window, int b, int i) {
+  if (!out_row || !q || !k_cache || !v_cache || !block_tables ||
+      !context_lens || num_seqs <= 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+      num_q_heads % num_kv_heads != 0 || b < 0 || b >= num_seqs || i < 0 ||
+      i >= num_q_heads || elem < ORACLE_ELEM_BF16 || elem > ORACLE_ELEM_F64)
+    return ORACLE_BAD_ARG;
+
+  const int group = num_q_heads / num_kv_heads;
+  const int h = i / group;
+  const int L = context_lens[b];
+  if (L < 0 || (long long)L > (long long)max_blocks_per_seq * block_size)
+    return ORACLE_BAD_CONTEXT;
+  const int t0 = (window > 0 && L - window > 0) ? L - window : 0;
+  const int n = L - t0;
+
+  for (int d = 0; d < head_dim; ++d) out_row[d] = 0.0;
+  if (n == 0) return ORACLE_OK;
+
+  /* Request lookup: physical page of every token in the range. */
+  int* page_of = (int*)malloc(sizeof(int) * (size_t)n);
+  double* s = (double*)malloc(sizeof(double) * (size_t)n);
+  if (!page_of || !s) {
+    free(page_of);
+    free(s);
+    return ORACLE_NO_MEMORY;
+  }
+  for (int j = 0; j < n; ++j) {
+    const int t = t0 + j;
+    const int page = block_tables[(size_t)b * max_blocks_per_seq + t / block_size];
+    if (page < 0 || page >= num_blocks) {
+      free(page_of);
+      free(s);
+      return ORACLE_BAD_PAGE;
+    }
+    page_of[j] = page;
+  }
+
+  /* Scores s_t = scale * <q_i, k_t>. */
+  const size_t q_row = ((size_t)b * num_q_heads + i) * head_dim;
+  for (int j = 0; j < n; ++j) {
+    const int slot = (t0 + j) % block_size;
+    double dot = 0.0;
+    for (int d = 0; d < head_dim; ++d) {
+      const double kd = element(k_cache, elem,
+                                cache_index(page_of[j], slot, h, d, block_size,
+                                            num_kv_heads, head_dim));
+      dot += element(q, elem, q_row + d) * kd;
+    }
+    s[j] = scale * dot;
+  }
+
+  /* Pass 1: the row maximum. */
+  double M = s[0];
+  for (int j = 1; j < n; ++j)
+    if (s[j] > M) M = s[j];
+
+  /* Pass 2: normaliser and weighted sum of values. */
+  double Z = 0.0;
+  for (int j = 0; j < n; ++j) {
+    const int slot = (t0 + j) % block_size;
+    const double w = exp(s[j] - M);
+    Z += w;
+    for (int d = 0; d < head_dim; ++d)
+      out_row[d] += w * element(v_cache, elem,
+                                cache_index(page_of[j], slot, h, d, block_size,
+                                            num_kv_heads, head_dim));
+  }
+  for (int d = 0; d < head_dim; ++d) out_row[d] /= Z;
+
+  free(page_of);
+  free(s);
+  return ORACLE_OK;
+}
+
+/* Every row: out is [num_seqs][num_q_heads][head_dim] doubles. */
+int oracle_decode(double* out, const void* q, const void* k_cache,
+                  const void* v_cache, int elem, const int32_t* block_tables,
+                  const int32_t* context_lens, int num_seqs, int num_q_heads,
+                  int num_kv_heads, int head_dim, int block_size,
+                  int max_blocks_per_seq, int num_blocks, double scale,
+                  int window) {
+  if (!out || num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0)
+    return ORACLE_BAD_ARG;
+  for (int b = 0; b < num_seqs; ++b)
+    for (int i = 0; i < num_q_heads; ++i) {
+      const int rc = oracle_decode_row(
+          out + ((size_t)b * num_q_heads + i) * head_dim, q, k_cache, v_cache,
+          elem, block_tables, context_lens, num_seqs, num_q_heads,
+          num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+          scale, window, b, i);
+      if (rc != ORACLE_OK) return rc;
+    }
+  return ORACLE_OK;
+}
+
+/* A chosen list of rows: rows[2*r] = b, rows[2*r+1] = i; out is
+ * [num_rows][head_dim].  Used to check sampled outputs of large batches. */
+int oracle_decode_rows(double* out, const int32_t* rows, int num_rows,
+                       const void* q, const void* k_cache, const void* v_cache,
+                       int elem, const int32_t* block_tables,
+                       const int32_t* context_lens, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int max_blocks_per_seq, int num_blocks,
+                       double scale, int window) {
+  if (!out || !rows || num_rows < 0 || head_dim <= 0) return ORACLE_BAD_ARG;
+  for (int r = 0; r < num_rows; ++r) {
+    const int rc = oracle_decode_row(
+        out + (size_t)r * head_dim, q, k_cache, v_cache, elem, block_tables,
+        context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+        block_size, max_blocks_per_seq, num_blocks, scale, window, rows[2 * r],
+        rows[2 * r + 1]);
+    if (rc != ORACLE_OK) return rc;
+  }
+  return ORACLE_OK;
+}

@@ -1,0 +1,386 @@
+"""Pins for the CPU oracle: facts fixed by mathematics or by the pages, not by
+the oracle itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with:
+  * a library routine (torch's fp64 scaled_dot_product_attention on dense,
+    contiguous K/V with its own GQA expansion),
+  * a closed form (one token returns it; equal scores give the mean; window 1
+    returns the last token; two tokens give a logistic blend; a hand-worked
+    fixture under tests/golden/),
+  * an invariance (physical page order, block size, splitting query heads),
+  * the bfloat16 format (bit patterns whose values are fixed by the format).
+``test_oracle.py`` runs them on the real oracle and ``test_oracle_mutants.py``
+runs them on deliberately broken copies to show each plausible mistake is
+caught by at least one of them.
+"""
+from __future__ import annotations
+
+import json
+import math
+from pathlib import Path
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+GOLDEN = Path(__file__).resolve().parent / "golden"
+STRADDLE_CONTEXTS = (1, 31, 32, 33, 64, 100, 685, 1000)
+
+
+# ----------------------------------------------------------------------------
+# Layout helpers (no attention arithmetic): dense per-sequence K/V -> paged pool
+# ----------------------------------------------------------------------------
+def paginate(dense_k, dense_v, block_size, rng, num_blocks=None, pad_pages=3):
+    """Scatter dense per-sequence K/V (lists of [L_b][Hkv][D] arrays) into a
+    shuffled page pool.  Returns (k_cache, v_cache, block_tables, context_lens).
+    Unused pool pages and in-page tails hold NaN."""
+    lens = [k.shape[0] for k in dense_k]
+    pages = [(L + block_size - 1) // block_size for L in lens]
+    hkv, d = dense_k[0].shape[1], dense_k[0].shape[2]
+    used = sum(pages)
+    nb = num_blocks if num_blocks is not None else used + pad_pages
+    perm = rng.permutation(nb)
+    dtype = dense_k[0].dtype
+    fill = 0x7FC0 if dtype == np.uint16 else np.nan  # bf16 NaN bits / float NaN
+    k_cache = np.full((nb, block_size, hkv, d), fill, dtype=dtype)
+    v_cache = np.full((nb, block_size, hkv, d), fill, dtype=dtype)
+    maxb = max(max(pages), 1)
+    bt = np.full((len(lens), maxb), perm[-1], dtype=np.int32)
+    pos = 0
+    for b, L in enumerate(lens):
+        for t in range(L):
+            page = perm[pos + t // block_size]
+            k_cache[page, t % block_size] = dense_k[b][t]
+            v_cache[page, t % block_size] = dense_v[b][t]
+        bt[b, :pages[b]] = perm[pos:pos + pages[b]]
+        pos += pages[b]
+    return k_cache, v_cache, bt, np.asarray(lens, dtype=np.int32)
+
+
+def sdpa_reference(q, dense_k, dense_v, scale, window=0):
+    """torch fp64 scaled_dot_product_attention per sequence; q is [B][Hq][D]."""
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b in range(q.shape[0]):
+        L = dense_k[b].shape[0]
+        if L == 0:
+            continue
+        qq = torch.from_numpy(np.asarray(q[b], dtype=np.float64))[None, :, None, :]
+        kk = torch.from_numpy(np.asarray(dense_k[b], dtype=np.float64)).permute(1, 0, 2)[None]
+        vv = torch.from_numpy(np.asarray(dense_v[b], dtype=np.float64)).permute(1, 0, 2)[None]
+        mask = torch.ones((1, 1, 1, L), dtype=torch.bool)
+        if window > 0 and L > window:
+            mask[..., : L - window] = False
+        o = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale,
+                                           enable_gqa=True)
+        out[b] = o[0, :, 0, :].numpy()
+    return out
+
+
+def _rand(rng, shape, kind):
+    x = rng.standard_normal(shape)
+    if kind == "f64":
+        return x
+    if kind == "f32":
+        return x.astype(np.float32)
+    # bf16: round float32 draws to bfloat16 with torch (RNE), keep the bits
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def widen(a):
+    """Exact float64 value of oracle storage (uint16 = bf16 bits)."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    return a.astype(np.float64)
+
+
+def _case(rng, lens, hq, hkv, d, kind):
+    q = _rand(rng, (len(lens), hq, d), kind)
+    dk = [_rand(rng, (L, hkv, d), kind) for L in lens]
+    dv = [_rand(rng, (L, hkv, d), kind) for L in lens]
+    return q, dk, dv
+
+
+def _check_against_sdpa(oracle, rng, lens, hq, hkv, d, block_size, kind, window, tol):
+    q, dk, dv = _case(rng, lens, hq, hkv, d, kind)
+    kc, vc, bt, cl = paginate(dk, dv, block_size, rng)
+    scale = 1.0 / math.sqrt(d)
+    got = oracle.decode(q, kc, vc, bt, cl, scale, window)
+    want = sdpa_reference(widen(q), [widen(k) for k in dk], [widen(v) for v in dv], scale, window)
+    err = np.abs(got - want).max()
+    assert err <= tol, f"oracle vs SDPA max |err| {err:.3e} (lens {lens}, g {hq // hkv}, W {window})"
+
+
+# ----------------------------------------------------------------------------
+# Pins
+# ----------------------------------------------------------------------------
+def pin_sdpa_small_shapes(oracle):
+    """Brute force on dense K/V for tiny shapes, several GQA groups, block sizes
+    and windows (fp64 storage)."""
+    rng = np.random.default_rng(11)
+    for hq, hkv in ((4, 4), (4, 2), (8, 2), (6, 3)):
+        for block_size in (1, 4, 32):
+            for window in (0, 1, 3, 7):
+                _check_against_sdpa(oracle, rng, [1, 5, 9, 13], hq, hkv, 8, block_size,
+                                    "f64", window, 1e-12)
+
+
+def pin_sdpa_straddle_contexts(oracle):
+    """Contexts straddling the 32-token page boundary (the list the head_dim-128
+    decode PR's numerics table uses), head_dim 128, bf16 storage."""
+    rng = np.random.default_rng(12)
+    _check_against_sdpa(oracle, rng, list(STRADDLE_CONTEXTS), 4, 2, 128, 32, "bf16", 0, 1e-12)
+    _check_against_sdpa(oracle, rng, list(STRADDLE_CONTEXTS), 4, 2, 128, 32, "bf16", 40, 1e-12)
+
+
+def pin_sdpa_fp32_storage_d256(oracle):
+    rng = np.random.default_rng(13)
+    _check_against_sdpa(oracle, rng, [1, 33, 70], 8, 2, 256, 32, "f32", 0, 1e-12)
+    _check_against_sdpa(oracle, rng, [1, 33, 70], 8, 2, 256, 32, "f32", 17, 1e-12)
+
+
+def pin_context_one_returns_v(oracle):
+    """softmax over one key is 1: the row is that token's value, bit for bit."""
+    rng = np.random.default_rng(14)
+    for kind in ("bf16", "f32", "f64"):
+        q, dk, dv = _case(rng, [1, 1], 4, 2, 16, kind)
+        kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+        got = oracle.decode(q, kc, vc, bt, cl, 0.25, 0)
+        for b in range(2):
+            for i in range(4):
+                assert np.array_equal(got[b, i], widen(dv[b])[0, i // 2]), (kind, b, i)
+
+
+def pin_equal_scores_give_mean(oracle):
+    """q = 0 (or scale = 0) makes every score 0: the row is the mean of the
+    window's values."""
+    rng = np.random.default_rng(15)
+    lens = [3, 32, 45]
+    _, dk, dv = _case(rng, lens, 4, 2, 16, "f64")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    for window in (0, 10):
+        for q, scale in ((np.zeros((3, 4, 16)), 0.5), (rng.standard_normal((3, 4, 16)), 0.0)):
+            got = oracle.decode(q, kc, vc, bt, cl, scale, window)
+            for b, L in enumerate(lens):
+                t0 = max(0, L - window) if window > 0 else 0
+                mean = dv[b][t0:L].mean(axis=0)
+                for i in range(4):
+                    np.testing.assert_allclose(got[b, i], mean[i // 2], rtol=0, atol=1e-14)
+
+
+def pin_window_one_returns_last(oracle):
+    rng = np.random.default_rng(16)
+    lens = [1, 2, 32, 33, 77]
+    q, dk, dv = _case(rng, lens, 4, 2, 16, "bf16")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    got = oracle.decode(q, kc, vc, bt, cl, 0.25, 1)
+    for b, L in enumerate(lens):
+        for i in range(4):
+            assert np.array_equal(got[b, i], widen(dv[b])[L - 1, i // 2]), (b, i)
+
+
+def pin_window_covering_context_is_no_window(oracle):
+    rng = np.random.default_rng(17)
+    lens = [5, 32, 64, 100]
+    q, dk, dv = _case(rng, lens, 4, 2, 16, "bf16")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    full = oracle.decode(q, kc, vc, bt, cl, 0.25, 0)
+    for window in (100, 101, 1 << 20):
+        assert np.array_equal(oracle.decode(q, kc, vc, bt, cl, 0.25, window), full)
+
+
+def pin_window_is_truncated_sequence(oracle):
+    """Window W over a context of L equals the plain problem over the last W
+    tokens laid out as a fresh sequence (in other pages)."""
+    rng = np.random.default_rng(18)
+    lens = [40, 70, 129]
+    q, dk, dv = _case(rng, lens, 4, 2, 16, "bf16")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    for window in (1, 31, 32, 33, 64):
+        got = oracle.decode(q, kc, vc, bt, cl, 0.25, window)
+        tk = [k[-window:] for k in dk]
+        tv = [v[-window:] for v in dv]
+        kc2, vc2, bt2, cl2 = paginate(tk, tv, 32, rng)
+        want = oracle.decode(q, kc2, vc2, bt2, cl2, 0.25, 0)
+        assert np.array_equal(got, want), window
+
+
+def pin_page_permutation_invariance(oracle):
+    """Where the pages sit in the pool (and hence the table's ids) must not
+    change a single bit of the output."""
+    rng = np.random.default_rng(19)
+    lens = list(STRADDLE_CONTEXTS[:6])
+    q, dk, dv = _case(rng, lens, 4, 2, 32, "bf16")
+    outs = []
+    for seed in (1, 2, 3):
+        kc, vc, bt, cl = paginate(dk, dv, 32, np.random.default_rng(seed), pad_pages=9)
+        outs.append(oracle.decode(q, kc, vc, bt, cl, 0.2, 0))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def pin_block_size_invariance(oracle):
+    """The same token sequence paged with 1-, 8- and 32-token pages gives the
+    same bits."""
+    rng = np.random.default_rng(20)
+    lens = [1, 9, 40]
+    q, dk, dv = _case(rng, lens, 4, 2, 16, "f32")
+    outs = []
+    for bs in (1, 8, 32):
+        kc, vc, bt, cl = paginate(dk, dv, bs, rng)
+        outs.append(oracle.decode(q, kc, vc, bt, cl, 0.3, 0))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def pin_gqa_value_head_mapping(oracle):
+    """V of kv head h is the constant 2**h: every query head of group h must
+    return exactly 2**h (weights sum to one; powers of two scale exactly)."""
+    rng = np.random.default_rng(21)
+    hq, hkv, d = 12, 3, 8
+    lens = [7, 33]
+    q, dk, _ = _case(rng, lens, hq, hkv, d, "f64")
+    dv = [np.broadcast_to((2.0 ** np.arange(hkv))[None, :, None], (L, hkv, d)).copy()
+          for L in lens]
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    got = oracle.decode(q, kc, vc, bt, cl, 0.3, 0)
+    for i in range(hq):
+        assert np.array_equal(got[:, i], np.full((2, d), 2.0 ** (i // (hq // hkv)))), i
+
+
+def pin_gqa_key_head_mapping(oracle):
+    """Key head h has one dominant key, at token h; values encode the token
+    index.  Query heads of group h must pick token h."""
+    hq, hkv, d, L = 8, 4, 4, 6
+    q = np.ones((1, hq, d))
+    k = np.zeros((L, hkv, d))
+    for h in range(hkv):
+        k[h, h, :] = 20.0
+    v = np.broadcast_to(np.arange(L, dtype=np.float64)[:, None, None], (L, hkv, d)).copy()
+    kc, vc, bt, cl = paginate([k], [v], 4, np.random.default_rng(22))
+    got = oracle.decode(q, kc, vc, bt, cl, 1.0, 0)
+    for i in range(hq):
+        np.testing.assert_allclose(got[0, i], i // (hq // hkv), rtol=0, atol=1e-9, err_msg=str(i))
+
+
+def pin_two_token_logistic(oracle):
+    """Two keys with scores a and b: row = v1 + (v0 - v1) / (1 + exp(b - a))."""
+    a, b = 0.5, -1.25
+    q = np.array([[[1.0, 0.0]]])
+    k = np.array([[[a, 0.0]], [[b, 0.0]]])
+    v = np.array([[[3.0, -1.0]], [[-2.0, 5.0]]])
+    kc, vc, bt, cl = paginate([k], [v], 1, np.random.default_rng(23))
+    got = oracle.decode(q, kc, vc, bt, cl, 1.0, 0)[0, 0]
+    want = v[1, 0] + (v[0, 0] - v[1, 0]) / (1.0 + math.exp(b - a))
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-15)
+
+
+def pin_large_scores_stay_finite(oracle):
+    """Scores near 1600 overflow exp() unless the maximum is subtracted first;
+    the row must equal the dominant token's value."""
+    d, L = 16, 5
+    q = np.full((1, 1, d), 10.0)
+    k = np.zeros((L, 1, d))
+    k[3, 0, :] = 10.0
+    k[1, 0, :] = 9.0
+    v = np.arange(L * d, dtype=np.float64).reshape(L, 1, d)
+    kc, vc, bt, cl = paginate([k], [v], 2, np.random.default_rng(24))
+    got = oracle.decode(q, kc, vc, bt, cl, 1.0, 0)[0, 0]
+    assert np.all(np.isfinite(got))
+    np.testing.assert_allclose(got, v[3, 0], rtol=0, atol=1e-12)
+
+
+def pin_scores_scale_by_scale(oracle):
+    """Doubling ``scale`` equals doubling every key."""
+    rng = np.random.default_rng(25)
+    q, dk, dv = _case(rng, [20], 2, 1, 8, "f64")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    a = oracle.decode(q, kc, vc, bt, cl, 0.5, 0)
+    b = oracle.decode(q, kc * 2.0, vc, bt, cl, 0.25, 0)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+    c = oracle.decode(q, kc, vc, bt, cl, 0.25, 0)
+    assert np.abs(a - c).max() > 1e-3
+
+
+def pin_query_heads_independent(oracle):
+    """Each query head alone (Hq = Hkv = 1, its kv head's pages) gives the same
+    bits as inside the full GQA problem."""
+    rng = np.random.default_rng(26)
+    hq, hkv, d = 6, 2, 16
+    lens = [17, 40]
+    q, dk, dv = _case(rng, lens, hq, hkv, d, "bf16")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    full = oracle.decode(q, kc, vc, bt, cl, 0.25, 0)
+    for i in range(hq):
+        h = i // (hq // hkv)
+        one = oracle.decode(np.ascontiguousarray(q[:, i:i + 1]), np.ascontiguousarray(kc[:, :, h:h + 1]),
+                            np.ascontiguousarray(vc[:, :, h:h + 1]), bt, cl, 0.25, 0)
+        assert np.array_equal(one[:, 0], full[:, i]), i
+
+
+def pin_hand_worked_fixture(oracle):
+    fx = json.loads((GOLDEN / "hand_worked_decode.json").read_text())
+    P, nb = fx["block_size"], fx["num_blocks"]
+    hkv, d = fx["num_kv_heads"], fx["head_dim"]
+    kc = np.full((nb, P, hkv, d), np.nan)
+    vc = np.full((nb, P, hkv, d), np.nan)
+    for t, (page, slot) in enumerate(fx["token_pages"]):
+        kc[page, slot, 0] = fx["k_tokens"][t]
+        vc[page, slot, 0] = fx["v_tokens"][t]
+    q = np.asarray(fx["q"], dtype=np.float64)
+    bt = np.asarray(fx["block_tables"], dtype=np.int32)
+    cl = np.asarray(fx["context_lens"], dtype=np.int32)
+    for window, key in ((0, "window_0"), (2, "window_2")):
+        got = oracle.decode(q, kc, vc, bt, cl, fx["scale"], window)
+        np.testing.assert_allclose(got, np.asarray(fx["expected"][key]), rtol=0,
+                                   atol=fx["tolerance"], err_msg=key)
+
+
+# bfloat16 bit patterns and the values the format assigns them.
+BF16_VALUES = {0x3F80: 1.0, 0xC040: -3.0, 0x3F81: 1.0078125, 0x0001: 2.0 ** -133,
+               0x7F7F: 3.3895313892515355e38, 0x8000: -0.0, 0x4049: 3.140625,
+               0x3E80: 0.25, 0xBF00: -0.5}
+
+
+def pin_bf16_widening(oracle):
+    """One-token contexts return V exactly, so the row shows the oracle's
+    reading of each stored bf16 bit pattern."""
+    bits = list(BF16_VALUES)
+    d = len(bits)
+    v = np.asarray(bits, dtype=np.uint16).reshape(1, 1, d)
+    k = np.zeros((1, 1, d), dtype=np.uint16)
+    q = np.zeros((1, 1, d), dtype=np.uint16)
+    kc, vc, bt, cl = paginate([k], [v], 32, np.random.default_rng(27))
+    got = oracle.decode(q, kc, vc, bt, cl, 1.0, 0)[0, 0]
+    for j, b in enumerate(bits):
+        assert got[j] == BF16_VALUES[b], hex(b)
+
+
+def pin_empty_context_is_zero_row(oracle):
+    rng = np.random.default_rng(28)
+    q, dk, dv = _case(rng, [5], 2, 1, 8, "f64")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    bt2 = np.concatenate([bt, bt])
+    cl2 = np.asarray([0, 5], dtype=np.int32)
+    q2 = np.concatenate([q, q])
+    got = oracle.decode(q2, kc, vc, bt2, cl2, 0.3, 0)
+    assert np.array_equal(got[0], np.zeros((2, 8)))
+    assert np.array_equal(got[1], oracle.decode(q, kc, vc, bt, cl, 0.3, 0)[0])
+
+
+def pin_rejects_bad_inputs(oracle):
+    from oracle import OracleError
+    rng = np.random.default_rng(29)
+    q, dk, dv = _case(rng, [40], 2, 1, 8, "f64")
+    kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+    for bad_bt, bad_cl in ((bt, np.asarray([-1], np.int32)),
+                           (bt, np.asarray([bt.shape[1] * 32 + 1], np.int32)),
+                           (np.where(bt >= 0, kc.shape[0], bt).astype(np.int32), cl),
+                           (np.full_like(bt, -1), cl)):
+        try:
+            oracle.decode(q, kc, vc, bad_bt, bad_cl, 0.3, 0)
+        except OracleError:
+            continue
+        raise AssertionError("oracle accepted an invalid input")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
