@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode attention path on GB300.
+
+One step = one vt_paged_attn_decode call over one synthetic decode batch
+(request lookup, page gather, QK^T, mask, online softmax, PV, split partials,
+LSE combine, finalize: the whole hot path, one kernel launch).  Inputs sit in
+HBM before timing starts.  L2 is flushed (a 2x-L2 write) before every timed
+call, outside the call's CUDA events, so K/V come from HBM.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the reference arm: a deliberately plain fp64 program on host cores).
+Multi-GPU (torchrun, N > 1): every rank runs its own replica of the batch
+(independent decode problems, no collective on the data path); the reported
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "µs/call and achieved KV HBM GB/s (fraction of GB300 peak) per decode step"
+UNIT = "µs/call"
+DEFAULT_WORKLOAD = "qwen3_1p7b_b8_gqa2_d128"
+SWEEP = ["d256_gqa4_b16", "d256_gqa4_b16_w1024", "d256_gqa4_b16_f32", "large_gqa8_b64_d128",
+         "skewed_b128_gqa4_d128", "batch1_ctx32768_gqa4_d128"]
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "decode_d128_bf16.cu", "decode_d256_bf16.cu",
+                  "decode_d128_f32.cu", "decode_d256_f32.cu", "vt_paged_attn_api.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update((ROOT / "paged_attention_decode_kv_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    try:
+        data = json.loads(p.read_text())
+    except Exception:
+        return None
+    entry = data.get(workload)
+    if not entry or entry.get("kernel_hash") != kernel_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.1)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.06)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.file.flush()
+        rows = []
+        for line in Path(self.file.name).read_text().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, p in rows for k in range(4) if p[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def make_device_case(name: str, seed: int, device):
+    from paged_attention_decode_kv_gb300 import workloads as W
+    case = W.make_case(W.WORKLOADS[name], seed)
+    k, v = case.pool(device)
+    return case, {"q": case.q.to(device), "k": k, "v": v, "bt": case.block_tables.to(device),
+                  "cl": case.context_lens.to(device)}
+
+
+def time_calls(vt, case, t, steps, warmup, flush):
+    """Per-call CUDA-event times (s) on the launching stream, L2 flushed before each."""
+    import torch
+    w = case.workload
+    out = torch.empty_like(t["q"])
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        vt.decode(t["q"], t["k"], t["v"], t["bt"], t["cl"], w.scale, w.window, out=out)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for s in range(steps):
+        flush.zero_()
+        starts[s].record(stream)
+        vt.decode(t["q"], t["k"], t["v"], t["bt"], t["cl"], w.scale, w.window, out=out)
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    status = vt.vt_paged_attn_device_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after timed calls")
+    return [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
+
+
+def time_e2e(vt, case, t, steps, warmup, flush):
+    """Through the C-ABI with host buffers: pinned H2D of the step's inputs
+    (q, block table, context lengths), the decode, D2H of the output."""
+    import torch
+    w = case.workload
+    hq = case.q.pin_memory()
+    hbt = case.block_tables.pin_memory()
+    hcl = case.context_lens.pin_memory()
+    hout = torch.empty_like(case.q).pin_memory()
+    dq, dbt, dcl = torch.empty_like(t["q"]), torch.empty_like(t["bt"]), torch.empty_like(t["cl"])
+    out = torch.empty_like(t["q"])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dcl.copy_(hcl, non_blocking=True)
+        vt.decode(dq, t["k"], t["v"], dbt, dcl, w.scale, w.window, out=out)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for s in range(steps):
+        flush.zero_()
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hcl.numel() * 4
+    d2h = hout.numel() * hout.element_size()
+    return [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)], h2d, d2h
+
+
+def oracle_baseline(case, budget_s: float):
+    """The oracle, as it stands, on host cores: whole calls of this workload, or
+    a row sample of one call when a whole call exceeds the budget."""
+    import oracle
+    from paged_attention_decode_kv_gb300 import workloads as W
+    o = oracle.default_oracle()
+    w = case.workload
+    k, v, bt = case.compact()
+    args = (W.to_oracle_array(case.q), W.to_oracle_array(k), W.to_oracle_array(v), bt.numpy(),
+            case.context_lens.numpy(), w.scale, w.window)
+    rows_all = [(b, i) for b in range(w.num_seqs) for i in range(w.num_q_heads)]
+    t0 = time.perf_counter()
+    o.decode_rows(rows_all[:1], *args)
+    one_row = max(time.perf_counter() - t0, 1e-6)
+    if one_row * len(rows_all) <= budget_s:
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            o.decode_rows(rows_all, *args)
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or calls >= 1000:
+                break
+        return el / calls, f"{calls} whole calls ({len(rows_all)} rows each) of {w.name}, single thread"
+    # row sample, spread over the batch, then scaled by rows
+    import numpy as np
+    n = max(1, int(budget_s / one_row))
+    pick = np.linspace(0, len(rows_all) - 1, min(n, len(rows_all))).astype(int)
+    rows = [rows_all[p] for p in pick]
+    t0 = time.perf_counter()
+    o.decode_rows(rows, *args)
+    el = time.perf_counter() - t0
+    return el / len(rows) * len(rows_all), (f"{len(rows)} of {len(rows_all)} rows of one call of {w.name}, "
+                                            f"single thread, scaled to a whole call")
+
+
+def run_reference(args, rank, world):
+    from paged_attention_decode_kv_gb300 import workloads as W
+    if rank != 0:
+        return 0
+    case = W.make_case(W.WORKLOADS[args.workload], 0)
+    for _ in range(args.warmup):
+        oracle_baseline(case, 0.0)
+    times = []
+    sample = ""
+    for _ in range(args.steps):
+        t, sample = oracle_baseline(case, args.ref_budget)
+        times.append(t)
+    us = statistics.mean(times) * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "storage_dtype": case.workload.dtype},
+            "cpu_baseline": {"kind": "oracle", "value": us, "unit": UNIT, "cores": 1, "sample": sample},
+            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def summarize(times):
+    s = sorted(times)
+    return {"mean_us": statistics.mean(s) * 1e6, "median_us": s[len(s) // 2] * 1e6,
+            "p10_us": s[len(s) // 10] * 1e6, "p90_us": s[(9 * len(s)) // 10] * 1e6}
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import paged_attention_decode_kv_gb300 as vt
+    from paged_attention_decode_kv_gb300 import build_lib
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not build_lib.up_to_date():
+        build_lib.build()
+    if dist is not None:
+        dist.barrier()
+    vt.library()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20)
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    peak, peak_src = hbm_peak()
+
+    case, t = make_device_case(args.workload, args.seed + rank, dev)
+    w = case.workload
+    kv = case.kv_bytes()
+    algo = kv + case.qo_bytes()
+    context_tokens = int(case.context_lens.sum())
+
+    # timed region: barrier + synchronize on both sides, clocks sampled during it
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        times = time_calls(vt, case, t, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    plan = vt.vt_paged_attn_last_plan()
+    mean_s = statistics.mean(times)
+    if dist is not None:
+        tt = torch.tensor([mean_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_s = float(tt.item())
+    e2e_times, h2d, d2h = time_e2e(vt, case, t, max(50, args.steps // 10), args.warmup, flush)
+    e2e_s = statistics.mean(e2e_times)
+    if dist is not None:
+        tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+
+    host_case = case
+    del t
+    torch.cuda.empty_cache()
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        for name in SWEEP:
+            if name == args.workload:
+                continue
+            case_s, t_s = make_device_case(name, args.seed, dev)
+            ts = time_calls(vt, case_s, t_s, args.sweep_steps, 3, flush)
+            m = statistics.mean(ts)
+            a_bytes = case_s.kv_bytes() + case_s.qo_bytes()
+            sweep.append({"workload": name, **summarize(ts), "kv_gbs": case_s.kv_bytes() / m / 1e9,
+                          "achieved_gbs": a_bytes / m / 1e9, "frac": a_bytes / m / 1e9 / peak,
+                          "algorithmic_bytes": a_bytes, "plan": vt.vt_paged_attn_last_plan()})
+            del case_s, t_s
+            torch.cuda.empty_cache()
+
+    if rank != 0:
+        return 0
+    cpu_s, cpu_sample = oracle_baseline(host_case, args.ref_budget)
+    achieved = algo / mean_s / 1e9
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": mean_s * 1e6, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_s * 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "num_seqs": w.num_seqs,
+                   "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "storage_dtype": w.dtype, "window": w.window,
+                   "context_tokens": context_tokens,
+                   "l2": "flushed before every timed call (2x L2 write, outside the call's events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "per_call": summarize(times),
+        "kv_gbs": kv / mean_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "algorithmic_bytes_per_launch": algo, "peak_source": peak_src,
+                     "kernel": "vt::paged_decode_kernel"},
+        "cpu_baseline": {"value": cpu_s * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": cpu_sample},
+        "e2e": {"value": e2e_s * 1e6, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"]},
+        "plan": plan,
+        "kernel_hash": kernel_hash(),
+        "sweep": sweep,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--sweep-steps", type=int, default=300)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=10.0, help="seconds of oracle work per reference sample")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group(backend=backend)
+        dist = tdist
+    try:
+        if args.impl == "reference":
+            return run_reference(args, rank, world)
+        return run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

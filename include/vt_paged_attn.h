@@ -1,0 +1,151 @@
+/*
+ * vt_paged_attn -- single-token decode attention over a paged KV cache,
+ * hand-written for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (issue "ROCm gfx1200: PagedAttnOnline is 8.1x slower per call
+ * than vLLM's paged-attention kernel", section "Where to look"; PR
+ * "perf(cuda): head_dim-128 arm for the warp-split-KV decode kernel", commit
+ * message): every sequence b has one query row per query head; query head i
+ * attends, with a numerically stable softmax, over the keys and values of kv
+ * head h = i / (num_q_heads / num_kv_heads) for the tokens of its context,
+ * which live in 32-token pages named by the sequence's block-table row:
+ *
+ *   L = context_lens[b]; t0 = window > 0 ? max(0, L - window) : 0
+ *   s_t = scale * <q[b][i], k_cache[bt[b][t/32]][t%32][h]>      t0 <= t < L
+ *   out[b][i] = sum_t softmax(s)_t * v_cache[bt[b][t/32]][t%32][h]
+ *
+ * Storage is bf16 (or fp32); all arithmetic accumulates in fp32.  A context
+ * of 0 tokens produces a zero row.
+ *
+ * Threading / ordering: every call only enqueues work on `stream` and
+ * returns; it never synchronises the device.  The library keeps one
+ * split-KV workspace per device; calls that share a device must be ordered
+ * on the GPU (same stream, or streams ordered by events), otherwise they race
+ * on that workspace.
+ */
+#ifndef VT_PAGED_ATTN_H
+#define VT_PAGED_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VT_API __attribute__((visibility("default")))
+#else
+#define VT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as CUDA's cudaStream_t / CUstream (NULL = legacy default stream). */
+typedef struct CUstream_st* vt_stream_t;
+
+typedef enum {
+  VT_OK = 0,
+  VT_ERR_INVALID_ARG = 1,   /* an argument is out of range, NULL or misaligned */
+  VT_ERR_UNSUPPORTED = 2,   /* well-formed but not implemented (head_dim, block_size, group) */
+  VT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see vt_last_cuda_error() */
+  VT_ERR_OOM = 4,           /* the split workspace could not be allocated */
+  VT_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up a bounded wait (see vt_paged_attn_device_status) */
+} vt_status;
+
+typedef enum { VT_BF16 = 0, VT_F32 = 1 } vt_dtype;
+
+/*
+ * vt_paged_attn_decode -- the decode step.
+ *
+ * Device pointers (all caller-owned; nothing is retained after the call):
+ *   out          [num_seqs][num_q_heads][head_dim] dtype, written.  16-byte aligned.
+ *   q            [num_seqs][num_q_heads][head_dim] dtype.  16-byte aligned.
+ *   k_cache      [num_blocks][block_size][num_kv_heads][head_dim] dtype ("NHD"
+ *                pages, head_dim contiguous).  16-byte aligned.
+ *   v_cache      same layout as k_cache.  16-byte aligned.
+ *   block_tables [num_seqs][max_blocks_per_seq] int32 physical page ids; only
+ *                the first ceil(L_b / block_size) entries of row b are read,
+ *                and of those only pages that overlap the window.
+ *   context_lens [num_seqs] int32, 0 <= L_b <= max_blocks_per_seq * block_size.
+ * Sizes:
+ *   num_seqs >= 0 (0 is a no-op), num_q_heads % num_kv_heads == 0,
+ *   head_dim in {128, 256}, block_size == 32, scale finite (1/sqrt(head_dim)
+ *   is usual), window <= 0 for full context else the number of most recent
+ *   tokens attended (query token included).
+ * Forced additions to the classic signature:
+ *   max_blocks_per_seq  block-table row stride (entries) and per-row bound;
+ *   num_blocks          pool size in pages: extent of the cache tensors, and
+ *                       the bound every page id read is checked against;
+ *   dtype               storage type of q, k_cache, v_cache and out.
+ *
+ * Invalid data found on the device never faults: a context length outside
+ * [0, max_blocks_per_seq*block_size] or a page id outside [0, num_blocks)
+ * turns that sequence's (or that kv head's) output rows into NaN.
+ *
+ * Returns VT_OK once the work is enqueued; argument errors return before any
+ * launch; VT_ERR_CUDA reports a launch or runtime failure.
+ */
+VT_API vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, float scale, int window,
+                               vt_stream_t stream, int max_blocks_per_seq,
+                               int num_blocks, vt_dtype dtype);
+
+/* What the last successful vt_paged_attn_decode on this host thread launched. */
+typedef struct {
+  int grid_ctas;          /* CTAs launched (persistent, balanced split of the work) */
+  int ctas_per_sm;        /* resident CTAs per SM for this kernel variant */
+  int num_sms;            /* SMs of the device */
+  int consumer_warps;     /* compute warps per CTA (plus one TMA producer warp) */
+  int stages;             /* K/V page tiles in flight per CTA */
+  int group_tile;         /* query heads computed per kv head and CTA (padded) */
+  int subgroups;          /* ceil(group / group_tile) */
+  int min_units_per_cta;  /* lower bound on (page, kv head) tiles per CTA */
+  int head_dim;
+  int dtype;              /* vt_dtype */
+  size_t smem_bytes;      /* dynamic shared memory per CTA */
+  size_t workspace_bytes; /* split-KV workspace used (partials + arrival counters) */
+} vt_plan;
+
+VT_API vt_status vt_paged_attn_last_plan(vt_plan* plan);
+
+/*
+ * Test / benchmark override of the launch plan for this host thread, read on
+ * every call.  grid_ctas > 0 forces the number of CTAs (so tests can force
+ * every sequence to be split, or never split); min_units_per_cta > 0 replaces
+ * the default lower bound on work per CTA.  0 restores the automatic choice.
+ */
+VT_API vt_status vt_paged_attn_set_override(int grid_ctas, int min_units_per_cta);
+
+/*
+ * Reads and clears the device status word that kernels set when a bounded
+ * wait gives up (bit 0: page tile never arrived, bit 1: stage never released,
+ * bit 2: consumer-warp rendezvous, bit 3: drain of copies in flight).
+ * Synchronises `stream` first.  *status is 0 when all is well; the call
+ * returns VT_ERR_DEVICE_TIMEOUT if it was not.  Clearing also resets the
+ * split workspace's arrival counters.
+ */
+VT_API vt_status vt_paged_attn_device_status(vt_stream_t stream, unsigned* status);
+
+/* Bytes of split-KV workspace a call with these sizes uses on the current device. */
+VT_API size_t vt_paged_attn_workspace_bytes(int num_seqs, int num_q_heads,
+                                     int num_kv_heads, int head_dim,
+                                     vt_dtype dtype);
+
+/* Frees the library's per-device workspaces.  No call may be in flight. */
+VT_API void vt_paged_attn_release(void);
+
+VT_API const char* vt_status_string(vt_status status);
+
+/* Text of the last CUDA error seen by this host thread ("" if none). */
+VT_API const char* vt_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+VT_API int vt_paged_attn_version(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* VT_PAGED_ATTN_H */

@@ -1,0 +1,192 @@
+"""GB300-native paged decode attention: Python binding of libvt_paged_attn.
+
+The library (``_build/libvt_paged_attn.so``, built by ``build_lib.py``) does
+every step of the decode on the GPU; this module only marshals arguments
+through ctypes.  Functions named ``vt_*`` mirror the C entry points of
+``include/vt_paged_attn.h`` one to one (pointers as Python ints); ``decode``
+is a convenience wrapper that takes torch CUDA tensors.  There is no CPU
+fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+LIBRARY_PATH = Path(__file__).resolve().parent / "_build" / "libvt_paged_attn.so"
+
+VT_OK, VT_ERR_INVALID_ARG, VT_ERR_UNSUPPORTED, VT_ERR_CUDA, VT_ERR_OOM, VT_ERR_DEVICE_TIMEOUT = range(6)
+VT_BF16, VT_F32 = 0, 1
+BLOCK_SIZE = 32
+
+EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_last_plan", "vt_paged_attn_set_override",
+            "vt_paged_attn_device_status", "vt_paged_attn_workspace_bytes", "vt_paged_attn_release",
+            "vt_status_string", "vt_last_cuda_error", "vt_paged_attn_version")
+
+
+class VtError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: status {status}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+class vt_plan(ctypes.Structure):
+    _fields_ = [("grid_ctas", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("num_sms", ctypes.c_int),
+                ("consumer_warps", ctypes.c_int), ("stages", ctypes.c_int), ("group_tile", ctypes.c_int),
+                ("subgroups", ctypes.c_int), ("min_units_per_cta", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not LIBRARY_PATH.exists():
+                raise RuntimeError(
+                    f"{LIBRARY_PATH} is missing: build it with "
+                    "`python -m paged_attention_decode_kv_gb300.build_lib` (needs nvcc)")
+            lib = ctypes.CDLL(str(LIBRARY_PATH))
+            c_int, c_void, c_float, c_size = ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+            lib.vt_paged_attn_decode.argtypes = [c_void] * 6 + [c_int] * 5 + [c_float, c_int, c_void, c_int,
+                                                                               c_int, c_int]
+            lib.vt_paged_attn_decode.restype = c_int
+            lib.vt_paged_attn_last_plan.argtypes = [ctypes.POINTER(vt_plan)]
+            lib.vt_paged_attn_last_plan.restype = c_int
+            lib.vt_paged_attn_set_override.argtypes = [c_int, c_int]
+            lib.vt_paged_attn_set_override.restype = c_int
+            lib.vt_paged_attn_device_status.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint)]
+            lib.vt_paged_attn_device_status.restype = c_int
+            lib.vt_paged_attn_workspace_bytes.argtypes = [c_int] * 5
+            lib.vt_paged_attn_workspace_bytes.restype = c_size
+            lib.vt_paged_attn_release.argtypes = []
+            lib.vt_paged_attn_release.restype = None
+            lib.vt_status_string.argtypes = [c_int]
+            lib.vt_status_string.restype = ctypes.c_char_p
+            lib.vt_last_cuda_error.argtypes = []
+            lib.vt_last_cuda_error.restype = ctypes.c_char_p
+            lib.vt_paged_attn_version.argtypes = []
+            lib.vt_paged_attn_version.restype = c_int
+            _lib = lib
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != VT_OK:
+        lib = library()
+        detail = lib.vt_status_string(status).decode()
+        cuda = lib.vt_last_cuda_error().decode()
+        if cuda:
+            detail += f"; {cuda}"
+        raise VtError(status, where, detail)
+
+
+# ---- C entry points, same names -------------------------------------------
+def vt_paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                         num_kv_heads, head_dim, block_size, scale, window, stream, max_blocks_per_seq,
+                         num_blocks, dtype) -> int:
+    """Raw call: pointers and the stream handle are ints; returns the status code."""
+    return library().vt_paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                          num_q_heads, num_kv_heads, head_dim, block_size, float(scale),
+                                          int(window), stream, max_blocks_per_seq, num_blocks, dtype)
+
+
+def vt_paged_attn_last_plan() -> dict:
+    p = vt_plan()
+    _check(library().vt_paged_attn_last_plan(ctypes.byref(p)), "vt_paged_attn_last_plan")
+    return p.as_dict()
+
+
+def vt_paged_attn_set_override(grid_ctas: int = 0, min_units_per_cta: int = 0) -> None:
+    _check(library().vt_paged_attn_set_override(grid_ctas, min_units_per_cta), "vt_paged_attn_set_override")
+
+
+def vt_paged_attn_device_status(stream=None) -> int:
+    """Status word of bounded waits that gave up (0 = none); clears it."""
+    word = ctypes.c_uint(0)
+    library().vt_paged_attn_device_status(_stream_handle(stream), ctypes.byref(word))
+    return int(word.value)
+
+
+def vt_paged_attn_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, dtype) -> int:
+    return int(library().vt_paged_attn_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, dtype))
+
+
+def vt_paged_attn_release() -> None:
+    library().vt_paged_attn_release()
+
+
+def vt_status_string(status: int) -> str:
+    return library().vt_status_string(status).decode()
+
+
+def vt_paged_attn_version() -> int:
+    return int(library().vt_paged_attn_version())
+
+
+# ---- torch convenience -------------------------------------------------------
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return VT_BF16
+    if t.dtype == torch.float32:
+        return VT_F32
+    raise TypeError(f"storage dtype must be bfloat16 or float32, got {t.dtype}")
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, window: int = 0, out=None,
+           stream=None):
+    """Decode attention for torch CUDA tensors.
+
+    q [B][Hq][D]; k_cache, v_cache [num_blocks][32][Hkv][D]; block_tables
+    [B][max_blocks] int32; context_lens [B] int32.  Returns out [B][Hq][D]
+    (allocated unless given).  Asynchronous on ``stream`` (default: current).
+    """
+    import torch
+    B, Hq, D = q.shape
+    nb, P, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks][32][Hkv][head_dim] matching q")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
+                    ("context_lens", context_lens)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+    if scale is None:
+        scale = D ** -0.5
+    st = vt_paged_attn_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                              block_tables.data_ptr(), context_lens.data_ptr(), B, Hq, Hkv, D, P, scale,
+                              window, _stream_handle(stream), block_tables.shape[1], nb, dtype_code(q))
+    _check(st, "vt_paged_attn_decode")
+    return out

@@ -1,0 +1,94 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+entry point the header declares, and rejects bad arguments on the host before
+touching CUDA."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import paged_attention_decode_kv_gb300 as vt
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "vt_paged_attn.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_attention_decode_kv_gb300 import build_lib
+    build_lib.build()
+    return vt.library()
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"VT_API\s+[\w\s\*]+?\b(vt_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(vt.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_version_and_status_strings(lib):
+    assert vt.vt_paged_attn_version() == 10000
+    assert vt.vt_status_string(vt.VT_OK) == "ok"
+    assert "unsupported" in vt.vt_status_string(vt.VT_ERR_UNSUPPORTED)
+    assert vt.vt_status_string(99) == "unknown status"
+
+
+def _call(**over):
+    args = dict(out=0x1000, q=0x2000, k_cache=0x3000, v_cache=0x4000, block_tables=0x5000,
+                context_lens=0x6000, num_seqs=2, num_q_heads=16, num_kv_heads=8, head_dim=128,
+                block_size=32, scale=0.088, window=0, stream=None, max_blocks_per_seq=4, num_blocks=16,
+                dtype=vt.VT_BF16)
+    args.update(over)
+    return vt.vt_paged_attn_decode(**args)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(num_seqs=0, out=None, q=None), vt.VT_OK),           # empty batch: no-op, no launch
+    (dict(num_seqs=-1), vt.VT_ERR_INVALID_ARG),
+    (dict(out=None), vt.VT_ERR_INVALID_ARG),
+    (dict(k_cache=None), vt.VT_ERR_INVALID_ARG),
+    (dict(block_tables=None), vt.VT_ERR_INVALID_ARG),
+    (dict(q=0x2008), vt.VT_ERR_INVALID_ARG),                  # 16-byte alignment
+    (dict(context_lens=0x6002), vt.VT_ERR_INVALID_ARG),       # 4-byte alignment
+    (dict(num_q_heads=12, num_kv_heads=8), vt.VT_ERR_INVALID_ARG),
+    (dict(num_kv_heads=0), vt.VT_ERR_INVALID_ARG),
+    (dict(head_dim=64), vt.VT_ERR_UNSUPPORTED),
+    (dict(head_dim=512), vt.VT_ERR_UNSUPPORTED),
+    (dict(block_size=16), vt.VT_ERR_UNSUPPORTED),
+    (dict(max_blocks_per_seq=0), vt.VT_ERR_INVALID_ARG),
+    (dict(num_blocks=0), vt.VT_ERR_INVALID_ARG),
+    (dict(num_blocks=1 << 27), vt.VT_ERR_UNSUPPORTED),        # token rows must fit int32
+    (dict(scale=float("nan")), vt.VT_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), vt.VT_ERR_INVALID_ARG),
+    (dict(dtype=7), vt.VT_ERR_INVALID_ARG),
+])
+def test_host_validation(lib, over, status):
+    assert _call(**over) == status
+
+
+def test_override_validation(lib):
+    assert lib.vt_paged_attn_set_override(-1, 0) == vt.VT_ERR_INVALID_ARG
+    assert lib.vt_paged_attn_set_override(0, -5) == vt.VT_ERR_INVALID_ARG
+    assert lib.vt_paged_attn_set_override(0, 0) == vt.VT_OK
+
+
+def test_last_plan_before_any_launch(lib):
+    p = vt.vt_plan()
+    assert lib.vt_paged_attn_last_plan(None) == vt.VT_ERR_INVALID_ARG
+    # this host thread has launched nothing
+    assert lib.vt_paged_attn_last_plan(ctypes.byref(p)) == vt.VT_ERR_INVALID_ARG
+
+
+def test_workspace_bytes_rejects_bad_shapes(lib):
+    assert vt.vt_paged_attn_workspace_bytes(0, 16, 8, 128, vt.VT_BF16) == 0
+    assert vt.vt_paged_attn_workspace_bytes(4, 12, 8, 128, vt.VT_BF16) == 0
+    assert vt.vt_paged_attn_workspace_bytes(4, 16, 8, 64, vt.VT_BF16) == 0

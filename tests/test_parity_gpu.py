@@ -1,0 +1,234 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C-ABI.
+
+Tolerances (fixed by the decode PR's CPU-oracle gate and the workload spec):
+bf16 storage: NMSE <= 5e-4 over the call's outputs and max |err| <= 2e-2;
+fp32 storage: max |err| <= 1e-5.  NMSE = sum (gpu - ref)^2 / sum ref^2.
+
+These tests fail (never skip) when no GPU or no library is present: a GPU
+job that cannot run them must not look green.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import paged_attention_decode_kv_gb300 as vt
+from paged_attention_decode_kv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+BF16_NMSE, BF16_MAXABS, F32_MAXABS = 5e-4, 2e-2, 1e-5
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from paged_attention_decode_kv_gb300 import build_lib
+    build_lib.build()
+    vt.library()
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _reset_override():
+    yield
+    if vt._lib is not None:
+        vt.vt_paged_attn_set_override(0, 0)
+
+
+def gpu_run(case, dev, grid=0, min_units=0, window=None, tables=None, lens=None, stream=None):
+    w = case.workload
+    k, v = case.pool(dev)
+    q = case.q.to(dev)
+    bt = (case.block_tables if tables is None else tables).to(dev)
+    cl = (case.context_lens if lens is None else lens).to(dev)
+    vt.vt_paged_attn_set_override(grid, min_units)
+    out = vt.decode(q, k, v, bt, cl, w.scale, w.window if window is None else window, stream=stream)
+    plan = vt.vt_paged_attn_last_plan()
+    vt.vt_paged_attn_set_override(0, 0)
+    torch.cuda.synchronize()
+    assert vt.vt_paged_attn_device_status() == 0
+    return out.cpu(), plan
+
+
+def oracle_rows(case, rows=None, window=None, lens=None):
+    import oracle
+    o = oracle.default_oracle()
+    w = case.workload
+    k, v, bt = case.compact()
+    cl = case.context_lens if lens is None else lens
+    args = (W.to_oracle_array(case.q), W.to_oracle_array(k), W.to_oracle_array(v), bt.numpy(), cl.numpy(),
+            w.scale, w.window if window is None else window)
+    if rows is None:
+        rows = [(b, i) for b in range(w.num_seqs) for i in range(w.num_q_heads)]
+    return np.asarray(rows), o.decode_rows(rows, *args, threads=THREADS)
+
+
+def compare(got, ref, dtype, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = got - ref
+    maxabs = float(np.abs(err).max()) if err.size else 0.0
+    if dtype == torch.float32:
+        assert maxabs <= F32_MAXABS, f"{what}: fp32 max|err| {maxabs:.3e}"
+        return maxabs, 0.0
+    nmse = float((err ** 2).sum() / max((ref ** 2).sum(), 1e-300))
+    assert nmse <= BF16_NMSE and maxabs <= BF16_MAXABS, f"{what}: nmse {nmse:.3e} max|err| {maxabs:.3e}"
+    return maxabs, nmse
+
+
+def check_case(case, dev, rows=None, **kw):
+    out, plan = gpu_run(case, dev, **kw)
+    idx, ref = oracle_rows(case, rows, window=kw.get("window"))
+    got = out[idx[:, 0], idx[:, 1]].to(torch.float64).numpy()
+    return compare(got, ref, case.q.dtype, case.workload.name), plan
+
+
+# ---------------------------------------------------------------------------
+SMALL = [W.TINY, W.QWEN3_1P7B, W.D256_GQA4, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D256_GQA4_F32_W1024]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_workload_all_rows(dev, w, seed):
+    """Every output row of the small and medium workloads, default launch plan."""
+    check_case(W.make_case(w, seed), dev)
+
+
+def _sample_rows(case, n_seqs=6):
+    """All heads of the longest, the shortest and a few other sequences."""
+    L = case.context_lens.numpy()
+    order = np.argsort(L)
+    pick = {int(order[0]), int(order[-1]), int(order[len(order) // 2])}
+    rng = np.random.default_rng(case.seed)
+    pick |= set(int(x) for x in rng.choice(len(L), size=min(n_seqs, len(L)), replace=False))
+    return [(b, i) for b in sorted(pick) for i in range(case.workload.num_q_heads)]
+
+
+@pytest.mark.parametrize("w", [W.LARGE_GQA, W.SKEWED, W.BATCH1_LONG], ids=lambda w: w.name)
+def test_workload_full_size_sampled(dev, w):
+    """Full-size workloads in the benchmark's launch plan; the oracle checks all
+    heads of sampled sequences (always the longest and the shortest)."""
+    case = W.make_case(w, 0)
+    check_case(case, dev, rows=_sample_rows(case))
+
+
+@pytest.mark.parametrize("grid", [1, 2, 3, 7, 64, 152, 500, 1500])
+@pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_W1024, W.D256_GQA4_F32], ids=lambda w: w.name)
+def test_forced_partitions(dev, w, grid):
+    """The split/no-split paths and the combine: any CTA count (with at least
+    one tile per CTA) gives the oracle's result."""
+    (_, _), plan = check_case(W.make_case(w, 4), dev, grid=grid, min_units=1)
+    assert plan["grid_ctas"] == grid
+
+
+STRADDLE = (1, 31, 32, 33, 64, 100, 685, 1000)
+
+
+@pytest.mark.parametrize("ctx", STRADDLE)
+def test_page_boundary_contexts(dev, ctx):
+    """Contexts straddling the 32-token page, at the Qwen3 geometry (16 q / 8 kv
+    heads, head_dim 128: 2048 outputs), split and unsplit."""
+    case = W.make_case(W.custom(f"straddle{ctx}", [ctx], 16, 8, 128), 7)
+    check_case(case, dev)
+    check_case(case, dev, grid=max(2, ctx // 16), min_units=1)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4), (16, 4), (20, 4), (32, 4), (48, 4), (64, 4), (6, 2)])
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (128, "f32")])
+def test_group_sizes(dev, hq, hkv, d, dtype):
+    """GQA groups 1..16 including ones that pad the group tile (3, 5) or need
+    several query subgroups per kv head (12, 16)."""
+    case = W.make_case(W.custom(f"g{hq // hkv}", [1, 40, 97, 300], hq, hkv, d, dtype=dtype), 8)
+    check_case(case, dev)
+    check_case(case, dev, grid=5, min_units=1)
+
+
+@pytest.mark.parametrize("window", [1, 2, 31, 32, 33, 64, 299, 300, 301, 5000])
+def test_windows(dev, window):
+    case = W.make_case(W.custom("win", [1, 33, 300, 1000], 16, 4, 128), 9)
+    check_case(case, dev, window=window)
+    check_case(case, dev, window=window, grid=11, min_units=1)
+
+
+def test_empty_contexts_give_zero_rows(dev):
+    case = W.make_case(W.custom("empty", [0, 5, 0, 70, 0], 8, 2, 128), 10)
+    out, _ = gpu_run(case, dev)
+    for b in (0, 2, 4):
+        assert torch.count_nonzero(out[b]) == 0
+    idx, ref = oracle_rows(case, [(b, i) for b in (1, 3) for i in range(8)])
+    compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16)
+    allempty = W.make_case(W.custom("allempty", [0, 0], 8, 2, 256), 10)
+    out, _ = gpu_run(allempty, dev)
+    assert torch.count_nonzero(out) == 0
+
+
+def test_invalid_device_data_poisons_only_its_rows(dev):
+    """A page id outside the pool or an impossible context length turns only the
+    affected rows into NaN; nothing faults and other sequences are exact."""
+    case = W.make_case(W.custom("bad", [40, 70, 33, 100], 8, 2, 128), 11)
+    bt = case.block_tables.clone()
+    lens = case.context_lens.clone()
+    bt[1, 1] = case.num_blocks + 5        # sequence 1: page id past the pool
+    bt[2, 0] = -3                         # sequence 2: negative page id
+    lens[3] = case.workload.max_blocks_per_seq * 32 + 1  # sequence 3: longer than its table row
+    for grid in (0, 3):
+        out, _ = gpu_run(case, dev, tables=bt, lens=lens, grid=grid, min_units=1)
+        assert torch.isnan(out[1].float()).all() and torch.isnan(out[2].float()).all()
+        assert torch.isnan(out[3].float()).all()
+        idx, ref = oracle_rows(case, [(0, i) for i in range(8)])
+        compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16)
+    neg = case.context_lens.clone()
+    neg[0] = -1
+    out, _ = gpu_run(case, dev, lens=neg)
+    assert torch.isnan(out[0].float()).all()
+
+
+def test_deterministic_bits(dev):
+    case = W.make_case(W.QWEN3_1P7B, 12)
+    a, _ = gpu_run(case, dev, grid=40, min_units=1)
+    b, _ = gpu_run(case, dev, grid=40, min_units=1)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_default_plan(dev):
+    case = W.make_case(W.QWEN3_1P7B, 0)
+    _, plan = gpu_run(case, dev)
+    props = torch.cuda.get_device_properties(0)
+    assert plan["num_sms"] == props.multi_processor_count
+    assert plan["grid_ctas"] == plan["num_sms"] * plan["ctas_per_sm"]
+    assert plan["stages"] >= 2 and plan["group_tile"] == 2 and plan["subgroups"] == 1
+    assert plan["workspace_bytes"] > 0
+
+
+def test_side_stream_and_reuse(dev):
+    """Calls on a non-default stream, back to back with different shapes, share
+    the library workspace correctly."""
+    s = torch.cuda.Stream()
+    cases = [W.make_case(W.QWEN3_1P7B, 13), W.make_case(W.D256_GQA4, 13),
+             W.make_case(W.custom("many", [3] * 300, 8, 8, 128), 13)]
+    with torch.cuda.stream(s):
+        for case in cases:
+            out, _ = gpu_run(case, dev, stream=s, grid=97, min_units=1)
+            idx, ref = oracle_rows(case)
+            compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, case.q.dtype, case.workload.name)
+
+
+def test_scale_zero_gives_mean_of_values(dev):
+    case = W.make_case(W.custom("scale0", [77], 4, 2, 128), 14)
+    k, v = case.pool(dev)
+    out = vt.decode(case.q.to(dev), k, v, case.block_tables.to(dev), case.context_lens.to(dev), scale=0.0)
+    idx = torch.tensor([case.block_tables[0, t // 32] for t in range(77)])
+    vv = v[idx.to(dev), torch.arange(77, device=dev) % 32].double()  # [77][Hkv][D]
+    mean = vv.mean(0)
+    for i in range(4):
+        assert (out[0, i].double() - mean[i // 2]).abs().max() < 2e-2
+
+
+def test_device_status_clean(dev):
+    assert vt.vt_paged_attn_device_status() == 0
