@@ -253,6 +253,16 @@ def run_reference(args, rank, world):
     return 0
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def summarize(times):
     s = sorted(times)
     return {"mean_us": statistics.mean(s) * 1e6, "median_us": s[len(s) // 2] * 1e6,
@@ -292,17 +302,9 @@ def run_ours(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     plan = vt.vt_paged_attn_last_plan()
-    mean_s = statistics.mean(times)
-    if dist is not None:
-        tt = torch.tensor([mean_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_s = float(tt.item())
+    mean_s = max_over_ranks(statistics.mean(times), dist, dev)
     e2e_times, h2d, d2h = time_e2e(vt, case, t, max(50, args.steps // 10), args.warmup, flush)
-    e2e_s = statistics.mean(e2e_times)
-    if dist is not None:
-        tt = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(statistics.mean(e2e_times), dist, dev)
 
     host_case = case
     del t

@@ -121,12 +121,22 @@ VT_API vt_status vt_paged_attn_set_override(int grid_ctas, int min_units_per_cta
 /*
  * Reads and clears the device status word that kernels set when a bounded
  * wait gives up (bit 0: page tile never arrived, bit 1: stage never released,
- * bit 2: consumer-warp rendezvous, bit 3: drain of copies in flight).
+ * bit 2: consumer-warp rendezvous, bit 3: drain of copies in flight) or a
+ * self-check fails (bit 4: a CTA's tile walk did not match its share).
  * Synchronises `stream` first.  *status is 0 when all is well; the call
  * returns VT_ERR_DEVICE_TIMEOUT if it was not.  Clearing also resets the
  * split workspace's arrival counters.
  */
 VT_API vt_status vt_paged_attn_device_status(vt_stream_t stream, unsigned* status);
+
+/*
+ * Copies the first n_words (<= 8) words of the device status area without
+ * clearing them: [0] status bits as above; [1] 1 + index of the CTA whose
+ * wait gave up first (0: none); [2] its status bit | (thread index << 8);
+ * [3] shared-memory address of the barrier it waited on; [4] the phase
+ * parity it waited for.  Synchronises `stream` first.
+ */
+VT_API vt_status vt_paged_attn_device_status_detail(vt_stream_t stream, unsigned* words, int n_words);
 
 /* Bytes of split-KV workspace a call with these sizes uses on the current device. */
 VT_API size_t vt_paged_attn_workspace_bytes(int num_seqs, int num_q_heads,

@@ -20,7 +20,7 @@ VT_BF16, VT_F32 = 0, 1
 BLOCK_SIZE = 32
 
 EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_last_plan", "vt_paged_attn_set_override",
-            "vt_paged_attn_device_status", "vt_paged_attn_workspace_bytes", "vt_paged_attn_release",
+            "vt_paged_attn_device_status", "vt_paged_attn_device_status_detail", "vt_paged_attn_workspace_bytes", "vt_paged_attn_release",
             "vt_status_string", "vt_last_cuda_error", "vt_paged_attn_version")
 
 
@@ -70,6 +70,8 @@ def library() -> ctypes.CDLL:
             lib.vt_paged_attn_set_override.restype = c_int
             lib.vt_paged_attn_device_status.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint)]
             lib.vt_paged_attn_device_status.restype = c_int
+            lib.vt_paged_attn_device_status_detail.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint), c_int]
+            lib.vt_paged_attn_device_status_detail.restype = c_int
             lib.vt_paged_attn_workspace_bytes.argtypes = [c_int] * 5
             lib.vt_paged_attn_workspace_bytes.restype = c_size
             lib.vt_paged_attn_release.argtypes = []
@@ -119,6 +121,16 @@ def vt_paged_attn_device_status(stream=None) -> int:
     word = ctypes.c_uint(0)
     library().vt_paged_attn_device_status(_stream_handle(stream), ctypes.byref(word))
     return int(word.value)
+
+
+def vt_paged_attn_device_status_detail(stream=None, n_words: int = 5) -> list:
+    """First n_words of the device status area (not cleared): status bits, then
+    where the first bounded wait that gave up was (1 + CTA, bit | thread << 8,
+    barrier address, parity)."""
+    words = (ctypes.c_uint * n_words)()
+    _check(library().vt_paged_attn_device_status_detail(_stream_handle(stream), words, n_words),
+           "vt_paged_attn_device_status_detail")
+    return [int(x) for x in words]
 
 
 def vt_paged_attn_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, dtype) -> int:

@@ -53,7 +53,7 @@ constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drained
 enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8 };
 
 // Status bits (global status word).
-enum : unsigned { kStatusFull = 1u, kStatusEmpty = 2u, kStatusSync = 4u, kStatusDrain = 8u };
+enum : unsigned { kStatusFull = 1u, kStatusEmpty = 2u, kStatusSync = 4u, kStatusDrain = 8u, kStatusWalk = 16u };
 
 struct DecodeArgs {
   void* out;
@@ -188,6 +188,12 @@ __device__ __forceinline__ bool wait_phase(unsigned long long* bar, uint32_t par
     if (global_ns() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(status, code);
+      // first give-up in the grid: record where (status[1..4])
+      if (atomicCAS(status + 1, 0u, 1u + blockIdx.x) == 0u) {
+        status[2] = code | (threadIdx.x << 8);
+        status[3] = static_cast<unsigned>(smem_addr(bar));
+        status[4] = parity;
+      }
       return false;
     }
   }
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     long long u = u0, cum = s.cum_start;
     int b = s.b_start;
     // window of 32 context lengths cached across the warp
-    int win_base = -1, win_len = 0;
+    int win_base = -(1 << 30), win_len = 0;  // nothing cached yet
     auto length_of = [&](int bb) -> int {
       if (bb < win_base || bb >= win_base + 32) {
         win_base = bb;
@@ -503,6 +509,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         ++b;
       } while (ok && u < u1 && b < a.num_seqs && seq_span(length_of(b), a.window, a.max_blocks).np == 0);
       if (b >= a.num_seqs) break;
+    }
+    // Self-check: the walk must have produced exactly this CTA's tiles.
+    if (ok && issued != u1 - u0 && lane == 0) {
+      atomicOr(a.status, kStatusWalk);
+      s.abort_flag = 1;
     }
     // Let every copy this warp issued land before the CTA can exit.
     if (lane == 0) {

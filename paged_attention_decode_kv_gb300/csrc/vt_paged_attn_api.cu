@@ -410,6 +410,23 @@ vt_status vt_paged_attn_device_status(vt_stream_t stream_handle, unsigned* statu
   return VT_ERR_DEVICE_TIMEOUT;
 }
 
+vt_status vt_paged_attn_device_status_detail(vt_stream_t stream_handle, unsigned* words, int n_words) {
+  if (!words || n_words < 0 || n_words > 8) return VT_ERR_INVALID_ARG;
+  for (int k = 0; k < n_words; ++k) words[k] = 0;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& ds = device_state(dev);
+  if (!ds.ws || n_words == 0) return VT_OK;
+  e = cudaMemcpy(words, ds.ws, sizeof(unsigned) * n_words, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  return VT_OK;
+}
+
 void vt_paged_attn_release(void) {
   std::lock_guard<std::mutex> lock(g_mutex);
   int cur = 0;
