@@ -98,6 +98,7 @@ typedef struct {
   int ctas_per_sm;        /* resident CTAs per SM for this kernel variant */
   int num_sms;            /* SMs of the device */
   int consumer_warps;     /* compute warps per CTA (plus one TMA producer warp) */
+  int tensor_cores;       /* 1: QK^T and PV on tensor cores (bf16), 0: CUDA cores (fp32) */
   int stages;             /* K/V page tiles in flight per CTA */
   int group_tile;         /* query heads computed per kv head and CTA (padded) */
   int subgroups;          /* ceil(group / group_tile) */

@@ -35,7 +35,7 @@ class VtError(RuntimeError):
 
 class vt_plan(ctypes.Structure):
     _fields_ = [("grid_ctas", ctypes.c_int), ("ctas_per_sm", ctypes.c_int), ("num_sms", ctypes.c_int),
-                ("consumer_warps", ctypes.c_int), ("stages", ctypes.c_int), ("group_tile", ctypes.c_int),
+                ("consumer_warps", ctypes.c_int), ("tensor_cores", ctypes.c_int), ("stages", ctypes.c_int), ("group_tile", ctypes.c_int),
                 ("subgroups", ctypes.c_int), ("min_units_per_cta", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
                 ("workspace_bytes", ctypes.c_size_t)]

@@ -1,14 +1,15 @@
-// Decode kernel variants for head_dim 256, f32 storage: group tiles 1, 2, 4, 8.
+// Decode kernel variants for head_dim 256, f32 storage, CUDA-core consumer:
+// group tiles 1, 2, 4, 8.
 #include "kernel_variants.cuh"
 
 namespace vt {
 
 const VariantInfo* variants_d256_f32(int* count) {
   static const VariantInfo table[] = {
-      Variant<256, float, 1, 8, 1, 4>::info(),
-      Variant<256, float, 2, 8, 1, 4>::info(),
-      Variant<256, float, 4, 8, 1, 4>::info(),
-      Variant<256, float, 8, 8, 1, 4>::info(),
+      Variant<256, float, 1, 8, 1, 4, Math::kSimt>::info(),
+      Variant<256, float, 2, 8, 1, 4, Math::kSimt>::info(),
+      Variant<256, float, 4, 8, 1, 4, Math::kSimt>::info(),
+      Variant<256, float, 8, 8, 1, 4, Math::kSimt>::info(),
   };
   *count = 4;
   return table;

@@ -8,17 +8,21 @@
 //                        balanced without any host-side knowledge of lengths;
 //   S2  page gather      a producer warp streams each K and V page tile
 //                        (32 tokens x head_dim, NHD, row stride Hkv*head_dim)
-//                        with one 3-D TMA copy each into a ring of
-//                        shared-memory stages guarded by mbarriers;
-//   S3  QK^T (GQA)       consumer warps hold the g query rows that share the
-//                        kv head in registers, so every K/V byte is read from
-//                        HBM once per kv head;
+//                        with 3-D TMA copies into a ring of shared-memory
+//                        stages guarded by mbarriers;
+//   S3  QK^T (GQA)       the g query rows that share a kv head are computed
+//                        together, so every K/V byte is read from HBM once
+//                        per kv head.  bf16 storage: tensor cores
+//                        (mma.sync m16n8k16, queries as the M dimension);
+//                        fp32 storage: CUDA-core FMAs;
 //   S4  mask             tail slots past the context and tokens before the
 //                        window are excluded; pages wholly outside the window
 //                        are never loaded;
 //   S5  online softmax   per query row, base-2 exponentials on pre-scaled
 //                        scores, warp-shuffle reductions;
-//   S6  PV               fp32 accumulation of p * v;
+//   S6  PV               fp32 accumulation of p * v (tensor cores for bf16,
+//                        with p split into two bf16 terms, hi + lo, so the
+//                        weights keep ~16 significant bits);
 //   S7  split partials   a (sequence, kv head) whose tiles span several CTAs
 //                        leaves one normalised partial (o, m, l) per CTA;
 //   S8  LSE combine      the last CTA to finish such an item merges the
@@ -45,7 +49,7 @@
 namespace vt {
 
 constexpr int kPageTokens = 32;  // tokens per KV page (block_size)
-constexpr int kLaneElems = 8;    // head_dim elements each lane owns per row
+constexpr int kSwizzleCols = 64; // bf16 columns per 128-byte swizzled sub-tile row
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drained copy
 
@@ -73,7 +77,7 @@ struct DecodeArgs {
   int* counters;    // [num_seqs * num_kv_heads * subgroups] arrival counters, zero between calls
   float* part_ml;   // [2 * grid][G][2]  (m, l) of each partial, log2 domain
   float* part_o;    // [2 * grid][G][D]  normalised partial rows
-  unsigned* status; // status word
+  unsigned* status; // status words
 };
 
 struct StageHeader {
@@ -87,26 +91,38 @@ struct StageHeader {
   long long item_u;  // first tile index of the (sequence, virtual head)
 };
 
-template <int D, typename T, int G, int NCW, int NSTAGE>
+// Consumer kinds.
+enum class Math { kSimt, kMma };
+
+template <int D, typename T, int G, int NCW, int NSTAGE, Math M>
 struct Smem {
-  static constexpr int GS = D / kLaneElems;       // lanes per row group
-  static constexpr int NG = NCW * 32 / GS;        // row groups per CTA
-  static constexpr int TPG = kPageTokens / NG;    // tokens per group per page
-  alignas(128) T k[NSTAGE][kPageTokens * D];
-  alignas(128) T v[NSTAGE][kPageTokens * D];
+  // CUDA-core layout: lane c of a row group owns 8 elements of every row.
+  static constexpr int GS = D / 8;
+  static constexpr int NG = (M == Math::kSimt) ? NCW * 32 / GS : 1;
+  static constexpr int TPG = kPageTokens / NG;
+  // mma layout: warps split (token half, head_dim half) of the page.
+  static constexpr int kRedRows = (M == Math::kSimt) ? NG : 2;
+  alignas(1024) T k[NSTAGE][kPageTokens * D];
+  alignas(1024) T v[NSTAGE][kPageTokens * D];
   alignas(128) T q[NSTAGE][G * D];
   alignas(16) float red_acc[G][D];
-  alignas(16) float pbuf[2][NG][G][TPG];
-  float abuf[2][NG][G];
-  float red_m[2][NG][G];  // double-buffered by segment parity
-  float red_l[2][NG][G];
+  // CUDA-core consumer only: per-group broadcast of p and the rescale factor.
+  static constexpr int PG = (M == Math::kSimt) ? G : 1;
+  static constexpr int PT = (M == Math::kSimt) ? TPG : 1;
+  alignas(16) float pbuf[2][NG][PG][PT];
+  float abuf[2][NG][PG];
+  float red_m[2][kRedRows][G];  // double-buffered by segment parity
+  float red_l[2][kRedRows][G];
+  float fin_m[G];
+  float fin_l[G];
   StageHeader hdr[NSTAGE];
   alignas(8) unsigned long long full[NSTAGE];
   unsigned long long empty[NSTAGE];
   unsigned long long csync;
   long long scan[16];
-  long long total_units, u0, u1, cum_start;
-  int c_eff, b_start, flag_last;
+  int b_start_s;
+  long long cum_start_s;
+  int flag_last;
   volatile int abort_flag;
 };
 
@@ -148,7 +164,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// 3-D tiled TMA load: box (D, 1, 32) at element coordinates (x, y, z).
+// 3-D tiled TMA load at element coordinates (x, y, z).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             unsigned long long* bar) {
   asm volatile(
@@ -171,6 +187,35 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// D = A * B + D, bf16 inputs, fp32 accumulators, m16n8k16.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's
 // abort flag plus a global status bit) once the wall-time limit is exceeded,
@@ -200,10 +245,12 @@ __device__ __forceinline__ bool wait_phase(unsigned long long* bar, uint32_t par
 }
 
 // ---------------------------------------------------------------------------
-// Element access.  Lane c of a row group owns 8 elements of every row:
+// Element access for the CUDA-core consumer.  Lane c of a row group owns 8
+// elements of every row:
 //   bf16: [8c, 8c+8)                  -> one 16-byte shared load
 //   fp32: [4c, 4c+4) and [D/2+4c, +4) -> two 16-byte shared loads, each
 //         contiguous across the group's lanes (no bank conflicts)
+// store(row, d0, x) writes 8 contiguous columns d0..d0+7 of a global row.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 struct LaneMap;
@@ -216,19 +263,13 @@ struct LaneMap<__nv_bfloat16, D> {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      x[2 * k] = __uint_as_float(w[k] << 16);
-      x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+      x[2 * k] = bf16_lo_f(w[k]);
+      x[2 * k + 1] = bf16_hi_f(w[k]);
     }
   }
   __device__ __forceinline__ static void store(__nv_bfloat16* row, int d0, const float (&x)[8]) {
-    // d0 is the first of 8 contiguous columns
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
-      w[k] = *reinterpret_cast<const uint32_t*>(&p);
-    }
-    *reinterpret_cast<uint4*>(row + d0) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(row + d0) = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                                     pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
   }
 };
 
@@ -335,23 +376,22 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, typename T, int G, int NCW, int NSTAGE, int MINB>
+template <int D, typename T, int G, int NCW, int NSTAGE, int MINB, Math MATH>
 __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const DecodeArgs a) {
-  using S = Smem<D, T, G, NCW, NSTAGE>;
-  using Map = LaneMap<T, D>;
+  using S = Smem<D, T, G, NCW, NSTAGE, MATH>;
   constexpr int NT = (NCW + 1) * 32;
   constexpr int NC = NCW * 32;  // consumer threads
-  constexpr int GS = S::GS, NG = S::NG, TPG = S::TPG;
   constexpr uint32_t kTileBytes = kPageTokens * D * sizeof(T);
-  static_assert(GS <= 32 && (32 % GS) == 0, "row group must tile a warp");
-  static_assert(NG * TPG == kPageTokens, "groups must tile the page");
-  static_assert(G <= GS && (GS % G) == 0, "group tile must divide the row group");
+  constexpr bool kMma = MATH == Math::kMma;
+  static_assert(!kMma || (sizeof(T) == 2 && NCW == 4 && G <= 16 && D % 128 == 0), "mma consumer shape");
+  static_assert(kMma || (S::GS <= 32 && (32 % S::GS) == 0 && S::NG * S::TPG == kPageTokens &&
+                         G <= S::GS && (S::GS % G) == 0), "CUDA-core consumer shape");
 
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // TMA destinations want 128-byte (here 1024-byte) aligned shared addresses;
-  // the launch reserves 1 KB of slack for this round-up.
+  // TMA destinations (128-byte swizzle atoms) want 1024-byte aligned shared
+  // addresses; the launch reserves 1 KB of slack for this round-up.
   const uint32_t raw_addr = smem_addr(smem_raw);
   S& s = *reinterpret_cast<S*>(smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr));
 
@@ -365,12 +405,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     }
     mbar_init(&s.csync, NC);
     s.abort_flag = 0;
+    s.b_start_s = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   for (int e = tid; e < G * D; e += NT) (&s.red_acc[0][0])[e] = 0.f;
 
   // ---- S1: request lookup and balanced partition ---------------------------
-  long long U = 0;
+  // Pass 1 sums the tiles; when the whole batch fits one pass of the block,
+  // the same scan also locates this CTA's first sequence (no second pass).
+  long long U = 0, my_excl = 0, my_units = 0;
   for (int base = 0; base < a.num_seqs; base += NT) {
     const int b = base + tid;
     long long units = 0;
@@ -384,11 +427,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 #pragma unroll
         for (int e = 0; e < 8; ++e) vals[e] = fill;
         T* row0 = static_cast<T*>(a.out) + static_cast<size_t>(b) * a.num_q_heads * D;
-        for (int e = 0; e < a.num_q_heads * D; e += 8) Map::store(row0, e, vals);
+        for (int e = 0; e < a.num_q_heads * D; e += 8) LaneMap<T, D>::store(row0, e, vals);
       }
     }
     long long tot;
-    block_exclusive_scan<NT>(units, s.scan, tot);
+    const long long excl = block_exclusive_scan<NT>(units, s.scan, tot);
+    my_excl = U + excl;
+    my_units = units;
     U += tot;
   }
   if (U == 0) return;
@@ -398,18 +443,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   const Partition part{U, C};
   const long long u0 = part.start(blockIdx.x), u1 = part.start(blockIdx.x + 1);
 
-  if (tid == 0) { s.b_start = -1; }
-  {
+  if (a.num_seqs <= NT) {
+    if (my_units > 0 && my_excl <= u0 && u0 < my_excl + my_units) {
+      s.b_start_s = tid;
+      s.cum_start_s = my_excl;
+    }
+  } else {
     long long carry = 0;
     for (int base = 0; base < a.num_seqs; base += NT) {
       const int b = base + tid;
       long long units = 0;
-      if (b < a.num_seqs) units = static_cast<long long>(seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks).np) * nvh;
+      if (b < a.num_seqs)
+        units = static_cast<long long>(seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks).np) * nvh;
       long long tot;
       const long long excl = carry + block_exclusive_scan<NT>(units, s.scan, tot);
       if (units > 0 && excl <= u0 && u0 < excl + units) {
-        s.b_start = b;
-        s.cum_start = excl;
+        s.b_start_s = b;
+        s.cum_start_s = excl;
       }
       carry += tot;
       if (carry > u0) break;  // uniform: carry is the same in every thread
@@ -426,8 +476,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
-    long long u = u0, cum = s.cum_start;
-    int b = s.b_start;
+    long long u = u0, cum = s.cum_start_s;
+    int b = s.b_start_s;
     // window of 32 context lengths cached across the warp
     int win_base = -(1 << 30), win_len = 0;  // nothing cached yet
     auto length_of = [&](int bb) -> int {
@@ -438,7 +488,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       }
       return __shfl_sync(0xffffffffu, win_len, bb - win_base);
     };
-    bool ok = true;
+    bool ok = b >= 0;
     while (ok && u < u1) {
       const SeqSpan sp = seq_span(length_of(b), a.window, a.max_blocks);
       const long long ub = static_cast<long long>(sp.np) * nvh;
@@ -483,8 +533,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               if (p == pa) bytes += static_cast<uint32_t>(gq) * D * sizeof(T);
               mbar_arrive_expect_tx(&s.full[stage], bytes);
               if (!bad) {
-                tma_load_3d(s.k[stage], &tmap_k, 0, h, pid * kPageTokens, &s.full[stage]);
-                tma_load_3d(s.v[stage], &tmap_v, 0, h, pid * kPageTokens, &s.full[stage]);
+                if constexpr (kMma) {
+                  // 128-byte swizzled sub-tiles of 64 columns: [D/64][32 tokens][64]
+#pragma unroll
+                  for (int sb = 0; sb < D / kSwizzleCols; ++sb) {
+                    tma_load_3d(s.k[stage] + sb * kPageTokens * kSwizzleCols, &tmap_k, sb * kSwizzleCols, h,
+                                pid * kPageTokens, &s.full[stage]);
+                    tma_load_3d(s.v[stage] + sb * kPageTokens * kSwizzleCols, &tmap_v, sb * kSwizzleCols, h,
+                                pid * kPageTokens, &s.full[stage]);
+                  }
+                } else {
+                  tma_load_3d(s.k[stage], &tmap_k, 0, h, pid * kPageTokens, &s.full[stage]);
+                  tma_load_3d(s.v[stage], &tmap_v, 0, h, pid * kPageTokens, &s.full[stage]);
+                }
               }
               if (p == pa) {
                 const T* qsrc = static_cast<const T*>(a.q) +
@@ -511,7 +572,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       if (b >= a.num_seqs) break;
     }
     // Self-check: the walk must have produced exactly this CTA's tiles.
-    if (ok && issued != u1 - u0 && lane == 0) {
+    if (issued != u1 - u0 && !s.abort_flag && lane == 0) {
       atomicOr(a.status, kStatusWalk);
       s.abort_flag = 1;
     }
@@ -530,22 +591,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   }
 
   // ===================== consumer warps (S3 - S9) =============================
-  const int ct = tid;                 // 0 .. NC-1
-  const int j = ct / GS;              // row group
-  const int c = ct % GS;              // lane within row group
-  constexpr int kSpread = GS / G;     // lanes holding the same query after the reduce
-  const int iq = c / kSpread;         // query row this lane's scores belong to
-  const bool owner = (c % kSpread) == 0;
+  const int ct = tid;  // 0 .. NC-1
   const float kNegInf = -__int_as_float(0x7f800000);
-
-  float qf[G][8];
-  float acc[G][8];
-  float m_run = kNegInf, l_run = 0.f;
-  bool poison = false;
-  int stage = 0;
-  uint32_t phase = 0, sync_phase = 0;
-  int par = 0, seg_par = 0;
-
+  const float kNaN = __int_as_float(0x7fc00000);
+  uint32_t sync_phase = 0;
   auto cons_sync = [&]() -> bool {
     mbar_arrive(&s.csync);
     const bool r = wait_phase(&s.csync, sync_phase, &s.abort_flag, a.status, kStatusSync);
@@ -553,107 +602,287 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     return r;
   };
 
+  // ---- per-consumer state --------------------------------------------------
+  // CUDA-core consumer (fp32): row group j (GS lanes), lane c owns 8 columns.
+  constexpr int GS = S::GS, NG = S::NG, TPG = S::TPG;
+  const int j = ct / GS;
+  const int c = ct % GS;
+  constexpr int kSpread = (GS / G) > 0 ? GS / G : 1;
+  const int iq = c / kSpread;
+  const bool owner = (c % kSpread) == 0;
+  // mma consumer (bf16): warp = (token half tg, head_dim half dp).
+  constexpr int kKSteps = D / 16;     // k-steps of QK^T over head_dim
+  constexpr int kONt = D / 16;        // 8-column output tiles per warp (half of head_dim)
+  constexpr bool kTwoRows = G > 8;    // second fragment row (queries 8..15) live
+  const int tg = warp & 1, dp = warp >> 1;
+  const int gid = lane >> 2, tig = lane & 3;
+
+  int stage = 0;
+  uint32_t phase = 0;
+  int par = 0, seg_par = 0;
   const long long n_tiles = u1 - u0;
-  for (long long it = 0; it < n_tiles; ++it) {
+  long long it = 0;
+  bool alive = true;
+  // One iteration per (sequence, virtual head) segment: the query fragments
+  // and accumulators are scoped to it, so they are dead in the epilogue.
+  while (alive && it < n_tiles) {
+  float qf[kMma ? 1 : G][8];
+  float acc[kMma ? 1 : G][8];
+  uint32_t qa[kMma ? kKSteps : 1][4];
+  float oacc[kMma ? kONt : 1][4];
+  float m_run = kNegInf, l_run = 0.f;     // simt: lane's query; mma: row gid
+  float m_run2 = kNegInf, l_run2 = 0.f;   // mma: row gid + 8
+  bool poison = false;
+  StageHeader hd;
+  do {
     bool ok = wait_phase(&s.full[stage], phase, &s.abort_flag, a.status, kStatusFull);
     ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    const StageHeader hd = s.hdr[stage];
-
-    if (hd.flags & kFirst) {
-      const T* qs = s.q[stage];
-#pragma unroll
-      for (int i = 0; i < G; ++i) {
-        float x[8];
-        if (i < hd.gq) {
-          Map::load(qs + i * D, c, x);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          qf[i][e] = x[e] * a.scale_log2;
-          acc[i][e] = 0.f;
-        }
-      }
-      m_run = kNegInf;
-      l_run = 0.f;
-      poison = false;
+    if (!ok) {
+      alive = false;
+      break;
     }
+    hd = s.hdr[stage];
 
-    if (hd.flags & kBadPage) {
-      poison = true;
-    } else {
-      const T* ks = s.k[stage];
-      const T* vs = s.v[stage];
-      // S3 + S4: scores of this group's tokens, for the lane's query row
-      float sc[TPG];
-#pragma unroll
-      for (int tt = 0; tt < TPG; ++tt) {
-        const int t = j + NG * tt;
-        float kx[8];
-        Map::load(ks + t * D, c, kx);
-        float part_s[G];
+    if constexpr (!kMma) {
+      // ====================== CUDA-core consumer ==============================
+      using Map = LaneMap<T, D>;
+      if (hd.flags & kFirst) {
+        const T* qs = s.q[stage];
 #pragma unroll
         for (int i = 0; i < G; ++i) {
-          float sum = 0.f;
+          float x[8];
+          if (i < hd.gq) {
+            Map::load(qs + i * D, c, x);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sum = fmaf(qf[i][e], kx[e], sum);
-          part_s[i] = sum;
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            qf[i][e] = x[e] * a.scale_log2;
+            acc[i][e] = 0.f;
+          }
         }
-        const float r = group_reduce_scatter<G, GS>(part_s, c);
-        sc[tt] = (t >= hd.lo && t < hd.hi) ? r : kNegInf;
+        m_run = kNegInf;
+        l_run = 0.f;
+        poison = false;
       }
-      // S5: online softmax update for query iq (base 2, scores pre-scaled)
-      float mloc = sc[0];
+      if (hd.flags & kBadPage) {
+        poison = true;
+      } else {
+        const T* ks = s.k[stage];
+        const T* vs = s.v[stage];
+        float sc[TPG];
 #pragma unroll
-      for (int tt = 1; tt < TPG; ++tt) mloc = fmaxf(mloc, sc[tt]);
-      const float m_new = fmaxf(m_run, mloc);
-      const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-      const float alpha = exp2f(m_run - m_use);
-      float p[TPG];
-      float psum = 0.f;
-#pragma unroll
-      for (int tt = 0; tt < TPG; ++tt) {
-        p[tt] = exp2f(sc[tt] - m_use);
-        psum += p[tt];
-      }
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      if (owner) {
-#pragma unroll
-        for (int tt = 0; tt < TPG; ++tt) s.pbuf[par][j][iq][tt] = p[tt];
-        s.abuf[par][j][iq] = alpha;
-      }
-      __syncwarp();
-      // rescale the accumulators if any row's maximum moved
-      const bool moved = __any_sync(0xffffffffu, alpha != 1.f);
-      if (moved) {
-#pragma unroll
-        for (int i = 0; i < G; ++i) {
-          const float ai = s.abuf[par][j][i];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[i][e] *= ai;
-        }
-      }
-      // S6: acc += p * v over this group's valid tokens
-#pragma unroll
-      for (int tt = 0; tt < TPG; ++tt) {
-        const int t = j + NG * tt;
-        if (t >= hd.lo && t < hd.hi) {
-          float vx[8];
-          Map::load(vs + t * D, c, vx);
+        for (int tt = 0; tt < TPG; ++tt) {
+          const int t = j + NG * tt;
+          float kx[8];
+          Map::load(ks + t * D, c, kx);
+          float part_s[G];
 #pragma unroll
           for (int i = 0; i < G; ++i) {
-            const float pi = s.pbuf[par][j][i][tt];
+            float sum = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pi, vx[e], acc[i][e]);
+            for (int e = 0; e < 8; ++e) sum = fmaf(qf[i][e], kx[e], sum);
+            part_s[i] = sum;
+          }
+          const float r = group_reduce_scatter<G, GS>(part_s, c);
+          sc[tt] = (t >= hd.lo && t < hd.hi) ? r : kNegInf;
+        }
+        float mloc = sc[0];
+#pragma unroll
+        for (int tt = 1; tt < TPG; ++tt) mloc = fmaxf(mloc, sc[tt]);
+        const float m_new = fmaxf(m_run, mloc);
+        const float m_use = (m_new == kNegInf) ? 0.f : m_new;
+        const float alpha = exp2f(m_run - m_use);
+        float p[TPG];
+        float psum = 0.f;
+#pragma unroll
+        for (int tt = 0; tt < TPG; ++tt) {
+          p[tt] = exp2f(sc[tt] - m_use);
+          psum += p[tt];
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_new;
+        if (owner) {
+#pragma unroll
+          for (int tt = 0; tt < TPG; ++tt) s.pbuf[par][j][iq][tt] = p[tt];
+          s.abuf[par][j][iq] = alpha;
+        }
+        __syncwarp();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int i = 0; i < G; ++i) {
+            const float ai = s.abuf[par][j][i];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[i][e] *= ai;
+          }
+        }
+#pragma unroll
+        for (int tt = 0; tt < TPG; ++tt) {
+          const int t = j + NG * tt;
+          if (t >= hd.lo && t < hd.hi) {
+            float vx[8];
+            Map::load(vs + t * D, c, vx);
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+              const float pi = s.pbuf[par][j][i][tt];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pi, vx[e], acc[i][e]);
+            }
+          }
+        }
+        par ^= 1;
+      }
+    } else {
+      // ======================== tensor-core consumer ==========================
+      if (hd.flags & kFirst) {
+        // Q as the A operand of m16n8k16 (rows = queries, k = head_dim);
+        // rows at or past the live group are zero.
+        const uint32_t* q32 = reinterpret_cast<const uint32_t*>(s.q[stage]);
+        const bool r0ok = gid < hd.gq, r1ok = kTwoRows && (gid + 8) < hd.gq;
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ++ks) {
+          const int col = ks * 16 + 2 * tig;
+          qa[ks][0] = r0ok ? q32[(gid * D + col) >> 1] : 0u;
+          qa[ks][1] = r1ok ? q32[((gid + 8) * D + col) >> 1] : 0u;
+          qa[ks][2] = r0ok ? q32[(gid * D + col + 8) >> 1] : 0u;
+          qa[ks][3] = r1ok ? q32[((gid + 8) * D + col + 8) >> 1] : 0u;
+        }
+#pragma unroll
+        for (int nt = 0; nt < kONt; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
+        m_run = m_run2 = kNegInf;
+        l_run = l_run2 = 0.f;
+        poison = false;
+      }
+      if (hd.flags & kBadPage) {
+        poison = true;
+      } else {
+        const uint32_t kbase = smem_addr(s.k[stage]);
+        const uint32_t vbase = smem_addr(s.v[stage]);
+        // S3: S = Q K^T for this warp's 16 tokens (two n8 tiles), full head_dim.
+        float sacc[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[n][e] = 0.f;
+        {
+          const int mi = lane >> 3, r = lane & 7;
+          const int t = 16 * tg + ((mi >> 1) << 3) + r;  // token row this lane addresses
+#pragma unroll
+          for (int ks = 0; ks < kKSteps; ++ks) {
+            const int d = ks * 16 + ((mi & 1) << 3);
+            const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
+            const uint32_t addr = kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
+            uint32_t bk[4];
+            ldmatrix_x4(addr, bk);
+            mma_bf16(sacc[0], qa[ks], bk[0], bk[1]);
+            mma_bf16(sacc[1], qa[ks], bk[2], bk[3]);
+          }
+        }
+        // S4 + S5: mask, scale, online softmax for rows gid and gid + 8.
+        float sv[2][4];
+        float mx0 = kNegInf, mx1 = kNegInf;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = 16 * tg + 8 * n + 2 * tig + (e & 1);
+            const bool row_ok = (e < 2) ? (gid < hd.gq) : (kTwoRows && gid + 8 < hd.gq);
+            const bool live = row_ok && t >= hd.lo && t < hd.hi;
+            sv[n][e] = live ? sacc[n][e] * a.scale_log2 : kNegInf;
+            if (e < 2) mx0 = fmaxf(mx0, sv[n][e]); else mx1 = fmaxf(mx1, sv[n][e]);
+          }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        if constexpr (kTwoRows) {
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        }
+        const float mn0 = fmaxf(m_run, mx0), mn1 = fmaxf(m_run2, mx1);
+        const float mu0 = (mn0 == kNegInf) ? 0.f : mn0, mu1 = (mn1 == kNegInf) ? 0.f : mn1;
+        const float al0 = exp2f(m_run - mu0), al1 = kTwoRows ? exp2f(m_run2 - mu1) : 1.f;
+        float pr[2][4];
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (e < 2) {
+              pr[n][e] = exp2f(sv[n][e] - mu0);
+              ps0 += pr[n][e];
+            } else if (kTwoRows) {
+              pr[n][e] = exp2f(sv[n][e] - mu1);
+              ps1 += pr[n][e];
+            } else {
+              pr[n][e] = 0.f;
+            }
+          }
+        l_run = l_run * al0 + ps0;
+        l_run2 = l_run2 * al1 + ps1;
+        m_run = mn0;
+        m_run2 = mn1;
+        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+          for (int nt = 0; nt < kONt; ++nt) {
+            oacc[nt][0] *= al0;
+            oacc[nt][1] *= al0;
+            oacc[nt][2] *= al1;
+            oacc[nt][3] *= al1;
+          }
+        }
+        // P as the A operand (rows = queries, k = the 16 tokens), split into
+        // bf16 hi + lo so that hi + lo carries ~16 significant bits of p.
+        // A-fragment order: (row g, k 0-7), (row g+8, k 0-7), (row g, k 8-15),
+        // (row g+8, k 8-15), i.e. n-tile 0 rows g / g+8, then n-tile 1.
+        uint32_t pa_hi[4], pa_lo[4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const uint32_t h01 = pack_bf16(pr[n][0], pr[n][1]);
+          const uint32_t h23 = pack_bf16(pr[n][2], pr[n][3]);
+          pa_hi[2 * n] = h01;
+          pa_hi[2 * n + 1] = h23;
+          pa_lo[2 * n] = pack_bf16(pr[n][0] - bf16_lo_f(h01), pr[n][1] - bf16_hi_f(h01));
+          pa_lo[2 * n + 1] = pack_bf16(pr[n][2] - bf16_lo_f(h23), pr[n][3] - bf16_hi_f(h23));
+        }
+        // V rows of masked tokens may hold anything (NaN in unused slots):
+        // zero this warp's part of them so 0 * v stays 0 in the MMA.
+        if (hd.lo > 16 * tg || hd.hi < 16 * tg + 16) {
+          constexpr int kSubs = (D / 2) / kSwizzleCols;  // sub-tiles in this warp's half
+          for (int idx = lane; idx < 16 * 8 * kSubs; idx += 32) {
+            const int t = 16 * tg + idx / (8 * kSubs);
+            const int rem = idx % (8 * kSubs);
+            const int sb = dp * kSubs + rem / 8, chunk = rem % 8;
+            if (t < hd.lo || t >= hd.hi)
+              *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(s.v[stage]) + sb * (kPageTokens * 128) +
+                                        t * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          // order these generic-proxy writes before the TMA that will refill the stage
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        // S6: O[:, this warp's half of head_dim] += P V over the 16 tokens.
+        {
+          const int mi = lane >> 3, r = lane & 7;
+          const int t = 16 * tg + ((mi & 1) << 3) + r;
+#pragma unroll
+          for (int np2 = 0; np2 < kONt / 2; ++np2) {
+            const int d = dp * (D / 2) + np2 * 16 + ((mi >> 1) << 3);
+            const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
+            const uint32_t addr = vbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
+            uint32_t bv[4];
+            ldmatrix_x4_trans(addr, bv);
+            mma_bf16(oacc[2 * np2], pa_hi, bv[0], bv[1]);
+            mma_bf16(oacc[2 * np2 + 1], pa_hi, bv[2], bv[3]);
+            mma_bf16(oacc[2 * np2], pa_lo, bv[0], bv[1]);
+            mma_bf16(oacc[2 * np2 + 1], pa_lo, bv[2], bv[3]);
           }
         }
       }
-      par ^= 1;
     }
+
     // release the stage to the producer
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.empty[stage]);
@@ -661,43 +890,95 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       stage = 0;
       phase ^= 1u;
     }
+    ++it;
+  } while (!(hd.flags & kLast) && it < n_tiles);
+  if (!alive || !(hd.flags & kLast)) break;
 
-    if (!(hd.flags & kLast)) continue;
-
-    // ---- end of a (sequence, virtual head) segment: merge the row groups ----
-    // red_m/red_l are double-buffered: a thread can only reach the next
-    // segment's first rendezvous after every thread finished reading these.
+    // ---- end of a (sequence, virtual head) segment: merge inside the CTA ----
+    // Result: red_acc[i][d] = the CTA's states scaled to the common maximum
+    // fin_m[i] and summed; fin_l[i] = the matching normaliser.
     float (*rm)[G] = s.red_m[seg_par];
     float (*rl)[G] = s.red_l[seg_par];
     seg_par ^= 1;
-    if (owner) {
-      rm[j][iq] = m_run;
-      rl[j][iq] = poison ? __int_as_float(0x7fc00000) : l_run;
-    }
-    if (!cons_sync()) break;
+    if constexpr (!kMma) {
+      if (owner) {
+        rm[j][iq] = m_run;
+        rl[j][iq] = poison ? kNaN : l_run;
+      }
+      if (!cons_sync()) break;
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      float M = kNegInf;
+      for (int i = 0; i < G; ++i) {
+        float Mx = kNegInf;
 #pragma unroll
-      for (int g2 = 0; g2 < NG; ++g2) M = fmaxf(M, rm[g2][i]);
-      const float f = exp2f(rm[j][i] - ((M == kNegInf) ? 0.f : M));
+        for (int g2 = 0; g2 < NG; ++g2) Mx = fmaxf(Mx, rm[g2][i]);
+        const float Ms = (Mx == kNegInf) ? 0.f : Mx;
+        const float f = exp2f(rm[j][i] - Ms);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) atomicAdd(&s.red_acc[i][Map::col(c, e)], acc[i][e] * f);
+        for (int e = 0; e < 8; ++e) atomicAdd(&s.red_acc[i][LaneMap<T, D>::col(c, e)], acc[i][e] * f);
+        if (ct == i) {
+          float L = 0.f;
+#pragma unroll
+          for (int g2 = 0; g2 < NG; ++g2) L += rl[g2][i] * exp2f(rm[g2][i] - Ms);
+          s.fin_m[i] = Ms;
+          s.fin_l[i] = L;
+        }
+      }
+    } else {
+      // row sums: each lane holds a quarter of its rows' columns
+      float lf0 = l_run, lf1 = l_run2;
+      lf0 += __shfl_xor_sync(0xffffffffu, lf0, 1);
+      lf0 += __shfl_xor_sync(0xffffffffu, lf0, 2);
+      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 1);
+      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 2);
+      if (dp == 0 && tig == 0) {
+        if (gid < G) {
+          rm[tg][gid] = m_run;
+          rl[tg][gid] = poison ? kNaN : lf0;
+        }
+        if (kTwoRows && gid + 8 < G) {
+          rm[tg][gid + 8] = m_run2;
+          rl[tg][gid + 8] = poison ? kNaN : lf1;
+        }
+      }
+      if (!cons_sync()) break;
+      const int r0 = gid, r1 = gid + 8;
+      float f0 = 0.f, f1 = 0.f;
+      if (r0 < hd.gq) {
+        const float Mx = fmaxf(rm[0][r0], rm[1][r0]);
+        f0 = exp2f(m_run - ((Mx == kNegInf) ? 0.f : Mx));
+      }
+      if (kTwoRows && r1 < hd.gq) {
+        const float Mx = fmaxf(rm[0][r1], rm[1][r1]);
+        f1 = exp2f(m_run2 - ((Mx == kNegInf) ? 0.f : Mx));
+      }
+#pragma unroll
+      for (int nt = 0; nt < kONt; ++nt) {
+        const int d = dp * (D / 2) + nt * 8 + 2 * tig;
+        if (r0 < hd.gq) {
+          atomicAdd(&s.red_acc[r0][d], oacc[nt][0] * f0);
+          atomicAdd(&s.red_acc[r0][d + 1], oacc[nt][1] * f0);
+        }
+        if (kTwoRows && r1 < hd.gq) {
+          atomicAdd(&s.red_acc[r1][d], oacc[nt][2] * f1);
+          atomicAdd(&s.red_acc[r1][d + 1], oacc[nt][3] * f1);
+        }
+      }
+      if (ct < G) {
+        const float Mx = fmaxf(rm[0][ct], rm[1][ct]);
+        const float Ms = (Mx == kNegInf) ? 0.f : Mx;
+        s.fin_m[ct] = Ms;
+        s.fin_l[ct] = rl[0][ct] * exp2f(rm[0][ct] - Ms) + rl[1][ct] * exp2f(rm[1][ct] - Ms);
+      }
     }
     if (!cons_sync()) break;
 
+    // ---- S9 / S7: final rows, or this CTA's normalised partial ---------------
     const int h = hd.vh / a.subgroups, sub = hd.vh - h * a.subgroups;
     const int q_row0 = h * a.group + sub * G;
     const bool split = (hd.flags & kSplit) != 0;
     for (int e0 = ct * 8; e0 < G * D; e0 += NC * 8) {
       const int i = e0 / D, d0 = e0 - i * D;
-      float M = kNegInf;
-#pragma unroll
-      for (int g2 = 0; g2 < NG; ++g2) M = fmaxf(M, rm[g2][i]);
-      M = (M == kNegInf) ? 0.f : M;
-      float L = 0.f;
-#pragma unroll
-      for (int g2 = 0; g2 < NG; ++g2) L += rl[g2][i] * exp2f(rm[g2][i] - M);
+      const float L = s.fin_l[i];
       float val[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -706,22 +987,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       }
       if (i >= hd.gq) continue;
       if (!split) {
-        // S9: final row, one rounding to the storage type
         T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D;
-        // columns d0..d0+7 are contiguous here (not the lane map)
-        if constexpr (sizeof(T) == 2) {
-          LaneMap<__nv_bfloat16, D>::store(reinterpret_cast<__nv_bfloat16*>(row), d0, val);
-        } else {
-          LaneMap<float, D>::store(reinterpret_cast<float*>(row), d0, val);
-        }
+        LaneMap<T, D>::store(row, d0, val);
       } else {
-        // S7: normalised partial row plus its (m, l)
         float* po = a.part_o + (static_cast<size_t>(hd.slot) * G + i) * D + d0;
         *reinterpret_cast<float4*>(po) = make_float4(val[0], val[1], val[2], val[3]);
         *reinterpret_cast<float4*>(po + 4) = make_float4(val[4], val[5], val[6], val[7]);
         if (d0 == 0) {
           float* pm = a.part_ml + (static_cast<size_t>(hd.slot) * G + i) * 2;
-          pm[0] = M;
+          pm[0] = s.fin_m[i];
           pm[1] = L;
         }
       }
@@ -742,38 +1016,45 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     if (!s.flag_last) continue;
     __threadfence();
     const int c_first = part.owner(hd.item_u);
-    for (int e0 = ct * 8; e0 < G * D; e0 += NC * 8) {
+    // Each thread owns 4 columns of one row and merges the partials online,
+    // eight at a time so their loads are all in flight together.
+    for (int e0 = ct * 4; e0 < G * D; e0 += NC * 4) {
       const int i = e0 / D, d0 = e0 - i * D;
       if (i >= hd.gq) continue;
-      float M = kNegInf;
-      for (int k = 0; k < hd.nsplit; ++k) {
-        const int sl = part.slot(c_first + k, hd.item_u);
-        M = fmaxf(M, __ldcg(a.part_ml + (static_cast<size_t>(sl) * G + i) * 2));
-      }
-      float L = 0.f, o[8];
+      float Mr = kNegInf, Lr = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k0 = 0; k0 < hd.nsplit; k0 += 8) {
+        float2 ml[8];
+        float4 ov[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = 0.f;
-      for (int k = 0; k < hd.nsplit; ++k) {
-        const int sl = part.slot(c_first + k, hd.item_u);
-        const float* pm = a.part_ml + (static_cast<size_t>(sl) * G + i) * 2;
-        const float w = __ldcg(pm + 1) * exp2f(__ldcg(pm) - M);
-        L += w;
-        const float* po = a.part_o + (static_cast<size_t>(sl) * G + i) * D + d0;
-        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(po));
-        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(po + 4));
-        o[0] = fmaf(w, x0.x, o[0]); o[1] = fmaf(w, x0.y, o[1]);
-        o[2] = fmaf(w, x0.z, o[2]); o[3] = fmaf(w, x0.w, o[3]);
-        o[4] = fmaf(w, x1.x, o[4]); o[5] = fmaf(w, x1.y, o[5]);
-        o[6] = fmaf(w, x1.z, o[6]); o[7] = fmaf(w, x1.w, o[7]);
-      }
-      float val[8];
+        for (int k = 0; k < 8; ++k) {
+          if (k0 + k < hd.nsplit) {
+            const int sl = part.slot(c_first + k0 + k, hd.item_u);
+            ml[k] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (static_cast<size_t>(sl) * G + i) * 2));
+            ov[k] = __ldcg(reinterpret_cast<const float4*>(a.part_o + (static_cast<size_t>(sl) * G + i) * D + d0));
+          } else {
+            ml[k] = make_float2(kNegInf, 0.f);
+            ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) val[e] = o[e] / L;
-      T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D;
+        for (int k = 0; k < 8; ++k) {
+          if (k0 + k >= hd.nsplit) continue;
+          const float Mn = fmaxf(Mr, ml[k].x);
+          const float sc_old = exp2f(Mr - Mn);  // Mr = -inf the first time -> 0
+          const float w = ml[k].y * exp2f(ml[k].x - Mn);
+          Lr = Lr * sc_old + w;
+          o[0] = o[0] * sc_old + w * ov[k].x;
+          o[1] = o[1] * sc_old + w * ov[k].y;
+          o[2] = o[2] * sc_old + w * ov[k].z;
+          o[3] = o[3] * sc_old + w * ov[k].w;
+          Mr = Mn;
+        }
+      }
+      T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D + d0;
       if constexpr (sizeof(T) == 2) {
-        LaneMap<__nv_bfloat16, D>::store(reinterpret_cast<__nv_bfloat16*>(row), d0, val);
+        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(o[0] / Lr, o[1] / Lr), pack_bf16(o[2] / Lr, o[3] / Lr));
       } else {
-        LaneMap<float, D>::store(reinterpret_cast<float*>(row), d0, val);
+        *reinterpret_cast<float4*>(row) = make_float4(o[0] / Lr, o[1] / Lr, o[2] / Lr, o[3] / Lr);
       }
     }
   }

@@ -7,6 +7,7 @@ namespace vt {
 
 struct VariantInfo {
   int head_dim;
+  int tensor_cores;    // 1: mma.sync consumer (bf16), 0: CUDA-core consumer
   int dtype;           // 0 bf16, 1 fp32
   int group_tile;      // G
   int consumer_warps;  // NCW
@@ -24,32 +25,33 @@ constexpr size_t kSmemPerSm = 233472;
 constexpr size_t kSmemReservedPerCta = 1024;
 
 // Deepest ring (<= ST stages) whose CTA still fits MINB times on an SM.
-template <int D, typename T, int G, int NCW, int MINB, int ST>
+template <int D, typename T, int G, int NCW, int MINB, Math M, int ST>
 struct StagePick {
-  static constexpr size_t bytes = sizeof(Smem<D, T, G, NCW, ST>) + 1024;
+  static constexpr size_t bytes = sizeof(Smem<D, T, G, NCW, ST, M>) + 1024;
   static constexpr int value =
-      (bytes + kSmemReservedPerCta) * MINB <= kSmemPerSm ? ST : StagePick<D, T, G, NCW, MINB, ST - 1>::value;
+      (bytes + kSmemReservedPerCta) * MINB <= kSmemPerSm ? ST : StagePick<D, T, G, NCW, MINB, M, ST - 1>::value;
 };
-template <int D, typename T, int G, int NCW, int MINB>
-struct StagePick<D, T, G, NCW, MINB, 0> {
+template <int D, typename T, int G, int NCW, int MINB, Math M>
+struct StagePick<D, T, G, NCW, MINB, M, 0> {
   static constexpr int value = 0;
 };
 
-template <int D, typename T, int G, int NCW, int MINB, int MAXST>
+template <int D, typename T, int G, int NCW, int MINB, int MAXST, Math M>
 struct Variant {
-  static constexpr int NSTAGE = StagePick<D, T, G, NCW, MINB, MAXST>::value;
+  static constexpr int NSTAGE = StagePick<D, T, G, NCW, MINB, M, MAXST>::value;
   static_assert(NSTAGE >= 2, "variant does not fit two stages in shared memory");
-  using S = Smem<D, T, G, NCW, NSTAGE>;
+  using S = Smem<D, T, G, NCW, NSTAGE, M>;
   static constexpr size_t smem = sizeof(S) + 1024;
 
   static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& args, int grid,
                             cudaStream_t stream) {
-    paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB><<<grid, (NCW + 1) * 32, smem, stream>>>(tk, tv, args);
+    paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M><<<grid, (NCW + 1) * 32, smem, stream>>>(tk, tv, args);
     return cudaGetLastError();
   }
 
   static VariantInfo info() {
     return VariantInfo{D,
+                       M == Math::kMma ? 1 : 0,
                        sizeof(T) == 2 ? 0 : 1,
                        G,
                        NCW,
@@ -57,7 +59,7 @@ struct Variant {
                        (NCW + 1) * 32,
                        MINB,
                        smem,
-                       reinterpret_cast<const void*>(&paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB>),
+                       reinterpret_cast<const void*>(&paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M>),
                        &launch};
   }
 };

@@ -51,7 +51,12 @@ const VariantInfo* find_variant(int head_dim, vt_dtype dtype, int group_tile) {
   return nullptr;
 }
 
-int group_tile_for(int group) {
+// Query rows computed per kv head and CTA.  bf16 runs on tensor cores with
+// the queries as the M dimension of m16n8k16: one tile of 8 (or 16) rows
+// covers any group up to that size.  fp32 runs on CUDA cores, where every
+// padded row costs FMAs: the next power of two, at most 8.
+int group_tile_for(int group, vt_dtype dtype) {
+  if (dtype == VT_BF16) return group <= 8 ? 8 : 16;
   int g = 1;
   while (g < group && g < kMaxGroupTile) g <<= 1;
   return g;
@@ -89,7 +94,6 @@ struct DeviceState {
   size_t ws_bytes = 0;
   size_t counters_cap = 0;  // bytes reserved for arrival counters (after the status word)
   size_t partial_cap = 0;   // bytes for partials, starting at 256 + counters_cap
-  std::vector<const void*> configured;  // kernels whose smem attribute is set
   std::vector<std::pair<const void*, int>> occupancy;
 };
 
@@ -216,12 +220,17 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
                               static_cast<cuuint64_t>(k.num_blocks) * vt::kPageTokens};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k.head_dim) * es,
                                  static_cast<cuuint64_t>(k.head_dim) * k.num_kv_heads * es};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(k.head_dim), 1u, static_cast<cuuint32_t>(vt::kPageTokens)};
+  // bf16 (tensor-core consumer): boxes of 64 columns (128 bytes) x 32 tokens
+  // with the 128-byte swizzle, so ldmatrix reads are bank-conflict free.
+  // fp32 (CUDA-core consumer): one unswizzled box of head_dim x 32 tokens.
+  const bool swz = k.dtype == VT_BF16;
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(swz ? vt::kSwizzleCols : k.head_dim), 1u,
+                             static_cast<cuuint32_t>(vt::kPageTokens)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   CUtensorMap m;
-  CUresult r = fn(&m, k.dtype == VT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+  CUresult r = fn(&m, swz ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                   const_cast<void*>(k.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     g_last_cuda_error = "cuTensorMapEncodeTiled failed (code " + std::to_string(static_cast<int>(r)) + ")";
@@ -276,7 +285,7 @@ size_t vt_paged_attn_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_h
                                      vt_dtype dtype) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
   const int group = num_q_heads / num_kv_heads;
-  const int gt = group_tile_for(group);
+  const int gt = group_tile_for(group, dtype);
   const VariantInfo* v = find_variant(head_dim, dtype, gt);
   if (!v) return 0;
   int dev = 0;
@@ -312,7 +321,7 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   if (static_cast<long long>(max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
 
   const int group = num_q_heads / num_kv_heads;
-  const int gt = group_tile_for(group);
+  const int gt = group_tile_for(group, dtype);
   const int subgroups = (group + gt - 1) / gt;
   const long long nvh = static_cast<long long>(num_kv_heads) * subgroups;
   if (nvh * num_seqs > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
@@ -375,6 +384,7 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   g_last_plan.grid_ctas = grid;
   g_last_plan.ctas_per_sm = per_sm;
   g_last_plan.consumer_warps = v->consumer_warps;
+  g_last_plan.tensor_cores = v->tensor_cores;
   g_last_plan.stages = v->stages;
   g_last_plan.group_tile = gt;
   g_last_plan.subgroups = subgroups;

@@ -202,7 +202,8 @@ def test_default_plan(dev):
     props = torch.cuda.get_device_properties(0)
     assert plan["num_sms"] == props.multi_processor_count
     assert plan["grid_ctas"] == plan["num_sms"] * plan["ctas_per_sm"]
-    assert plan["stages"] >= 2 and plan["group_tile"] == 2 and plan["subgroups"] == 1
+    assert plan["stages"] >= 2 and plan["group_tile"] == 8 and plan["subgroups"] == 1
+    assert plan["tensor_cores"] == 1
     assert plan["workspace_bytes"] > 0
 
 
