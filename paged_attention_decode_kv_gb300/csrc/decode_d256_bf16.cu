@@ -6,8 +6,8 @@ namespace vt {
 
 const VariantInfo* variants_d256_bf16(int* count) {
   static const VariantInfo table[] = {
-      Variant<256, __nv_bfloat16, 8, 4, 2, 4, Math::kMma>::info(),
-      Variant<256, __nv_bfloat16, 16, 4, 2, 4, Math::kMma>::info(),
+      Variant<256, __nv_bfloat16, 8, 4, 1, 6, Math::kMma>::info(),
+      Variant<256, __nv_bfloat16, 16, 4, 1, 6, Math::kMma>::info(),
   };
   *count = 2;
   return table;

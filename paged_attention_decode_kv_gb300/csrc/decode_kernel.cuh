@@ -50,8 +50,10 @@ namespace vt {
 
 constexpr int kPageTokens = 32;  // tokens per KV page (block_size)
 constexpr int kSwizzleCols = 64; // bf16 columns per 128-byte swizzled sub-tile row
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
-constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per drained copy
+// Wait limits in SM clock cycles (clock64 is a cheap per-SM counter; at the
+// GB300's 2.07 GHz maximum, 2^31 cycles is about 1 s and 2^28 about 0.13 s).
+constexpr long long kWaitLimitCycles = 1ll << 31;
+constexpr long long kDrainLimitCycles = 1ll << 28;
 
 // Stage flags written by the producer.
 enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8 };
@@ -75,7 +77,7 @@ struct DecodeArgs {
   float scale_log2; // scale * log2(e)
   int min_units;    // lower bound on tiles per CTA
   int* counters;    // [num_seqs * num_kv_heads * subgroups] arrival counters, zero between calls
-  float* part_ml;   // [2 * grid][G][2]  (m, l) of each partial, log2 domain
+  float* part_ml;   // [2 * grid][G][4]  (m, l, 0, 0) of each partial, log2 domain
   float* part_o;    // [2 * grid][G][D]  normalised partial rows
   unsigned* status; // status words
 };
@@ -94,6 +96,12 @@ struct StageHeader {
 // Consumer kinds.
 enum class Math { kSimt, kMma };
 
+// A combine the CTA owes: it was the last to finish a split item.
+struct PendingCombine {
+  int b, vh, nsplit, gq;
+  long long item_u;
+};
+
 template <int D, typename T, int G, int NCW, int NSTAGE, Math M>
 struct Smem {
   // CUDA-core layout: lane c of a row group owns 8 elements of every row.
@@ -105,7 +113,16 @@ struct Smem {
   alignas(1024) T k[NSTAGE][kPageTokens * D];
   alignas(1024) T v[NSTAGE][kPageTokens * D];
   alignas(128) T q[NSTAGE][G * D];
-  alignas(16) float red_acc[G][D];
+  // CUDA-core epilogue: the row groups' states summed by shared atomics.
+  static constexpr int RG = (M == Math::kSimt) ? G : 1;
+  static constexpr int RD = (M == Math::kSimt) ? D : 4;
+  alignas(16) float red_acc[RG][RD];
+  // Tensor-core epilogue: warps of token half 1 hand their accumulator
+  // fragments to the warps of token half 0 ([segment parity][dp][n-tile][lane]).
+  static constexpr int XV = (G > 8) ? 4 : 2;  // live accumulator values per lane and n-tile
+  static constexpr int XP = (M == Math::kMma) ? 2 : 1;
+  static constexpr int XN = (M == Math::kMma) ? D / 16 : 1;
+  alignas(16) float xbuf[XP][2][XN][32][XV];
   // CUDA-core consumer only: per-group broadcast of p and the rescale factor.
   static constexpr int PG = (M == Math::kSimt) ? G : 1;
   static constexpr int PT = (M == Math::kSimt) ? TPG : 1;
@@ -122,7 +139,8 @@ struct Smem {
   long long scan[16];
   int b_start_s;
   long long cum_start_s;
-  int flag_last;
+  PendingCombine pend[2];
+  int pend_n;
   volatile int abort_flag;
 };
 
@@ -188,6 +206,15 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 16-byte global -> shared copy through L2 only (the source may have been
+// written by another SM in this kernel), completion via cp.async groups.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -218,19 +245,22 @@ __device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(
 __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's
-// abort flag plus a global status bit) once the wall-time limit is exceeded,
-// or at once if the CTA has already aborted.
+// abort flag plus a global status bit) once the clock-cycle limit is
+// exceeded, or at once if the CTA has already aborted.  The limit is checked
+// with clock64 every 32 probes: a %globaltimer read costs far more than a
+// probe and would sit on the critical path of every wait that does not
+// complete at once.
 __device__ __forceinline__ bool wait_phase(unsigned long long* bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned* status, unsigned code,
-                                           unsigned long long limit = kWaitLimitNs) {
+                                           long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+  const long long t0 = clock64();
   for (;;) {
     if (*abort_flag) return false;
 #pragma unroll 1
     for (int k = 0; k < 32; ++k)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > limit) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(status, code);
       // first give-up in the grid: record where (status[1..4])
@@ -501,6 +531,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         const int pb = static_cast<int>(seg_end < sp.np ? seg_end : sp.np);
         const long long item_u = cum + static_cast<long long>(vh) * sp.np;
         const int nsplit = part.owner(item_u + sp.np - 1) - part.owner(item_u) + 1;
+        const int slot = part.slot(blockIdx.x, item_u);  // 64-bit divisions: once per segment
         const int h = vh / a.subgroups, sub = vh - h * a.subgroups;
         const int q_row0 = h * a.group + sub * G;
         const int gq = min(G, a.group - sub * G);
@@ -527,7 +558,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
                          (bad ? kBadPage : 0);
               hd.gq = gq;
               hd.nsplit = nsplit;
-              hd.slot = part.slot(blockIdx.x, item_u);
+              hd.slot = slot;
               hd.item_u = item_u;
               uint32_t bytes = bad ? 0u : 2u * kTileBytes;
               if (p == pa) bytes += static_cast<uint32_t>(gq) * D * sizeof(T);
@@ -584,7 +615,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         const int st = static_cast<int>(idx % NSTAGE);
         const uint32_t ph = static_cast<uint32_t>((idx / NSTAGE) & 1);
         volatile int never = 0;
-        if (!wait_phase(&s.full[st], ph, &never, a.status, kStatusDrain, kDrainLimitNs)) break;
+        if (!wait_phase(&s.full[st], ph, &never, a.status, kStatusDrain, kDrainLimitCycles)) break;
       }
     }
     return;
@@ -601,8 +632,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     sync_phase ^= 1u;
     return r;
   };
+  if (ct == 0) s.pend_n = 0;  // only thread 0 touches it until the final rendezvous
 
-  // ---- per-consumer state --------------------------------------------------
+  // ---- per-consumer constants ----------------------------------------------
   // CUDA-core consumer (fp32): row group j (GS lanes), lane c owns 8 columns.
   constexpr int GS = S::GS, NG = S::NG, TPG = S::TPG;
   const int j = ct / GS;
@@ -762,12 +794,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       } else {
         const uint32_t kbase = smem_addr(s.k[stage]);
         const uint32_t vbase = smem_addr(s.v[stage]);
-        // S3: S = Q K^T for this warp's 16 tokens (two n8 tiles), full head_dim.
-        float sacc[2][4];
+        // S3: S = Q K^T for this warp's 16 tokens (two n8 tiles), full
+        // head_dim; even and odd k-steps accumulate separately (two short
+        // dependency chains instead of one long one).
+        float sacc[2][2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[n][e] = 0.f;
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[n][hh][e] = 0.f;
         {
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi >> 1) << 3) + r;  // token row this lane addresses
@@ -778,8 +814,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const uint32_t addr = kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
             uint32_t bk[4];
             ldmatrix_x4(addr, bk);
-            mma_bf16(sacc[0], qa[ks], bk[0], bk[1]);
-            mma_bf16(sacc[1], qa[ks], bk[2], bk[3]);
+            mma_bf16(sacc[0][ks & 1], qa[ks], bk[0], bk[1]);
+            mma_bf16(sacc[1][ks & 1], qa[ks], bk[2], bk[3]);
           }
         }
         // S4 + S5: mask, scale, online softmax for rows gid and gid + 8.
@@ -792,7 +828,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const int t = 16 * tg + 8 * n + 2 * tig + (e & 1);
             const bool row_ok = (e < 2) ? (gid < hd.gq) : (kTwoRows && gid + 8 < hd.gq);
             const bool live = row_ok && t >= hd.lo && t < hd.hi;
-            sv[n][e] = live ? sacc[n][e] * a.scale_log2 : kNegInf;
+            sv[n][e] = live ? (sacc[n][0][e] + sacc[n][1][e]) * a.scale_log2 : kNegInf;
             if (e < 2) mx0 = fmaxf(mx0, sv[n][e]); else mx1 = fmaxf(mx1, sv[n][e]);
           }
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -847,22 +883,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           pa_lo[2 * n] = pack_bf16(pr[n][0] - bf16_lo_f(h01), pr[n][1] - bf16_hi_f(h01));
           pa_lo[2 * n + 1] = pack_bf16(pr[n][2] - bf16_lo_f(h23), pr[n][3] - bf16_hi_f(h23));
         }
-        // V rows of masked tokens may hold anything (NaN in unused slots):
-        // zero this warp's part of them so 0 * v stays 0 in the MMA.
-        if (hd.lo > 16 * tg || hd.hi < 16 * tg + 16) {
-          constexpr int kSubs = (D / 2) / kSwizzleCols;  // sub-tiles in this warp's half
-          for (int idx = lane; idx < 16 * 8 * kSubs; idx += 32) {
-            const int t = 16 * tg + idx / (8 * kSubs);
-            const int rem = idx % (8 * kSubs);
-            const int sb = dp * kSubs + rem / 8, chunk = rem % 8;
-            if (t < hd.lo || t >= hd.hi)
-              *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(s.v[stage]) + sb * (kPageTokens * 128) +
-                                        t * 128 + chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          // order these generic-proxy writes before the TMA that will refill the stage
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-        }
+        // V rows of masked tokens may hold anything (NaN in unused slots) and
+        // 0 * NaN is NaN inside the MMA: clear those tokens in the V fragments.
+        // This lane's fragments carry tokens 16tg + 2tig (+1) and (+8, +9).
+        const int tl = 16 * tg + 2 * tig;
+        const uint32_t mlo = ((tl >= hd.lo && tl < hd.hi) ? 0x0000ffffu : 0u) |
+                             ((tl + 1 >= hd.lo && tl + 1 < hd.hi) ? 0xffff0000u : 0u);
+        const uint32_t mhi = ((tl + 8 >= hd.lo && tl + 8 < hd.hi) ? 0x0000ffffu : 0u) |
+                             ((tl + 9 >= hd.lo && tl + 9 < hd.hi) ? 0xffff0000u : 0u);
         // S6: O[:, this warp's half of head_dim] += P V over the 16 tokens.
         {
           const int mi = lane >> 3, r = lane & 7;
@@ -874,6 +902,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const uint32_t addr = vbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
             uint32_t bv[4];
             ldmatrix_x4_trans(addr, bv);
+            bv[0] &= mlo;
+            bv[1] &= mhi;
+            bv[2] &= mlo;
+            bv[3] &= mhi;
             mma_bf16(oacc[2 * np2], pa_hi, bv[0], bv[1]);
             mma_bf16(oacc[2 * np2 + 1], pa_hi, bv[2], bv[3]);
             mma_bf16(oacc[2 * np2], pa_lo, bv[0], bv[1]);
@@ -894,88 +926,42 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   } while (!(hd.flags & kLast) && it < n_tiles);
   if (!alive || !(hd.flags & kLast)) break;
 
-    // ---- end of a (sequence, virtual head) segment: merge inside the CTA ----
-    // Result: red_acc[i][d] = the CTA's states scaled to the common maximum
-    // fin_m[i] and summed; fin_l[i] = the matching normaliser.
-    float (*rm)[G] = s.red_m[seg_par];
-    float (*rl)[G] = s.red_l[seg_par];
-    seg_par ^= 1;
-    if constexpr (!kMma) {
-      if (owner) {
-        rm[j][iq] = m_run;
-        rl[j][iq] = poison ? kNaN : l_run;
-      }
-      if (!cons_sync()) break;
+  // ---- end of a (sequence, virtual head) segment ----------------------------
+  const int h = hd.vh / a.subgroups, sub = hd.vh - h * a.subgroups;
+  const int q_row0 = h * a.group + sub * G;
+  const bool split = (hd.flags & kSplit) != 0;
+  // red_m / red_l / xbuf are double-buffered: a thread can only reach the next
+  // segment but one after every thread finished reading this segment's copy.
+  float (*rm)[G] = s.red_m[seg_par];
+  float (*rl)[G] = s.red_l[seg_par];
+  const int xp = seg_par;
+  seg_par ^= 1;
+  if constexpr (!kMma) {
+    // ---- merge the row groups through shared atomics ----
+    if (owner) {
+      rm[j][iq] = m_run;
+      rl[j][iq] = poison ? kNaN : l_run;
+    }
+    if (!cons_sync()) break;
 #pragma unroll
-      for (int i = 0; i < G; ++i) {
-        float Mx = kNegInf;
+    for (int i = 0; i < G; ++i) {
+      float Mx = kNegInf;
 #pragma unroll
-        for (int g2 = 0; g2 < NG; ++g2) Mx = fmaxf(Mx, rm[g2][i]);
-        const float Ms = (Mx == kNegInf) ? 0.f : Mx;
-        const float f = exp2f(rm[j][i] - Ms);
+      for (int g2 = 0; g2 < NG; ++g2) Mx = fmaxf(Mx, rm[g2][i]);
+      const float Ms = (Mx == kNegInf) ? 0.f : Mx;
+      const float f = exp2f(rm[j][i] - Ms);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) atomicAdd(&s.red_acc[i][LaneMap<T, D>::col(c, e)], acc[i][e] * f);
-        if (ct == i) {
-          float L = 0.f;
+      for (int e = 0; e < 8; ++e) atomicAdd(&s.red_acc[i][LaneMap<T, D>::col(c, e)], acc[i][e] * f);
+      if (ct == i) {
+        float L = 0.f;
 #pragma unroll
-          for (int g2 = 0; g2 < NG; ++g2) L += rl[g2][i] * exp2f(rm[g2][i] - Ms);
-          s.fin_m[i] = Ms;
-          s.fin_l[i] = L;
-        }
-      }
-    } else {
-      // row sums: each lane holds a quarter of its rows' columns
-      float lf0 = l_run, lf1 = l_run2;
-      lf0 += __shfl_xor_sync(0xffffffffu, lf0, 1);
-      lf0 += __shfl_xor_sync(0xffffffffu, lf0, 2);
-      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 1);
-      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 2);
-      if (dp == 0 && tig == 0) {
-        if (gid < G) {
-          rm[tg][gid] = m_run;
-          rl[tg][gid] = poison ? kNaN : lf0;
-        }
-        if (kTwoRows && gid + 8 < G) {
-          rm[tg][gid + 8] = m_run2;
-          rl[tg][gid + 8] = poison ? kNaN : lf1;
-        }
-      }
-      if (!cons_sync()) break;
-      const int r0 = gid, r1 = gid + 8;
-      float f0 = 0.f, f1 = 0.f;
-      if (r0 < hd.gq) {
-        const float Mx = fmaxf(rm[0][r0], rm[1][r0]);
-        f0 = exp2f(m_run - ((Mx == kNegInf) ? 0.f : Mx));
-      }
-      if (kTwoRows && r1 < hd.gq) {
-        const float Mx = fmaxf(rm[0][r1], rm[1][r1]);
-        f1 = exp2f(m_run2 - ((Mx == kNegInf) ? 0.f : Mx));
-      }
-#pragma unroll
-      for (int nt = 0; nt < kONt; ++nt) {
-        const int d = dp * (D / 2) + nt * 8 + 2 * tig;
-        if (r0 < hd.gq) {
-          atomicAdd(&s.red_acc[r0][d], oacc[nt][0] * f0);
-          atomicAdd(&s.red_acc[r0][d + 1], oacc[nt][1] * f0);
-        }
-        if (kTwoRows && r1 < hd.gq) {
-          atomicAdd(&s.red_acc[r1][d], oacc[nt][2] * f1);
-          atomicAdd(&s.red_acc[r1][d + 1], oacc[nt][3] * f1);
-        }
-      }
-      if (ct < G) {
-        const float Mx = fmaxf(rm[0][ct], rm[1][ct]);
-        const float Ms = (Mx == kNegInf) ? 0.f : Mx;
-        s.fin_m[ct] = Ms;
-        s.fin_l[ct] = rl[0][ct] * exp2f(rm[0][ct] - Ms) + rl[1][ct] * exp2f(rm[1][ct] - Ms);
+        for (int g2 = 0; g2 < NG; ++g2) L += rl[g2][i] * exp2f(rm[g2][i] - Ms);
+        s.fin_m[i] = Ms;
+        s.fin_l[i] = L;
       }
     }
     if (!cons_sync()) break;
-
-    // ---- S9 / S7: final rows, or this CTA's normalised partial ---------------
-    const int h = hd.vh / a.subgroups, sub = hd.vh - h * a.subgroups;
-    const int q_row0 = h * a.group + sub * G;
-    const bool split = (hd.flags & kSplit) != 0;
+    // ---- S9 / S7: final rows, or this CTA's normalised partial ----
     for (int e0 = ct * 8; e0 < G * D; e0 += NC * 8) {
       const int i = e0 / D, d0 = e0 - i * D;
       const float L = s.fin_l[i];
@@ -993,68 +979,190 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         float* po = a.part_o + (static_cast<size_t>(hd.slot) * G + i) * D + d0;
         *reinterpret_cast<float4*>(po) = make_float4(val[0], val[1], val[2], val[3]);
         *reinterpret_cast<float4*>(po + 4) = make_float4(val[4], val[5], val[6], val[7]);
-        if (d0 == 0) {
-          float* pm = a.part_ml + (static_cast<size_t>(hd.slot) * G + i) * 2;
-          pm[0] = s.fin_m[i];
-          pm[1] = L;
+        if (d0 == 0)
+          *reinterpret_cast<float4*>(a.part_ml + (static_cast<size_t>(hd.slot) * G + i) * 4) =
+              make_float4(s.fin_m[i], L, 0.f, 0.f);
+      }
+    }
+  } else {
+    // ---- token-half 1 hands its fragments to token-half 0 ----
+    float lf0 = l_run, lf1 = l_run2;  // each lane holds a quarter of its rows' columns
+    lf0 += __shfl_xor_sync(0xffffffffu, lf0, 1);
+    lf0 += __shfl_xor_sync(0xffffffffu, lf0, 2);
+    if constexpr (kTwoRows) {
+      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 1);
+      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 2);
+    }
+    if (dp == 0 && tig == 0) {
+      if (gid < G) {
+        rm[tg][gid] = m_run;
+        rl[tg][gid] = poison ? kNaN : lf0;
+      }
+      if (kTwoRows && gid + 8 < G) {
+        rm[tg][gid + 8] = m_run2;
+        rl[tg][gid + 8] = poison ? kNaN : lf1;
+      }
+    }
+    if (tg == 1) {
+#pragma unroll
+      for (int nt = 0; nt < kONt; ++nt) {
+        if constexpr (S::XV == 4) {
+          *reinterpret_cast<float4*>(&s.xbuf[xp][dp][nt][lane][0]) =
+              make_float4(oacc[nt][0], oacc[nt][1], oacc[nt][2], oacc[nt][3]);
+        } else {
+          *reinterpret_cast<float2*>(&s.xbuf[xp][dp][nt][lane][0]) = make_float2(oacc[nt][0], oacc[nt][1]);
         }
       }
     }
-    if (!split) continue;
-
-    // ---- S8: the last CTA to finish this item merges all partials ----------
-    __threadfence();
     if (!cons_sync()) break;
-    const int item = hd.b * nvh + hd.vh;
-    if (ct == 0) {
-      const int prev = atomicAdd(a.counters + item, 1);
-      const int last = (prev == hd.nsplit - 1) ? 1 : 0;
-      if (last) atomicExch(a.counters + item, 0);
-      s.flag_last = last;
-    }
-    if (!cons_sync()) break;
-    if (!s.flag_last) continue;
-    __threadfence();
-    const int c_first = part.owner(hd.item_u);
-    // Each thread owns 4 columns of one row and merges the partials online,
-    // eight at a time so their loads are all in flight together.
-    for (int e0 = ct * 4; e0 < G * D; e0 += NC * 4) {
-      const int i = e0 / D, d0 = e0 - i * D;
-      if (i >= hd.gq) continue;
-      float Mr = kNegInf, Lr = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int k0 = 0; k0 < hd.nsplit; k0 += 8) {
-        float2 ml[8];
-        float4 ov[8];
+    if (tg == 0) {
+      // merge the two token halves: rows gid (and gid + 8), this warp's columns
+      float f0[2], f1[2], inv[2], Ms[2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k0 + k < hd.nsplit) {
-            const int sl = part.slot(c_first + k0 + k, hd.item_u);
-            ml[k] = __ldcg(reinterpret_cast<const float2*>(a.part_ml + (static_cast<size_t>(sl) * G + i) * 2));
-            ov[k] = __ldcg(reinterpret_cast<const float4*>(a.part_o + (static_cast<size_t>(sl) * G + i) * D + d0));
+      for (int rr = 0; rr < (kTwoRows ? 2 : 1); ++rr) {
+        const int row = gid + 8 * rr;
+        const float m0 = rm[0][row], m1 = rm[1][row];
+        const float Mx = fmaxf(m0, m1);
+        Ms[rr] = (Mx == kNegInf) ? 0.f : Mx;
+        f0[rr] = exp2f(m0 - Ms[rr]);
+        f1[rr] = exp2f(m1 - Ms[rr]);
+        const float L = rl[0][row] * f0[rr] + rl[1][row] * f1[rr];
+        inv[rr] = 1.f / L;
+        if (split && dp == 0 && tig == 0 && row < hd.gq)
+          *reinterpret_cast<float4*>(a.part_ml + (static_cast<size_t>(hd.slot) * G + row) * 4) =
+              make_float4(Ms[rr], L, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int nt = 0; nt < kONt; ++nt) {
+        const int d = dp * (D / 2) + nt * 8 + 2 * tig;
+        float o[4];
+        if constexpr (S::XV == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(&s.xbuf[xp][dp][nt][lane][0]);
+          o[0] = (oacc[nt][0] * f0[0] + x.x * f1[0]) * inv[0];
+          o[1] = (oacc[nt][1] * f0[0] + x.y * f1[0]) * inv[0];
+          o[2] = (oacc[nt][2] * f0[1] + x.z * f1[1]) * inv[1];
+          o[3] = (oacc[nt][3] * f0[1] + x.w * f1[1]) * inv[1];
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(&s.xbuf[xp][dp][nt][lane][0]);
+          o[0] = (oacc[nt][0] * f0[0] + x.x * f1[0]) * inv[0];
+          o[1] = (oacc[nt][1] * f0[0] + x.y * f1[0]) * inv[0];
+          o[2] = o[3] = 0.f;
+        }
+#pragma unroll
+        for (int rr = 0; rr < (kTwoRows ? 2 : 1); ++rr) {
+          const int row = gid + 8 * rr;
+          if (row >= hd.gq) continue;
+          if (!split) {
+            T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + row) * D + d;
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16(o[2 * rr], o[2 * rr + 1]);
           } else {
-            ml[k] = make_float2(kNegInf, 0.f);
-            ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float2*>(a.part_o + (static_cast<size_t>(hd.slot) * G + row) * D + d) =
+                make_float2(o[2 * rr], o[2 * rr + 1]);
           }
         }
+      }
+    }
+  }
+  if (!split) continue;
+
+  // ---- S8 bookkeeping: the last CTA to finish this item owes its combine --
+  __threadfence();
+  if (!cons_sync()) break;
+  if (ct == 0) {
+    const int item = hd.b * nvh + hd.vh;
+    const int prev = atomicAdd(a.counters + item, 1);
+    if (prev == hd.nsplit - 1) {
+      atomicExch(a.counters + item, 0);
+      __threadfence();
+      // Only a CTA's first and last segments can be split, so at most two.
+      if (s.pend_n < 2) s.pend[s.pend_n++] = PendingCombine{hd.b, hd.vh, hd.nsplit, hd.gq, hd.item_u};
+    }
+  }
+  }  // segment loop
+
+  // ===================== S8: deferred LSE combines ============================
+  // Run after this CTA consumed all its tiles, so the stage ring is free to
+  // stage every partial of an item with cp.async (all loads in flight at
+  // once) before merging them from shared memory.
+  if (!alive) return;
+  if (!cons_sync()) return;
+  const int n_pend = s.pend_n;
+  unsigned char* ring = reinterpret_cast<unsigned char*>(&s.k[0][0]);
+  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(T);
+  constexpr int kChunksPerRow = D / 4;  // 16-byte chunks of an fp32 row
+  for (int pi = 0; pi < n_pend; ++pi) {
+    const PendingCombine pc = s.pend[pi];
+    const int h = pc.vh / a.subgroups, sub = pc.vh - h * a.subgroups;
+    const int q_row0 = h * a.group + sub * G;
+    const int gq = pc.gq;
+    const int c_first = part.owner(pc.item_u);
+    const int first_bit = part.start(c_first) < pc.item_u ? 1 : 0;
+    // partial slot of the k-th CTA sharing the item (later CTAs start inside it)
+    auto slot_of = [&](int k) { return 2 * (c_first + k) + (k == 0 ? first_bit : 0); };
+    const int rec = gq * (D * 4 + 16);
+    const int per_round = static_cast<int>(kRingBytes / rec);
+    float* so = reinterpret_cast<float*>(ring);
+    // online merge state for this thread's output chunks (row i, 4 columns)
+    constexpr int kMaxOwn = (G * kChunksPerRow + NC - 1) / NC;
+    float Mr[kMaxOwn], Lr[kMaxOwn], acc4[kMaxOwn][4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k0 + k >= hd.nsplit) continue;
-          const float Mn = fmaxf(Mr, ml[k].x);
-          const float sc_old = exp2f(Mr - Mn);  // Mr = -inf the first time -> 0
-          const float w = ml[k].y * exp2f(ml[k].x - Mn);
-          Lr = Lr * sc_old + w;
-          o[0] = o[0] * sc_old + w * ov[k].x;
-          o[1] = o[1] * sc_old + w * ov[k].y;
-          o[2] = o[2] * sc_old + w * ov[k].z;
-          o[3] = o[3] * sc_old + w * ov[k].w;
-          Mr = Mn;
+    for (int q = 0; q < kMaxOwn; ++q) {
+      Mr[q] = kNegInf;
+      Lr[q] = 0.f;
+      acc4[q][0] = acc4[q][1] = acc4[q][2] = acc4[q][3] = 0.f;
+    }
+    for (int k0 = 0; k0 < pc.nsplit; k0 += per_round) {
+      const int nk = min(per_round, pc.nsplit - k0);
+      if (!cons_sync()) return;  // everyone is done reading the previous round
+      float* sml = so + static_cast<size_t>(nk) * gq * D;
+      const int n_o = nk * gq * kChunksPerRow;
+      for (int qc = ct; qc < n_o + nk * gq; qc += NC) {
+        if (qc < n_o) {
+          const int k = qc / (gq * kChunksPerRow), rem = qc - k * (gq * kChunksPerRow);
+          const int i = rem / kChunksPerRow, cc = rem - i * kChunksPerRow;
+          cp_async_16(smem_addr(so + (static_cast<size_t>(k) * gq + i) * D + 4 * cc),
+                      a.part_o + (static_cast<size_t>(slot_of(k0 + k)) * G + i) * D + 4 * cc);
+        } else {
+          const int q2 = qc - n_o, k = q2 / gq, i = q2 - k * gq;
+          cp_async_16(smem_addr(sml + (static_cast<size_t>(k) * gq + i) * 4),
+                      a.part_ml + (static_cast<size_t>(slot_of(k0 + k)) * G + i) * 4);
         }
       }
-      T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D + d0;
+      cp_async_wait_all();
+      if (!cons_sync()) return;
+#pragma unroll
+      for (int q = 0; q < kMaxOwn; ++q) {
+        const int oc = ct + q * NC;
+        if (oc >= gq * kChunksPerRow) continue;
+        const int i = oc / kChunksPerRow, cc = oc - i * kChunksPerRow;
+        for (int k = 0; k < nk; ++k) {
+          const float4 ml = *reinterpret_cast<const float4*>(sml + (static_cast<size_t>(k) * gq + i) * 4);
+          const float4 ov = *reinterpret_cast<const float4*>(so + (static_cast<size_t>(k) * gq + i) * D + 4 * cc);
+          const float Mn = fmaxf(Mr[q], ml.x);
+          const float sc_old = exp2f(Mr[q] - Mn);  // -inf the first time -> 0
+          const float w = ml.y * exp2f(ml.x - Mn);
+          Lr[q] = Lr[q] * sc_old + w;
+          acc4[q][0] = acc4[q][0] * sc_old + w * ov.x;
+          acc4[q][1] = acc4[q][1] * sc_old + w * ov.y;
+          acc4[q][2] = acc4[q][2] * sc_old + w * ov.z;
+          acc4[q][3] = acc4[q][3] * sc_old + w * ov.w;
+          Mr[q] = Mn;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kMaxOwn; ++q) {
+      const int oc = ct + q * NC;
+      if (oc >= gq * kChunksPerRow) continue;
+      const int i = oc / kChunksPerRow, cc = oc - i * kChunksPerRow;
+      const float inv = 1.f / Lr[q];
+      T* row = static_cast<T*>(a.out) + (static_cast<size_t>(pc.b) * a.num_q_heads + q_row0 + i) * D + 4 * cc;
       if constexpr (sizeof(T) == 2) {
-        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(o[0] / Lr, o[1] / Lr), pack_bf16(o[2] / Lr, o[3] / Lr));
+        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(acc4[q][0] * inv, acc4[q][1] * inv),
+                                                    pack_bf16(acc4[q][2] * inv, acc4[q][3] * inv));
       } else {
-        *reinterpret_cast<float4*>(row) = make_float4(o[0] / Lr, o[1] / Lr, o[2] / Lr, o[3] / Lr);
+        *reinterpret_cast<float4*>(row) =
+            make_float4(acc4[q][0] * inv, acc4[q][1] * inv, acc4[q][2] * inv, acc4[q][3] * inv);
       }
     }
   }

@@ -64,7 +64,7 @@ int group_tile_for(int group, vt_dtype dtype) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout: [status word (256 B) | counter region | partial (m, l) | partial rows].
+// Workspace layout: [status word (256 B) | counter region | partial (m, l, 0, 0) | partial rows].
 // The counter region is reserved at allocation and never holds anything but
 // arrival counters, which every kernel leaves at zero; partials start after it.
 struct WsNeed {
@@ -77,7 +77,7 @@ WsNeed ws_need(int num_seqs, int nvh, int grid, int group_tile, int head_dim) {
   WsNeed n;
   n.counters_bytes = static_cast<size_t>(num_seqs) * nvh * sizeof(int);
   const size_t slots = 2 * static_cast<size_t>(grid);
-  n.ml_bytes = align_up(slots * group_tile * 2 * sizeof(float), 256);
+  n.ml_bytes = align_up(slots * group_tile * 4 * sizeof(float), 256);
   n.o_bytes = slots * group_tile * head_dim * sizeof(float);
   return n;
 }
