@@ -433,7 +433,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       mbar_init(&s.full[st], 1);
       mbar_init(&s.empty[st], NCW);
     }
-    mbar_init(&s.csync, NC);
+    mbar_init(&s.csync, NCW);  // one arrival per consumer warp
     s.abort_flag = 0;
     s.b_start_s = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -626,9 +626,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   const float kNegInf = -__int_as_float(0x7f800000);
   const float kNaN = __int_as_float(0x7fc00000);
   uint32_t sync_phase = 0;
+  // Rendezvous of the consumer warps.  One elected lane per warp arrives
+  // (after __syncwarp has ordered the warp's shared-memory writes): 128
+  // arrivals on one mbarrier word serialise and cost microseconds.
   auto cons_sync = [&]() -> bool {
-    mbar_arrive(&s.csync);
-    const bool r = wait_phase(&s.csync, sync_phase, &s.abort_flag, a.status, kStatusSync);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.csync);
+    bool r = wait_phase(&s.csync, sync_phase, &s.abort_flag, a.status, kStatusSync);
+    r = __all_sync(0xffffffffu, r);
     sync_phase ^= 1u;
     return r;
   };

@@ -23,7 +23,7 @@ using vt::VariantInfo;
 
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr int kMaxGroupTile = 8;
-constexpr int kDefaultMinUnits = 8;
+constexpr int kDefaultMinUnits = 2;
 
 thread_local int g_override_grid = 0;
 thread_local int g_override_min_units = 0;
