@@ -48,7 +48,8 @@ typedef enum {
   VT_ERR_UNSUPPORTED = 2,   /* well-formed but not implemented (head_dim, block_size, group) */
   VT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see vt_last_cuda_error() */
   VT_ERR_OOM = 4,           /* the split workspace could not be allocated */
-  VT_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up a bounded wait (see vt_paged_attn_device_status) */
+  VT_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up a bounded wait (see vt_paged_attn_device_status) */
+  VT_ERR_SCRATCH_LIMIT = 6   /* vt_paged_attn_decode_noalloc: the call needs more than its fixed scratch */
 } vt_status;
 
 typedef enum { VT_BF16 = 0, VT_F32 = 1 } vt_dtype;
@@ -91,6 +92,48 @@ VT_API vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_ca
                                int block_size, float scale, int window,
                                vt_stream_t stream, int max_blocks_per_seq,
                                int num_blocks, vt_dtype dtype);
+
+/*
+ * vt_paged_attn_decode_noalloc -- the same decode, for callers that cannot
+ * allocate device memory.  The pages this library follows have no
+ * counterpart to it; it exists for the caller's sake.
+ *
+ * vt_paged_attn_decode allocates its split scratch (partial results and
+ * arrival counters) itself, on first use and whenever a call needs more,
+ * with cudaMallocAsync.  Some callers cannot let a library do that: serving
+ * engines that hand nearly all device memory to their KV-cache pool up front,
+ * programs whose device memory belongs to one external allocator or arena
+ * that no library may bypass, and latency-critical decode loops where a
+ * library may not enter the CUDA allocator after start-up.  This entry point
+ * never allocates: it takes its scratch from one file-scope device array of
+ * VT_NOALLOC_SCRATCH_BYTES (8 MiB), which every GPU that loads the library
+ * holds until the process exits.  The caller still passes q, the caches, the
+ * tables and out, exactly as for vt_paged_attn_decode; arguments, layouts,
+ * results and error codes are the same.
+ *
+ * - The first call on each device looks up the array's device address with
+ *   that device current (a one-time set-up); make that first call before
+ *   any stream capture.
+ * - A call whose scratch would exceed the array (very large batches, or a
+ *   very large forced grid) returns VT_ERR_SCRATCH_LIMIT before launching
+ *   anything; vt_last_cuda_error() names the sizes.
+ * - All calls share the one array and it keeps the previous call's contents;
+ *   each call clears the parts that must start at zero (status word and
+ *   arrival counters) on its stream first.  Calls that overlap on the GPU
+ *   (concurrent streams, or several host threads) race on the array and
+ *   produce wrong results: order them.
+ * - The status word of bounded waits lives in the array and is cleared by
+ *   the next call; vt_paged_attn_device_status does not read it.
+ * - Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define VT_NOALLOC_SCRATCH_BYTES (8u << 20)
+VT_API vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              const int32_t* context_lens, int num_seqs,
+                                              int num_q_heads, int num_kv_heads, int head_dim,
+                                              int block_size, float scale, int window,
+                                              vt_stream_t stream, int max_blocks_per_seq,
+                                              int num_blocks, vt_dtype dtype);
 
 /* What the last successful vt_paged_attn_decode on this host thread launched. */
 typedef struct {

@@ -15,11 +15,12 @@ from pathlib import Path
 
 LIBRARY_PATH = Path(__file__).resolve().parent / "_build" / "libvt_paged_attn.so"
 
-VT_OK, VT_ERR_INVALID_ARG, VT_ERR_UNSUPPORTED, VT_ERR_CUDA, VT_ERR_OOM, VT_ERR_DEVICE_TIMEOUT = range(6)
+(VT_OK, VT_ERR_INVALID_ARG, VT_ERR_UNSUPPORTED, VT_ERR_CUDA, VT_ERR_OOM, VT_ERR_DEVICE_TIMEOUT,
+ VT_ERR_SCRATCH_LIMIT) = range(7)
 VT_BF16, VT_F32 = 0, 1
 BLOCK_SIZE = 32
 
-EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_last_plan", "vt_paged_attn_set_override",
+EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_last_plan", "vt_paged_attn_set_override",
             "vt_paged_attn_device_status", "vt_paged_attn_device_status_detail", "vt_paged_attn_workspace_bytes", "vt_paged_attn_release",
             "vt_status_string", "vt_last_cuda_error", "vt_paged_attn_version")
 
@@ -64,6 +65,8 @@ def library() -> ctypes.CDLL:
             lib.vt_paged_attn_decode.argtypes = [c_void] * 6 + [c_int] * 5 + [c_float, c_int, c_void, c_int,
                                                                                c_int, c_int]
             lib.vt_paged_attn_decode.restype = c_int
+            lib.vt_paged_attn_decode_noalloc.argtypes = lib.vt_paged_attn_decode.argtypes
+            lib.vt_paged_attn_decode_noalloc.restype = c_int
             lib.vt_paged_attn_last_plan.argtypes = [ctypes.POINTER(vt_plan)]
             lib.vt_paged_attn_last_plan.restype = c_int
             lib.vt_paged_attn_set_override.argtypes = [c_int, c_int]
@@ -104,6 +107,17 @@ def vt_paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, n
     return library().vt_paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                                           num_q_heads, num_kv_heads, head_dim, block_size, float(scale),
                                           int(window), stream, max_blocks_per_seq, num_blocks, dtype)
+
+
+def vt_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                                 num_kv_heads, head_dim, block_size, scale, window, stream, max_blocks_per_seq,
+                                 num_blocks, dtype) -> int:
+    """Raw call of the allocation-free entry point (scratch in a fixed static
+    device array instead of a library allocation); returns the status code."""
+    return library().vt_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                                  num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                                  float(scale), int(window), stream, max_blocks_per_seq,
+                                                  num_blocks, dtype)
 
 
 def vt_paged_attn_last_plan() -> dict:

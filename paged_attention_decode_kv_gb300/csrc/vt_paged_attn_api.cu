@@ -259,6 +259,7 @@ const char* vt_status_string(vt_status s) {
     case VT_ERR_CUDA: return "CUDA error";
     case VT_ERR_OOM: return "out of device memory";
     case VT_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case VT_ERR_SCRATCH_LIMIT: return "call needs more scratch than the static buffer holds";
   }
   return "unknown status";
 }
@@ -393,6 +394,148 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   g_last_plan.dtype = dtype;
   g_last_plan.smem_bytes = v->smem_bytes;
   g_last_plan.workspace_bytes = ws_used;
+  g_have_plan = true;
+  return VT_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the split scratch is a fixed, file-scope device
+// array instead of the library's lazily allocated per-device workspace.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = VT_NOALLOC_SCRATCH_BYTES;  // held on every device that loads the library
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+std::vector<void*> g_noalloc_ptr;  // device address of the array, per device
+
+// In host code the array's name is only a host-side stand-in: its device
+// address must be looked up, once per device, with that device current.
+vt_status noalloc_scratch(int dev, void** ptr) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (static_cast<int>(g_noalloc_ptr.size()) <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return VT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                       float scale, int window, vt_stream_t stream_handle, int max_blocks_per_seq,
+                                       int num_blocks, vt_dtype dtype) {
+  if (num_seqs < 0) return VT_ERR_INVALID_ARG;
+  if (num_seqs == 0) return VT_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return VT_ERR_INVALID_ARG;
+  if (dtype != VT_BF16 && dtype != VT_F32) return VT_ERR_INVALID_ARG;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return VT_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0 || head_dim <= 0) return VT_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return VT_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return VT_ERR_INVALID_ARG;
+  if (head_dim != 128 && head_dim != 256) return VT_ERR_UNSUPPORTED;
+  if (block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
+
+  const int group = num_q_heads / num_kv_heads;
+  const int gt = group_tile_for(group, dtype);
+  const int subgroups = (group + gt - 1) / gt;
+  const long long nvh = static_cast<long long>(num_kv_heads) * subgroups;
+  if (nvh * num_seqs > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
+  const VariantInfo* v = find_variant(head_dim, dtype, gt);
+  if (!v) return VT_ERR_UNSUPPORTED;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+  int grid = 0, per_sm = 0, min_units = 0, num_sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& ds = device_state(dev);
+    vt_status st = prepare_device(dev, ds);
+    if (st != VT_OK) return st;
+    st = prepare_variant(ds, *v, &per_sm);
+    if (st != VT_OK) return st;
+    grid = g_override_grid > 0 ? g_override_grid : ds.num_sms * per_sm;
+    min_units = g_override_min_units > 0 ? g_override_min_units : kDefaultMinUnits;
+    num_sms = ds.num_sms;
+  }
+  // Layout inside the fixed array: [status 256 B | counters | partial (m, l) | partial rows].
+  const WsNeed need = ws_need(num_seqs, static_cast<int>(nvh), grid, gt, head_dim);
+  const size_t counters_region = align_up(need.counters_bytes, 256);
+  const size_t total = 256 + counters_region + need.ml_bytes + need.o_bytes;
+  if (total > kNoAllocScratchBytes) {
+    g_last_cuda_error = "vt_paged_attn_decode_noalloc: this call needs " + std::to_string(total) +
+                        " bytes of scratch; the static buffer holds " + std::to_string(kNoAllocScratchBytes);
+    return VT_ERR_SCRATCH_LIMIT;
+  }
+  void* base_ptr = nullptr;
+  vt_status st = noalloc_scratch(dev, &base_ptr);
+  if (st != VT_OK) return st;
+  char* base = static_cast<char*>(base_ptr);
+  // The array keeps the previous call's contents: the status word and the
+  // arrival counters must start at zero.
+  e = cudaMemsetAsync(base, 0, 256 + counters_region, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+
+  CUtensorMap tk, tv;
+  st = tensor_map(MapKey{k_cache, head_dim, num_kv_heads, num_blocks, dtype, dev}, &tk);
+  if (st != VT_OK) return st;
+  st = tensor_map(MapKey{v_cache, head_dim, num_kv_heads, num_blocks, dtype, dev}, &tv);
+  if (st != VT_OK) return st;
+
+  DecodeArgs args{};
+  args.status = reinterpret_cast<unsigned*>(base);
+  args.counters = reinterpret_cast<int*>(base + 256);
+  args.part_ml = reinterpret_cast<float*>(base + 256 + counters_region);
+  args.part_o = reinterpret_cast<float*>(base + 256 + counters_region + need.ml_bytes);
+  args.out = out;
+  args.q = q;
+  args.block_tables = block_tables;
+  args.context_lens = context_lens;
+  args.num_seqs = num_seqs;
+  args.num_q_heads = num_q_heads;
+  args.num_kv_heads = num_kv_heads;
+  args.group = group;
+  args.subgroups = subgroups;
+  args.max_blocks = max_blocks_per_seq;
+  args.num_blocks = num_blocks;
+  args.window = window > 0 ? window : 0;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  args.min_units = min_units;
+
+  e = v->launch(tk, tv, args, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+
+  g_last_plan.num_sms = num_sms;
+  g_last_plan.grid_ctas = grid;
+  g_last_plan.ctas_per_sm = per_sm;
+  g_last_plan.consumer_warps = v->consumer_warps;
+  g_last_plan.tensor_cores = v->tensor_cores;
+  g_last_plan.stages = v->stages;
+  g_last_plan.group_tile = gt;
+  g_last_plan.subgroups = subgroups;
+  g_last_plan.min_units_per_cta = min_units;
+  g_last_plan.head_dim = head_dim;
+  g_last_plan.dtype = dtype;
+  g_last_plan.smem_bytes = v->smem_bytes;
+  g_last_plan.workspace_bytes = total;
   g_have_plan = true;
   return VT_OK;
 }
