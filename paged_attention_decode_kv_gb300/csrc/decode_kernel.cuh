@@ -215,6 +215,18 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+// Arrival counter increment with acquire-release semantics at GPU scope: the
+// release orders every store the CTA made before the preceding rendezvous,
+// the acquire lets the last arriver see the other CTAs' partials.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void st_relaxed_gpu(int* p, int v) {
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -546,8 +558,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
+            const bool bad = pid < 0 || pid >= a.num_blocks;
             if (lane == 0) {
-              const bool bad = pid < 0 || pid >= a.num_blocks;
               const int first_tok = (sp.p_lo + p) * kPageTokens;
               StageHeader& hd = s.hdr[stage];
               hd.b = b;
@@ -563,26 +575,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               uint32_t bytes = bad ? 0u : 2u * kTileBytes;
               if (p == pa) bytes += static_cast<uint32_t>(gq) * D * sizeof(T);
               mbar_arrive_expect_tx(&s.full[stage], bytes);
-              if (!bad) {
-                if constexpr (kMma) {
-                  // 128-byte swizzled sub-tiles of 64 columns: [D/64][32 tokens][64]
-#pragma unroll
-                  for (int sb = 0; sb < D / kSwizzleCols; ++sb) {
-                    tma_load_3d(s.k[stage] + sb * kPageTokens * kSwizzleCols, &tmap_k, sb * kSwizzleCols, h,
-                                pid * kPageTokens, &s.full[stage]);
-                    tma_load_3d(s.v[stage] + sb * kPageTokens * kSwizzleCols, &tmap_v, sb * kSwizzleCols, h,
-                                pid * kPageTokens, &s.full[stage]);
-                  }
-                } else {
-                  tma_load_3d(s.k[stage], &tmap_k, 0, h, pid * kPageTokens, &s.full[stage]);
-                  tma_load_3d(s.v[stage], &tmap_v, 0, h, pid * kPageTokens, &s.full[stage]);
-                }
-              }
-              if (p == pa) {
-                const T* qsrc = static_cast<const T*>(a.q) +
-                                (static_cast<size_t>(b) * a.num_q_heads + q_row0) * D;
-                bulk_load(s.q[stage], qsrc, static_cast<uint32_t>(gq) * D * sizeof(T), &s.full[stage]);
-              }
+            }
+            __syncwarp();
+            // Each copy is issued by its own lane: a TMA instruction occupies its
+            // issuing thread for tens of cycles, so one lane issuing them all
+            // would serialise the page gather.
+            constexpr int kBoxes = kMma ? D / kSwizzleCols : 1;  // boxes per K (or V) tile
+            if (!bad && lane < 2 * kBoxes) {
+              const int sb = lane >> 1;
+              const bool is_v = (lane & 1) != 0;
+              T* dst = (is_v ? s.v[stage] : s.k[stage]) + (kMma ? sb * kPageTokens * kSwizzleCols : 0);
+              tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, kMma ? sb * kSwizzleCols : 0, h, pid * kPageTokens,
+                          &s.full[stage]);
+            }
+            if (p == pa && lane == 31) {
+              const T* qsrc = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.num_q_heads + q_row0) * D;
+              bulk_load(s.q[stage], qsrc, static_cast<uint32_t>(gq) * D * sizeof(T), &s.full[stage]);
             }
             __syncwarp();
             ++issued;
@@ -1071,14 +1079,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   if (!split) continue;
 
   // ---- S8 bookkeeping: the last CTA to finish this item owes its combine --
-  __threadfence();
+  // The rendezvous orders every consumer's partial stores before thread 0's
+  // release-acquire increment (one GPU-scope round trip instead of a fence
+  // in every thread plus an atomic plus another fence).
   if (!cons_sync()) break;
   if (ct == 0) {
     const int item = hd.b * nvh + hd.vh;
-    const int prev = atomicAdd(a.counters + item, 1);
+    const int prev = atom_add_acq_rel_gpu(a.counters + item, 1);
     if (prev == hd.nsplit - 1) {
-      atomicExch(a.counters + item, 0);
-      __threadfence();
+      st_relaxed_gpu(a.counters + item, 0);  // every other CTA has arrived: reset for the next call
       // Only a CTA's first and last segments can be split, so at most two.
       if (s.pend_n < 2) s.pend[s.pend_n++] = PendingCombine{hd.b, hd.vh, hd.nsplit, hd.gq, hd.item_u};
     }
