@@ -4,8 +4,9 @@
 One step = one vt_paged_attn_decode call over one synthetic decode batch
 (request lookup, page gather, QK^T, mask, online softmax, PV, split partials,
 LSE combine, finalize: the whole hot path, one kernel launch).  Inputs sit in
-HBM before timing starts.  L2 is flushed (a 2x-L2 write) before every timed
-call, outside the call's CUDA events, so K/V come from HBM.
+HBM before timing starts.  Calls rotate over copies of the KV pool holding at
+least 2x L2 of referenced KV bytes, so every call reads its pages from HBM
+(no flush kernel: its dirty lines would be written back during the call).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 instead (the reference arm: a deliberately plain fp64 program on host cores).
@@ -125,30 +126,44 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def make_device_case(name: str, seed: int, device):
+ROTATE_BYTES = 256 << 20  # distinct KV bytes read between two uses of the same pool copy (2x L2)
+
+
+def make_device_case(name: str, seed: int, device, pool_blocks: int = 0):
+    """The workload on the device, with enough copies of its KV pool that
+    consecutive calls never find their pages in L2: copy c serves calls
+    c, c + n, ..., and n copies hold >= 2x L2 of referenced KV bytes.
+    pool_blocks > 0 shrinks the page pool (same contexts and pages used)."""
     from paged_attention_decode_kv_gb300 import workloads as W
-    case = W.make_case(W.WORKLOADS[name], seed)
+    w = W.WORKLOADS[name]
+    if pool_blocks > 0:
+        w = w.with_(pool_blocks=pool_blocks)
+    case = W.make_case(w, seed)
     k, v = case.pool(device)
-    return case, {"q": case.q.to(device), "k": k, "v": v, "bt": case.block_tables.to(device),
-                  "cl": case.context_lens.to(device)}
+    n_copies = max(2, -(-ROTATE_BYTES // max(case.kv_bytes(), 1)) + 1)
+    pools = [(k, v)] + [(k.clone(), v.clone()) for _ in range(n_copies - 1)]
+    return case, {"q": case.q.to(device), "pools": pools, "k": k, "v": v,
+                  "bt": case.block_tables.to(device), "cl": case.context_lens.to(device)}
 
 
-def time_calls(vt, case, t, steps, warmup, flush):
-    """Per-call CUDA-event times (s) on the launching stream, L2 flushed before each."""
+def time_calls(vt, case, t, steps, warmup):
+    """Per-call CUDA-event times (s) on the launching stream; call s reads pool
+    copy s mod n, so its KV pages come from HBM, not L2."""
     import torch
     w = case.workload
     out = torch.empty_like(t["q"])
     stream = torch.cuda.current_stream()
-    for _ in range(warmup):
-        flush.zero_()
-        vt.decode(t["q"], t["k"], t["v"], t["bt"], t["cl"], w.scale, w.window, out=out)
+    pools = t["pools"]
+    for i in range(warmup):
+        k, v = pools[i % len(pools)]
+        vt.decode(t["q"], k, v, t["bt"], t["cl"], w.scale, w.window, out=out)
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for s in range(steps):
-        flush.zero_()
+        k, v = pools[(warmup + s) % len(pools)]
         starts[s].record(stream)
-        vt.decode(t["q"], t["k"], t["v"], t["bt"], t["cl"], w.scale, w.window, out=out)
+        vt.decode(t["q"], k, v, t["bt"], t["cl"], w.scale, w.window, out=out)
         ends[s].record(stream)
     torch.cuda.synchronize()
     status = vt.vt_paged_attn_device_status()
@@ -157,9 +172,10 @@ def time_calls(vt, case, t, steps, warmup, flush):
     return [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)]
 
 
-def time_e2e(vt, case, t, steps, warmup, flush):
+def time_e2e(vt, case, t, steps, warmup):
     """Through the C-ABI with host buffers: pinned H2D of the step's inputs
-    (q, block table, context lengths), the decode, D2H of the output."""
+    (q, block table, context lengths), the decode, D2H of the output.  The KV
+    pool is resident state (rotated across copies as in time_calls)."""
     import torch
     w = case.workload
     hq = case.q.pin_memory()
@@ -169,24 +185,24 @@ def time_e2e(vt, case, t, steps, warmup, flush):
     dq, dbt, dcl = torch.empty_like(t["q"]), torch.empty_like(t["bt"]), torch.empty_like(t["cl"])
     out = torch.empty_like(t["q"])
     stream = torch.cuda.current_stream()
+    pools = t["pools"]
 
-    def step():
+    def step(i):
+        k, v = pools[i % len(pools)]
         dq.copy_(hq, non_blocking=True)
         dbt.copy_(hbt, non_blocking=True)
         dcl.copy_(hcl, non_blocking=True)
-        vt.decode(dq, t["k"], t["v"], dbt, dcl, w.scale, w.window, out=out)
+        vt.decode(dq, k, v, dbt, dcl, w.scale, w.window, out=out)
         hout.copy_(out, non_blocking=True)
 
-    for _ in range(warmup):
-        flush.zero_()
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for s in range(steps):
-        flush.zero_()
         starts[s].record(stream)
-        step()
+        step(warmup + s)
         ends[s].record(stream)
     torch.cuda.synchronize()
     h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hcl.numel() * 4
@@ -269,6 +285,27 @@ def summarize(times):
             "p10_us": s[len(s) // 10] * 1e6, "p90_us": s[(9 * len(s)) // 10] * 1e6}
 
 
+def run_profile_only(args):
+    """A short, fixed run of one workload for ncu captures (no timing and no
+    JSON line): warm-up calls plus --steps calls, pools rotated as in the bench."""
+    import torch
+    import paged_attention_decode_kv_gb300 as vt
+    from paged_attention_decode_kv_gb300 import build_lib
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    case, t = make_device_case(args.workload, args.seed, dev, args.pool_blocks)
+    w = case.workload
+    out = torch.empty_like(t["q"])
+    for i in range(args.warmup + args.steps):
+        k, v = t["pools"][i % len(t["pools"])]
+        vt.decode(t["q"], k, v, t["bt"], t["cl"], w.scale, w.window, out=out)
+    torch.cuda.synchronize()
+    status = vt.vt_paged_attn_device_status()
+    print(f"profile-only {w.name}: {args.warmup} + {args.steps} calls, kv bytes {case.kv_bytes()}, "
+          f"status {status}, plan {vt.vt_paged_attn_last_plan()}")
+    return 1 if status else 0
+
+
 def run_ours(args, rank, world, dist):
     import torch
     import paged_attention_decode_kv_gb300 as vt
@@ -281,9 +318,6 @@ def run_ours(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     vt.library()
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 128 << 20)
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     peak, peak_src = hbm_peak()
 
     case, t = make_device_case(args.workload, args.seed + rank, dev)
@@ -297,16 +331,17 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        times = time_calls(vt, case, t, args.steps, args.warmup, flush)
+        times = time_calls(vt, case, t, args.steps, args.warmup)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     plan = vt.vt_paged_attn_last_plan()
     mean_s = max_over_ranks(statistics.mean(times), dist, dev)
-    e2e_times, h2d, d2h = time_e2e(vt, case, t, max(50, args.steps // 10), args.warmup, flush)
+    e2e_times, h2d, d2h = time_e2e(vt, case, t, max(50, args.steps // 10), args.warmup)
     e2e_s = max_over_ranks(statistics.mean(e2e_times), dist, dev)
 
     host_case = case
+    n_pool_copies = len(t["pools"])
     del t
     torch.cuda.empty_cache()
     sweep = []
@@ -315,7 +350,7 @@ def run_ours(args, rank, world, dist):
             if name == args.workload:
                 continue
             case_s, t_s = make_device_case(name, args.seed, dev)
-            ts = time_calls(vt, case_s, t_s, args.sweep_steps, 3, flush)
+            ts = time_calls(vt, case_s, t_s, args.sweep_steps, 3)
             m = statistics.mean(ts)
             a_bytes = case_s.kv_bytes() + case_s.qo_bytes()
             sweep.append({"workload": name, **summarize(ts), "kv_gbs": case_s.kv_bytes() / m / 1e9,
@@ -337,7 +372,8 @@ def run_ours(args, rank, world, dist):
                    "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "block_size": w.block_size, "storage_dtype": w.dtype, "window": w.window,
                    "context_tokens": context_tokens,
-                   "l2": "flushed before every timed call (2x L2 write, outside the call's events)",
+                   "l2": f"inputs larger than L2: calls rotate over {n_pool_copies} copies of the KV pool "
+                         f"(>= 256 MiB of distinct KV between reuses)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "per_call": summarize(times),
         "kv_gbs": kv / mean_s / 1e9,
@@ -362,7 +398,7 @@ def run_ours(args, rank, world, dist):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -370,9 +406,15 @@ def main(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=300)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=10.0, help="seconds of oracle work per reference sample")
+    ap.add_argument("--profile-only", action="store_true",
+                    help="run --warmup + --steps calls of --workload for a profiler; no timing, no JSON line")
+    ap.add_argument("--pool-blocks", type=int, default=0, help="shrink the page pool (profile-only runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+
+    if args.profile_only:
+        return run_profile_only(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
