@@ -108,7 +108,9 @@ struct Smem {
   static constexpr int GS = D / 8;
   static constexpr int NG = (M == Math::kSimt) ? NCW * 32 / GS : 1;
   static constexpr int TPG = kPageTokens / NG;
-  // mma layout: warps split (token half, head_dim half) of the page.
+  // mma layout: warps split the page into (token half tg) x (head_dim part dp),
+  // NCW / 2 head_dim parts.
+  static constexpr int NDP = (M == Math::kMma) ? NCW / 2 : 1;
   static constexpr int kRedRows = (M == Math::kSimt) ? NG : 2;
   alignas(1024) T k[NSTAGE][kPageTokens * D];
   alignas(1024) T v[NSTAGE][kPageTokens * D];
@@ -121,8 +123,8 @@ struct Smem {
   // fragments to the warps of token half 0 ([segment parity][dp][n-tile][lane]).
   static constexpr int XV = (G > 8) ? 4 : 2;  // live accumulator values per lane and n-tile
   static constexpr int XP = (M == Math::kMma) ? 2 : 1;
-  static constexpr int XN = (M == Math::kMma) ? D / 16 : 1;
-  alignas(16) float xbuf[XP][2][XN][32][XV];
+  static constexpr int XN = (M == Math::kMma) ? D / NDP / 8 : 1;
+  alignas(16) float xbuf[XP][NDP][XN][32][XV];
   // CUDA-core consumer only: per-group broadcast of p and the rescale factor.
   static constexpr int PG = (M == Math::kSimt) ? G : 1;
   static constexpr int PT = (M == Math::kSimt) ? TPG : 1;
@@ -427,7 +429,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int NC = NCW * 32;  // consumer threads
   constexpr uint32_t kTileBytes = kPageTokens * D * sizeof(T);
   constexpr bool kMma = MATH == Math::kMma;
-  static_assert(!kMma || (sizeof(T) == 2 && NCW == 4 && G <= 16 && D % 128 == 0), "mma consumer shape");
+  static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
+                "mma consumer shape");
   static_assert(kMma || (S::GS <= 32 && (32 % S::GS) == 0 && S::NG * S::TPG == kPageTokens &&
                          G <= S::GS && (S::GS % G) == 0), "CUDA-core consumer shape");
 
@@ -655,9 +658,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int kSpread = (GS / G) > 0 ? GS / G : 1;
   const int iq = c / kSpread;
   const bool owner = (c % kSpread) == 0;
-  // mma consumer (bf16): warp = (token half tg, head_dim half dp).
+  // mma consumer (bf16): warp = (token half tg, head_dim part dp).  Every
+  // warp computes S for its 16 tokens over the full head_dim (duplicated
+  // across the dp warps: tensor cores have ample headroom) and P V for its
+  // D / NDP output columns.
+  constexpr int NDP = S::NDP;
+  constexpr int kDPart = D / NDP;     // output columns per warp
   constexpr int kKSteps = D / 16;     // k-steps of QK^T over head_dim
-  constexpr int kONt = D / 16;        // 8-column output tiles per warp (half of head_dim)
+  constexpr int kONt = kDPart / 8;    // 8-column output tiles per warp
   constexpr bool kTwoRows = G > 8;    // second fragment row (queries 8..15) live
   const int tg = warp & 1, dp = warp >> 1;
   const int gid = lane >> 2, tig = lane & 3;
@@ -904,13 +912,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
                              ((tl + 1 >= hd.lo && tl + 1 < hd.hi) ? 0xffff0000u : 0u);
         const uint32_t mhi = ((tl + 8 >= hd.lo && tl + 8 < hd.hi) ? 0x0000ffffu : 0u) |
                              ((tl + 9 >= hd.lo && tl + 9 < hd.hi) ? 0xffff0000u : 0u);
-        // S6: O[:, this warp's half of head_dim] += P V over the 16 tokens.
+        // S6: O[:, this warp's head_dim part] += P V over the 16 tokens.
         {
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;
 #pragma unroll
           for (int np2 = 0; np2 < kONt / 2; ++np2) {
-            const int d = dp * (D / 2) + np2 * 16 + ((mi >> 1) << 3);
+            const int d = dp * kDPart + np2 * 16 + ((mi >> 1) << 3);
             const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
             const uint32_t addr = vbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
             uint32_t bv[4];
@@ -1047,7 +1055,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       }
 #pragma unroll
       for (int nt = 0; nt < kONt; ++nt) {
-        const int d = dp * (D / 2) + nt * 8 + 2 * tig;
+        const int d = dp * kDPart + nt * 8 + 2 * tig;
         float o[4];
         if constexpr (S::XV == 4) {
           const float4 x = *reinterpret_cast<const float4*>(&s.xbuf[xp][dp][nt][lane][0]);
