@@ -119,11 +119,12 @@ struct Smem {
   static constexpr int RG = (M == Math::kSimt) ? G : 1;
   static constexpr int RD = (M == Math::kSimt) ? D : 4;
   alignas(16) float red_acc[RG][RD];
-  // Tensor-core epilogue: warps of token half 1 hand their accumulator
-  // fragments to the warps of token half 0 ([segment parity][dp][n-tile][lane]).
-  static constexpr int XV = (G > 8) ? 4 : 2;  // live accumulator values per lane and n-tile
+  // Tensor-core epilogue: warps of token half 1 hand their O^T accumulator
+  // fragments to the warps of token half 0 ([segment parity][dp][m-tile][lane]);
+  // token half 0 then reuses its slice to stage rows for coalesced stores.
+  static constexpr int XV = (G > 8) ? 8 : 4;  // accumulator values per lane and m-tile
   static constexpr int XP = (M == Math::kMma) ? 2 : 1;
-  static constexpr int XN = (M == Math::kMma) ? D / NDP / 8 : 1;
+  static constexpr int XN = (M == Math::kMma) ? D / NDP / 16 : 1;
   alignas(16) float xbuf[XP][NDP][XN][32][XV];
   // CUDA-core consumer only: per-group broadcast of p and the rescale factor.
   static constexpr int PG = (M == Math::kSimt) ? G : 1;
@@ -248,6 +249,15 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose of an 8x8 b16 matrix held one 32-bit pair per lane (row lane/4,
+// columns 2(lane%4), +1): afterwards each lane holds the same positions of
+// the transposed matrix.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -658,15 +668,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int kSpread = (GS / G) > 0 ? GS / G : 1;
   const int iq = c / kSpread;
   const bool owner = (c % kSpread) == 0;
-  // mma consumer (bf16): warp = (token half tg, head_dim part dp).  Every
-  // warp computes S for its 16 tokens over the full head_dim (duplicated
-  // across the dp warps: tensor cores have ample headroom) and P V for its
-  // D / NDP output columns.
+  // mma consumer (bf16): warp = (token half tg, head_dim part dp).  The
+  // products are taken transposed, with the warp's 16 tokens as the M
+  // dimension and the query group as N (8 or 16): S^T = K Q^T over the full
+  // head_dim (repeated by the dp warps), O^T = V^T P^T for the warp's
+  // D / NDP output rows of O^T.  No M padding for groups of up to 8.
   constexpr int NDP = S::NDP;
-  constexpr int kDPart = D / NDP;     // output columns per warp
-  constexpr int kKSteps = D / 16;     // k-steps of QK^T over head_dim
-  constexpr int kONt = kDPart / 8;    // 8-column output tiles per warp
-  constexpr bool kTwoRows = G > 8;    // second fragment row (queries 8..15) live
+  constexpr int kDPart = D / NDP;        // O^T rows (head_dim columns of O) per warp
+  constexpr int kKSteps = D / 16;        // k-steps of S^T over head_dim
+  constexpr int kMt = kDPart / 16;       // 16-row m-tiles of O^T per warp
+  constexpr int NQT = (G > 8) ? 2 : 1;   // 8-query n-tiles
   const int tg = warp & 1, dp = warp >> 1;
   const int gid = lane >> 2, tig = lane & 3;
 
@@ -681,10 +692,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   while (alive && it < n_tiles) {
   float qf[kMma ? 1 : G][8];
   float acc[kMma ? 1 : G][8];
-  uint32_t qa[kMma ? kKSteps : 1][4];
-  float oacc[kMma ? kONt : 1][4];
-  float m_run = kNegInf, l_run = 0.f;     // simt: lane's query; mma: row gid
-  float m_run2 = kNegInf, l_run2 = 0.f;   // mma: row gid + 8
+  uint32_t qb[kMma ? kKSteps : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
+  float oacc[kMma ? kMt : 1][NQT][4];       // O^T accumulators
+  float m_run = kNegInf, l_run = 0.f;       // simt: the lane's query
+  float mq[NQT][2], lq[NQT][2];             // mma: queries 8n + 2tig + {0,1}
   bool poison = false;
   StageHeader hd;
   do {
@@ -790,24 +801,32 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     } else {
       // ======================== tensor-core consumer ==========================
       if (hd.flags & kFirst) {
-        // Q as the A operand of m16n8k16 (rows = queries, k = head_dim);
-        // rows at or past the live group are zero.
+        // Q^T as the B operand (k = head_dim, n = query): lane holds query
+        // 8n + gid, columns 16ks + 2tig (+1) and +8; queries past the live
+        // group are zero.
         const uint32_t* q32 = reinterpret_cast<const uint32_t*>(s.q[stage]);
-        const bool r0ok = gid < hd.gq, r1ok = kTwoRows && (gid + 8) < hd.gq;
 #pragma unroll
-        for (int ks = 0; ks < kKSteps; ++ks) {
-          const int col = ks * 16 + 2 * tig;
-          qa[ks][0] = r0ok ? q32[(gid * D + col) >> 1] : 0u;
-          qa[ks][1] = r1ok ? q32[((gid + 8) * D + col) >> 1] : 0u;
-          qa[ks][2] = r0ok ? q32[(gid * D + col + 8) >> 1] : 0u;
-          qa[ks][3] = r1ok ? q32[((gid + 8) * D + col + 8) >> 1] : 0u;
+        for (int n = 0; n < NQT; ++n) {
+          const int qr = 8 * n + gid;
+          const bool ok = qr < hd.gq;
+#pragma unroll
+          for (int ks = 0; ks < kKSteps; ++ks) {
+            const int col = ks * 16 + 2 * tig;
+            qb[ks][n][0] = ok ? q32[(qr * D + col) >> 1] : 0u;
+            qb[ks][n][1] = ok ? q32[(qr * D + col + 8) >> 1] : 0u;
+          }
         }
 #pragma unroll
-        for (int nt = 0; nt < kONt; ++nt)
+        for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) oacc[nt][e] = 0.f;
-        m_run = m_run2 = kNegInf;
-        l_run = l_run2 = 0.f;
+          for (int n = 0; n < NQT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[mt][n][e] = 0.f;
+#pragma unroll
+        for (int n = 0; n < NQT; ++n) {
+          mq[n][0] = mq[n][1] = kNegInf;
+          lq[n][0] = lq[n][1] = 0.f;
+        }
         poison = false;
       }
       if (hd.flags & kBadPage) {
@@ -815,122 +834,112 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       } else {
         const uint32_t kbase = smem_addr(s.k[stage]);
         const uint32_t vbase = smem_addr(s.v[stage]);
-        // S3: S = Q K^T for this warp's 16 tokens (two n8 tiles), full
-        // head_dim; even and odd k-steps accumulate separately (two short
-        // dependency chains instead of one long one).
-        float sacc[2][2][4];
+        // S3: S^T = K Q^T for this warp's 16 tokens; even and odd k-steps
+        // accumulate separately (two short MMA chains instead of one long).
+        float sacc[NQT][2][4];
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NQT; ++n)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sacc[n][hh][e] = 0.f;
         {
           const int mi = lane >> 3, r = lane & 7;
-          const int t = 16 * tg + ((mi >> 1) << 3) + r;  // token row this lane addresses
+          const int t = 16 * tg + ((mi & 1) << 3) + r;  // token row this lane addresses
 #pragma unroll
           for (int ks = 0; ks < kKSteps; ++ks) {
-            const int d = ks * 16 + ((mi & 1) << 3);
+            const int d = ks * 16 + ((mi >> 1) << 3);
             const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
-            const uint32_t addr = kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
-            uint32_t bk[4];
-            ldmatrix_x4(addr, bk);
-            mma_bf16(sacc[0][ks & 1], qa[ks], bk[0], bk[1]);
-            mma_bf16(sacc[1][ks & 1], qa[ks], bk[2], bk[3]);
+            uint32_t ak[4];
+            ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
+#pragma unroll
+            for (int n = 0; n < NQT; ++n) mma_bf16(sacc[n][ks & 1], ak, qb[ks][n][0], qb[ks][n][1]);
           }
         }
-        // S4 + S5: mask, scale, online softmax for rows gid and gid + 8.
-        float sv[2][4];
-        float mx0 = kNegInf, mx1 = kNegInf;
+        // S4 + S5: mask and scale; online softmax per query column.  Lane
+        // holds tokens 16tg + gid (values 0, 1) and + 8 (values 2, 3) of
+        // queries 8n + 2tig (values 0, 2) and + 1 (values 1, 3).
+        const int t_lo = 16 * tg + gid, t_hi = t_lo + 8;
+        const bool tok_lo = t_lo >= hd.lo && t_lo < hd.hi, tok_hi = t_hi >= hd.lo && t_hi < hd.hi;
+        float pr[NQT][4];
+        float al[NQT][2];
+        bool moved = false;
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int n = 0; n < NQT; ++n) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = 16 * tg + 8 * n + 2 * tig + (e & 1);
-            const bool row_ok = (e < 2) ? (gid < hd.gq) : (kTwoRows && gid + 8 < hd.gq);
-            const bool live = row_ok && t >= hd.lo && t < hd.hi;
-            sv[n][e] = live ? (sacc[n][0][e] + sacc[n][1][e]) * a.scale_log2 : kNegInf;
-            if (e < 2) mx0 = fmaxf(mx0, sv[n][e]); else mx1 = fmaxf(mx1, sv[n][e]);
+          for (int jq = 0; jq < 2; ++jq) {
+            const int q = 8 * n + 2 * tig + jq;
+            const bool qok = q < hd.gq;
+            const float s_lo = (qok && tok_lo) ? (sacc[n][0][jq] + sacc[n][1][jq]) * a.scale_log2 : kNegInf;
+            const float s_hi = (qok && tok_hi) ? (sacc[n][0][jq + 2] + sacc[n][1][jq + 2]) * a.scale_log2 : kNegInf;
+            float mx = fmaxf(s_lo, s_hi);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(mq[n][jq], mx);
+            const float mu = (mn == kNegInf) ? 0.f : mn;
+            al[n][jq] = exp2f(mq[n][jq] - mu);
+            moved |= al[n][jq] != 1.f;
+            pr[n][jq] = exp2f(s_lo - mu);
+            pr[n][jq + 2] = exp2f(s_hi - mu);
+            lq[n][jq] = lq[n][jq] * al[n][jq] + pr[n][jq] + pr[n][jq + 2];
+            mq[n][jq] = mn;
           }
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-        if constexpr (kTwoRows) {
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
         }
-        const float mn0 = fmaxf(m_run, mx0), mn1 = fmaxf(m_run2, mx1);
-        const float mu0 = (mn0 == kNegInf) ? 0.f : mn0, mu1 = (mn1 == kNegInf) ? 0.f : mn1;
-        const float al0 = exp2f(m_run - mu0), al1 = kTwoRows ? exp2f(m_run2 - mu1) : 1.f;
-        float pr[2][4];
-        float ps0 = 0.f, ps1 = 0.f;
+        if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+          for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (e < 2) {
-              pr[n][e] = exp2f(sv[n][e] - mu0);
-              ps0 += pr[n][e];
-            } else if (kTwoRows) {
-              pr[n][e] = exp2f(sv[n][e] - mu1);
-              ps1 += pr[n][e];
-            } else {
-              pr[n][e] = 0.f;
+            for (int n = 0; n < NQT; ++n) {
+              oacc[mt][n][0] *= al[n][0];
+              oacc[mt][n][1] *= al[n][1];
+              oacc[mt][n][2] *= al[n][0];
+              oacc[mt][n][3] *= al[n][1];
             }
-          }
-        l_run = l_run * al0 + ps0;
-        l_run2 = l_run2 * al1 + ps1;
-        m_run = mn0;
-        m_run2 = mn1;
-        if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-          for (int nt = 0; nt < kONt; ++nt) {
-            oacc[nt][0] *= al0;
-            oacc[nt][1] *= al0;
-            oacc[nt][2] *= al1;
-            oacc[nt][3] *= al1;
-          }
         }
-        // P as the A operand (rows = queries, k = the 16 tokens), split into
-        // bf16 hi + lo so that hi + lo carries ~16 significant bits of p.
-        // A-fragment order: (row g, k 0-7), (row g+8, k 0-7), (row g, k 8-15),
-        // (row g+8, k 8-15), i.e. n-tile 0 rows g / g+8, then n-tile 1.
-        uint32_t pa_hi[4], pa_lo[4];
+        // P^T as the B operand (k = token, n = query): the S^T accumulator
+        // layout transposed per 8x8 block with movmatrix, split bf16 hi + lo so
+        // hi + lo carries ~16 significant bits of p.
+        uint32_t pbh[NQT][2], pbl[NQT][2];
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-          const uint32_t h01 = pack_bf16(pr[n][0], pr[n][1]);
-          const uint32_t h23 = pack_bf16(pr[n][2], pr[n][3]);
-          pa_hi[2 * n] = h01;
-          pa_hi[2 * n + 1] = h23;
-          pa_lo[2 * n] = pack_bf16(pr[n][0] - bf16_lo_f(h01), pr[n][1] - bf16_hi_f(h01));
-          pa_lo[2 * n + 1] = pack_bf16(pr[n][2] - bf16_lo_f(h23), pr[n][3] - bf16_hi_f(h23));
+        for (int n = 0; n < NQT; ++n) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {  // tokens 0-7 then 8-15 of the warp
+            const float p0 = pr[n][2 * hh], p1 = pr[n][2 * hh + 1];
+            const uint32_t h = pack_bf16(p0, p1);
+            const uint32_t l = pack_bf16(p0 - bf16_lo_f(h), p1 - bf16_hi_f(h));
+            pbh[n][hh] = movmatrix_trans(h);
+            pbl[n][hh] = movmatrix_trans(l);
+          }
         }
         // V rows of masked tokens may hold anything (NaN in unused slots) and
-        // 0 * NaN is NaN inside the MMA: clear those tokens in the V fragments.
-        // This lane's fragments carry tokens 16tg + 2tig (+1) and (+8, +9).
+        // 0 * NaN is NaN inside the MMA: clear those tokens in the V^T
+        // fragments.  This lane's fragments carry tokens 16tg + 2tig (+1) and
+        // (+8, +9).
         const int tl = 16 * tg + 2 * tig;
         const uint32_t mlo = ((tl >= hd.lo && tl < hd.hi) ? 0x0000ffffu : 0u) |
                              ((tl + 1 >= hd.lo && tl + 1 < hd.hi) ? 0xffff0000u : 0u);
         const uint32_t mhi = ((tl + 8 >= hd.lo && tl + 8 < hd.hi) ? 0x0000ffffu : 0u) |
                              ((tl + 9 >= hd.lo && tl + 9 < hd.hi) ? 0xffff0000u : 0u);
-        // S6: O[:, this warp's head_dim part] += P V over the 16 tokens.
+        // S6: O^T[this warp's rows] += V^T P^T over the 16 tokens.
         {
           const int mi = lane >> 3, r = lane & 7;
-          const int t = 16 * tg + ((mi & 1) << 3) + r;
+          const int t = 16 * tg + ((mi >> 1) << 3) + r;
 #pragma unroll
-          for (int np2 = 0; np2 < kONt / 2; ++np2) {
-            const int d = dp * kDPart + np2 * 16 + ((mi >> 1) << 3);
+          for (int mt = 0; mt < kMt; ++mt) {
+            const int d = dp * kDPart + mt * 16 + ((mi & 1) << 3);
             const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
-            const uint32_t addr = vbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4);
-            uint32_t bv[4];
-            ldmatrix_x4_trans(addr, bv);
-            bv[0] &= mlo;
-            bv[1] &= mhi;
-            bv[2] &= mlo;
-            bv[3] &= mhi;
-            mma_bf16(oacc[2 * np2], pa_hi, bv[0], bv[1]);
-            mma_bf16(oacc[2 * np2 + 1], pa_hi, bv[2], bv[3]);
-            mma_bf16(oacc[2 * np2], pa_lo, bv[0], bv[1]);
-            mma_bf16(oacc[2 * np2 + 1], pa_lo, bv[2], bv[3]);
+            uint32_t av[4];
+            ldmatrix_x4_trans(vbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), av);
+            av[0] &= mlo;
+            av[1] &= mlo;
+            av[2] &= mhi;
+            av[3] &= mhi;
+#pragma unroll
+            for (int n = 0; n < NQT; ++n) {
+              mma_bf16(oacc[mt][n], av, pbh[n][0], pbh[n][1]);
+              mma_bf16(oacc[mt][n], av, pbl[n][0], pbl[n][1]);
+            }
           }
         }
       }
@@ -1006,79 +1015,103 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       }
     }
   } else {
-    // ---- token-half 1 hands its fragments to token-half 0 ----
-    float lf0 = l_run, lf1 = l_run2;  // each lane holds a quarter of its rows' columns
-    lf0 += __shfl_xor_sync(0xffffffffu, lf0, 1);
-    lf0 += __shfl_xor_sync(0xffffffffu, lf0, 2);
-    if constexpr (kTwoRows) {
-      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 1);
-      lf1 += __shfl_xor_sync(0xffffffffu, lf1, 2);
-    }
-    if (dp == 0 && tig == 0) {
-      if (gid < G) {
-        rm[tg][gid] = m_run;
-        rl[tg][gid] = poison ? kNaN : lf0;
+    // ---- token-half 1 hands its O^T fragments to token-half 0 ----
+    // l: each lane summed its two tokens; the column sums run over the 8
+    // lanes that share tig.
+    float lfull[NQT][2];
+#pragma unroll
+    for (int n = 0; n < NQT; ++n)
+#pragma unroll
+      for (int jq = 0; jq < 2; ++jq) {
+        float l = lq[n][jq];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        lfull[n][jq] = l;
       }
-      if (kTwoRows && gid + 8 < G) {
-        rm[tg][gid + 8] = m_run2;
-        rl[tg][gid + 8] = poison ? kNaN : lf1;
-      }
+    if (dp == 0 && gid == 0) {
+#pragma unroll
+      for (int n = 0; n < NQT; ++n)
+#pragma unroll
+        for (int jq = 0; jq < 2; ++jq) {
+          const int q = 8 * n + 2 * tig + jq;
+          if (q < G) {
+            rm[tg][q] = mq[n][jq];
+            rl[tg][q] = poison ? kNaN : lfull[n][jq];
+          }
+        }
     }
+    float* xb = &s.xbuf[xp][dp][0][0][0];  // this dp's slice: kMt * 32 * XV floats
     if (tg == 1) {
 #pragma unroll
-      for (int nt = 0; nt < kONt; ++nt) {
-        if constexpr (S::XV == 4) {
-          *reinterpret_cast<float4*>(&s.xbuf[xp][dp][nt][lane][0]) =
-              make_float4(oacc[nt][0], oacc[nt][1], oacc[nt][2], oacc[nt][3]);
-        } else {
-          *reinterpret_cast<float2*>(&s.xbuf[xp][dp][nt][lane][0]) = make_float2(oacc[nt][0], oacc[nt][1]);
-        }
-      }
+      for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+        for (int n = 0; n < NQT; ++n)
+          *reinterpret_cast<float4*>(xb + (mt * 32 + lane) * S::XV + 4 * n) =
+              make_float4(oacc[mt][n][0], oacc[mt][n][1], oacc[mt][n][2], oacc[mt][n][3]);
     }
     if (!cons_sync()) break;
     if (tg == 0) {
-      // merge the two token halves: rows gid (and gid + 8), this warp's columns
-      float f0[2], f1[2], inv[2], Ms[2];
+      // merge the two token halves for this warp's queries and O^T rows
+      float f0[NQT][2], f1[NQT][2], inv[NQT][2];
 #pragma unroll
-      for (int rr = 0; rr < (kTwoRows ? 2 : 1); ++rr) {
-        const int row = gid + 8 * rr;
-        const float m0 = rm[0][row], m1 = rm[1][row];
-        const float Mx = fmaxf(m0, m1);
-        Ms[rr] = (Mx == kNegInf) ? 0.f : Mx;
-        f0[rr] = exp2f(m0 - Ms[rr]);
-        f1[rr] = exp2f(m1 - Ms[rr]);
-        const float L = rl[0][row] * f0[rr] + rl[1][row] * f1[rr];
-        inv[rr] = 1.f / L;
-        if (split && dp == 0 && tig == 0 && row < hd.gq)
-          *reinterpret_cast<float4*>(a.part_ml + (static_cast<size_t>(hd.slot) * G + row) * 4) =
-              make_float4(Ms[rr], L, 0.f, 0.f);
-      }
+      for (int n = 0; n < NQT; ++n)
 #pragma unroll
-      for (int nt = 0; nt < kONt; ++nt) {
-        const int d = dp * kDPart + nt * 8 + 2 * tig;
-        float o[4];
-        if constexpr (S::XV == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(&s.xbuf[xp][dp][nt][lane][0]);
-          o[0] = (oacc[nt][0] * f0[0] + x.x * f1[0]) * inv[0];
-          o[1] = (oacc[nt][1] * f0[0] + x.y * f1[0]) * inv[0];
-          o[2] = (oacc[nt][2] * f0[1] + x.z * f1[1]) * inv[1];
-          o[3] = (oacc[nt][3] * f0[1] + x.w * f1[1]) * inv[1];
-        } else {
-          const float2 x = *reinterpret_cast<const float2*>(&s.xbuf[xp][dp][nt][lane][0]);
-          o[0] = (oacc[nt][0] * f0[0] + x.x * f1[0]) * inv[0];
-          o[1] = (oacc[nt][1] * f0[0] + x.y * f1[0]) * inv[0];
-          o[2] = o[3] = 0.f;
+        for (int jq = 0; jq < 2; ++jq) {
+          const int q = 8 * n + 2 * tig + jq;
+          f0[n][jq] = f1[n][jq] = inv[n][jq] = 0.f;
+          if (q < hd.gq) {
+            const float m0 = rm[0][q], m1 = rm[1][q];
+            const float Mx = fmaxf(m0, m1);
+            const float Ms = (Mx == kNegInf) ? 0.f : Mx;
+            f0[n][jq] = exp2f(m0 - Ms);
+            f1[n][jq] = exp2f(m1 - Ms);
+            const float L = rl[0][q] * f0[n][jq] + rl[1][q] * f1[n][jq];
+            inv[n][jq] = 1.f / L;
+            if (split && dp == 0 && gid == 0)
+              *reinterpret_cast<float4*>(a.part_ml + (static_cast<size_t>(hd.slot) * G + q) * 4) =
+                  make_float4(Ms, L, 0.f, 0.f);
+          }
         }
+      float o[kMt][NQT][4];
 #pragma unroll
-        for (int rr = 0; rr < (kTwoRows ? 2 : 1); ++rr) {
-          const int row = gid + 8 * rr;
-          if (row >= hd.gq) continue;
-          if (!split) {
-            T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + row) * D + d;
-            *reinterpret_cast<uint32_t*>(dst) = pack_bf16(o[2 * rr], o[2 * rr + 1]);
-          } else {
-            *reinterpret_cast<float2*>(a.part_o + (static_cast<size_t>(hd.slot) * G + row) * D + d) =
-                make_float2(o[2 * rr], o[2 * rr + 1]);
+      for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+        for (int n = 0; n < NQT; ++n) {
+          const float4 x = *reinterpret_cast<const float4*>(xb + (mt * 32 + lane) * S::XV + 4 * n);
+          o[mt][n][0] = (oacc[mt][n][0] * f0[n][0] + x.x * f1[n][0]) * inv[n][0];
+          o[mt][n][1] = (oacc[mt][n][1] * f0[n][1] + x.y * f1[n][1]) * inv[n][1];
+          o[mt][n][2] = (oacc[mt][n][2] * f0[n][0] + x.z * f1[n][0]) * inv[n][0];
+          o[mt][n][3] = (oacc[mt][n][3] * f0[n][1] + x.w * f1[n][1]) * inv[n][1];
+        }
+      // Stage the rows [query][this warp's head_dim columns] in the slice the
+      // partner warp just handed over, then store them 16 bytes per lane.
+      __syncwarp();
+#pragma unroll
+      for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+        for (int n = 0; n < NQT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = 8 * n + 2 * tig + (e & 1);
+            const int dl = mt * 16 + gid + ((e >> 1) << 3);
+            xb[q * kDPart + dl] = o[mt][n][e];
+          }
+      __syncwarp();
+      constexpr int kChunk = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte store
+      for (int idx = lane; idx < hd.gq * (kDPart / 4); idx += 32) {
+        const int q = idx / (kDPart / 4), c4 = idx - q * (kDPart / 4);
+        const float4 v4 = *reinterpret_cast<const float4*>(xb + q * kDPart + 4 * c4);
+        const int d = dp * kDPart + 4 * c4;
+        if (split) {
+          *reinterpret_cast<float4*>(a.part_o + (static_cast<size_t>(hd.slot) * G + q) * D + d) = v4;
+        } else if constexpr (kChunk == 8) {
+          // bf16: two neighbouring float4 chunks make one 16-byte store
+          if ((c4 & 1) == 0) {
+            const float4 w4 = *reinterpret_cast<const float4*>(xb + q * kDPart + 4 * c4 + 4);
+            T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + q) * D + d;
+            *reinterpret_cast<uint4*>(row) = make_uint4(pack_bf16(v4.x, v4.y), pack_bf16(v4.z, v4.w),
+                                                        pack_bf16(w4.x, w4.y), pack_bf16(w4.z, w4.w));
           }
         }
       }
