@@ -165,7 +165,8 @@ VT_API vt_status vt_paged_attn_set_override(int grid_ctas, int min_units_per_cta
 /*
  * Reads and clears the device status word that kernels set when a bounded
  * wait gives up (bit 0: page tile never arrived, bit 1: stage never released,
- * bit 2: consumer-warp rendezvous, bit 3: drain of copies in flight) or a
+ * bit 2: consumer-warp rendezvous, bit 3: drain of copies in flight, bit 5:
+ * partials staged for a split-KV combine) or a
  * self-check fails (bit 4: a CTA's tile walk did not match its share).
  * Synchronises `stream` first.  *status is 0 when all is well; the call
  * returns VT_ERR_DEVICE_TIMEOUT if it was not.  Clearing also resets the

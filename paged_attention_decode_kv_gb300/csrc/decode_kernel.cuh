@@ -59,7 +59,14 @@ constexpr long long kDrainLimitCycles = 1ll << 28;
 enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8 };
 
 // Status bits (global status word).
-enum : unsigned { kStatusFull = 1u, kStatusEmpty = 2u, kStatusSync = 4u, kStatusDrain = 8u, kStatusWalk = 16u };
+enum : unsigned {
+  kStatusFull = 1u,
+  kStatusEmpty = 2u,
+  kStatusSync = 4u,
+  kStatusDrain = 8u,
+  kStatusWalk = 16u,
+  kStatusCombine = 32u
+};
 
 struct DecodeArgs {
   void* out;
@@ -77,8 +84,10 @@ struct DecodeArgs {
   float scale_log2; // scale * log2(e)
   int min_units;    // lower bound on tiles per CTA
   int* counters;    // [num_seqs * num_kv_heads * subgroups] arrival counters, zero between calls
-  float* part_ml;   // [2 * grid][G][4]  (m, l, 0, 0) of each partial, log2 domain
-  float* part_o;    // [2 * grid][G][D]  normalised partial rows
+  // Split partials, one record per slot ([2 * grid] slots of G * (4 + D)
+  // floats): (m, l, 0, 0) per row in the log2 domain, then the G normalised
+  // rows, so one bulk copy fetches a record's used part.
+  float* part;
   unsigned* status; // status words
 };
 
@@ -139,6 +148,7 @@ struct Smem {
   alignas(8) unsigned long long full[NSTAGE];
   unsigned long long empty[NSTAGE];
   unsigned long long csync;
+  unsigned long long comb;  // partials staged for a combine
   long long scan[16];
   int b_start_s;
   long long cum_start_s;
@@ -209,13 +219,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 16-byte global -> shared copy through L2 only (the source may have been
-// written by another SM in this kernel), completion via cp.async groups.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy (bulk copy) accesses: partials are written with plain stores
+// and read back by bulk copies of another CTA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Arrival counter increment with acquire-release semantics at GPU scope: the
@@ -373,8 +381,6 @@ struct Partition {
   __device__ __forceinline__ int owner(long long x) const {
     return static_cast<int>(((x + 1) * static_cast<long long>(C) - 1) / U);
   }
-  // partial slot that CTA c uses for the item starting at tile item_u
-  __device__ __forceinline__ int slot(int c, long long item_u) const { return 2 * c + (start(c) < item_u ? 1 : 0); }
 };
 
 struct SeqSpan {
@@ -438,6 +444,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int NT = (NCW + 1) * 32;
   constexpr int NC = NCW * 32;  // consumer threads
   constexpr uint32_t kTileBytes = kPageTokens * D * sizeof(T);
+  constexpr int kPartRec = G * (4 + D);  // floats of a partial record
   constexpr bool kMma = MATH == Math::kMma;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
                 "mma consumer shape");
@@ -459,6 +466,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       mbar_init(&s.empty[st], NCW);
     }
     mbar_init(&s.csync, NCW);  // one arrival per consumer warp
+    mbar_init(&s.comb, NCW);  // one arrival per consumer warp
     s.abort_flag = 0;
     s.b_start_s = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -556,7 +564,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         const int pb = static_cast<int>(seg_end < sp.np ? seg_end : sp.np);
         const long long item_u = cum + static_cast<long long>(vh) * sp.np;
         const int nsplit = part.owner(item_u + sp.np - 1) - part.owner(item_u) + 1;
-        const int slot = part.slot(blockIdx.x, item_u);  // 64-bit divisions: once per segment
+        const int slot = 2 * static_cast<int>(blockIdx.x) + (u0 < item_u ? 1 : 0);  // item starts inside our slice
         const int h = vh / a.subgroups, sub = vh - h * a.subgroups;
         const int q_row0 = h * a.group + sub * G;
         const int gq = min(G, a.group - sub * G);
@@ -1006,11 +1014,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D;
         LaneMap<T, D>::store(row, d0, val);
       } else {
-        float* po = a.part_o + (static_cast<size_t>(hd.slot) * G + i) * D + d0;
+        float* po = a.part + static_cast<size_t>(hd.slot) * kPartRec + G * 4 + i * D + d0;
         *reinterpret_cast<float4*>(po) = make_float4(val[0], val[1], val[2], val[3]);
         *reinterpret_cast<float4*>(po + 4) = make_float4(val[4], val[5], val[6], val[7]);
         if (d0 == 0)
-          *reinterpret_cast<float4*>(a.part_ml + (static_cast<size_t>(hd.slot) * G + i) * 4) =
+          *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * kPartRec + i * 4) =
               make_float4(s.fin_m[i], L, 0.f, 0.f);
       }
     }
@@ -1069,7 +1077,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const float L = rl[0][q] * f0[n][jq] + rl[1][q] * f1[n][jq];
             inv[n][jq] = 1.f / L;
             if (split && dp == 0 && gid == 0)
-              *reinterpret_cast<float4*>(a.part_ml + (static_cast<size_t>(hd.slot) * G + q) * 4) =
+              *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * kPartRec + q * 4) =
                   make_float4(Ms, L, 0.f, 0.f);
           }
         }
@@ -1104,7 +1112,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         const float4 v4 = *reinterpret_cast<const float4*>(xb + q * kDPart + 4 * c4);
         const int d = dp * kDPart + 4 * c4;
         if (split) {
-          *reinterpret_cast<float4*>(a.part_o + (static_cast<size_t>(hd.slot) * G + q) * D + d) = v4;
+          *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * kPartRec + G * 4 + q * D + d) = v4;
         } else if constexpr (kChunk == 8) {
           // bf16: two neighbouring float4 chunks make one 16-byte store
           if ((c4 & 1) == 0) {
@@ -1122,7 +1130,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   // ---- S8 bookkeeping: the last CTA to finish this item owes its combine --
   // The rendezvous orders every consumer's partial stores before thread 0's
   // release-acquire increment (one GPU-scope round trip instead of a fence
-  // in every thread plus an atomic plus another fence).
+  // in every thread plus an atomic plus another fence).  The proxy fence
+  // lets the combining CTA's bulk copies observe those stores.
+  fence_proxy_async_global();
   if (!cons_sync()) break;
   if (ct == 0) {
     const int item = hd.b * nvh + hd.vh;
@@ -1136,15 +1146,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   }  // segment loop
 
   // ===================== S8: deferred LSE combines ============================
-  // Run after this CTA consumed all its tiles, so the stage ring is free to
-  // stage every partial of an item with cp.async (all loads in flight at
-  // once) before merging them from shared memory.
+  // Run after this CTA consumed all its tiles, so the stage ring is free.  One
+  // bulk copy per partial record, spread over the lanes of all consumer
+  // warps and all in flight at once, stages a round of an item's partials.
+  // Each thread then merges its 4-column chunks: the round's largest m first,
+  // then every partial weighted by l * 2^(m - M).
   if (!alive) return;
-  if (!cons_sync()) return;
+  if (!cons_sync()) return;  // pend_n was written by thread 0
   const int n_pend = s.pend_n;
-  unsigned char* ring = reinterpret_cast<unsigned char*>(&s.k[0][0]);
+  float* const ring = reinterpret_cast<float*>(&s.k[0][0]);
   constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(T);
-  constexpr int kChunksPerRow = D / 4;  // 16-byte chunks of an fp32 row
+  constexpr int kRowChunks = D / 4;  // float4 chunks of a row
+  constexpr int kOwn = (G * kRowChunks + NC - 1) / NC;
+  uint32_t comb_phase = 0;
   for (int pi = 0; pi < n_pend; ++pi) {
     const PendingCombine pc = s.pend[pi];
     const int h = pc.vh / a.subgroups, sub = pc.vh - h * a.subgroups;
@@ -1154,70 +1168,97 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     const int first_bit = part.start(c_first) < pc.item_u ? 1 : 0;
     // partial slot of the k-th CTA sharing the item (later CTAs start inside it)
     auto slot_of = [&](int k) { return 2 * (c_first + k) + (k == 0 ? first_bit : 0); };
-    const int rec = gq * (D * 4 + 16);
-    const int per_round = static_cast<int>(kRingBytes / rec);
-    float* so = reinterpret_cast<float*>(ring);
-    // online merge state for this thread's output chunks (row i, 4 columns)
-    constexpr int kMaxOwn = (G * kChunksPerRow + NC - 1) / NC;
-    float Mr[kMaxOwn], Lr[kMaxOwn], acc4[kMaxOwn][4];
+    const int rec = G * 4 + gq * D;  // floats of a record's used part
+    const uint32_t rec_bytes = static_cast<uint32_t>(rec) * 4;
+    const int per_round = static_cast<int>(kRingBytes / rec_bytes);
+    float Mrun[kOwn], Lrun[kOwn], acc[kOwn][4];
 #pragma unroll
-    for (int q = 0; q < kMaxOwn; ++q) {
-      Mr[q] = kNegInf;
-      Lr[q] = 0.f;
-      acc4[q][0] = acc4[q][1] = acc4[q][2] = acc4[q][3] = 0.f;
+    for (int q = 0; q < kOwn; ++q) {
+      Mrun[q] = kNegInf;
+      Lrun[q] = 0.f;
+      acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
     }
     for (int k0 = 0; k0 < pc.nsplit; k0 += per_round) {
       const int nk = min(per_round, pc.nsplit - k0);
-      if (!cons_sync()) return;  // everyone is done reading the previous round
-      float* sml = so + static_cast<size_t>(nk) * gq * D;
-      const int n_o = nk * gq * kChunksPerRow;
-      for (int qc = ct; qc < n_o + nk * gq; qc += NC) {
-        if (qc < n_o) {
-          const int k = qc / (gq * kChunksPerRow), rem = qc - k * (gq * kChunksPerRow);
-          const int i = rem / kChunksPerRow, cc = rem - i * kChunksPerRow;
-          cp_async_16(smem_addr(so + (static_cast<size_t>(k) * gq + i) * D + 4 * cc),
-                      a.part_o + (static_cast<size_t>(slot_of(k0 + k)) * G + i) * D + 4 * cc);
-        } else {
-          const int q2 = qc - n_o, k = q2 / gq, i = q2 - k * gq;
-          cp_async_16(smem_addr(sml + (static_cast<size_t>(k) * gq + i) * 4),
-                      a.part_ml + (static_cast<size_t>(slot_of(k0 + k)) * G + i) * 4);
-        }
+      if (k0 > 0 || pi > 0) {
+        if (!cons_sync()) return;  // everyone is done reading the ring
       }
-      cp_async_wait_all();
-      if (!cons_sync()) return;
+      {
+        // warp w copies records w, w + NCW, ...; its arrival announces its bytes first
+        const int n_mine = warp < nk ? (nk - warp + NCW - 1) / NCW : 0;
+        if (lane == 0) mbar_arrive_expect_tx(&s.comb, static_cast<uint32_t>(n_mine) * rec_bytes);
+        __syncwarp();
+        if (n_mine > 0) fence_proxy_async_global();
+        for (int k = warp + NCW * lane; k < nk; k += 32 * NCW)
+          bulk_load(ring + static_cast<size_t>(k) * rec,
+                    a.part + static_cast<size_t>(slot_of(k0 + k)) * kPartRec, rec_bytes, &s.comb);
+      }
+      bool ok = wait_phase(&s.comb, comb_phase, &s.abort_flag, a.status, kStatusCombine);
+      comb_phase ^= 1u;
+      if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll
-      for (int q = 0; q < kMaxOwn; ++q) {
+      for (int q = 0; q < kOwn; ++q) {
         const int oc = ct + q * NC;
-        if (oc >= gq * kChunksPerRow) continue;
-        const int i = oc / kChunksPerRow, cc = oc - i * kChunksPerRow;
-        for (int k = 0; k < nk; ++k) {
-          const float4 ml = *reinterpret_cast<const float4*>(sml + (static_cast<size_t>(k) * gq + i) * 4);
-          const float4 ov = *reinterpret_cast<const float4*>(so + (static_cast<size_t>(k) * gq + i) * D + 4 * cc);
-          const float Mn = fmaxf(Mr[q], ml.x);
-          const float sc_old = exp2f(Mr[q] - Mn);  // -inf the first time -> 0
-          const float w = ml.y * exp2f(ml.x - Mn);
-          Lr[q] = Lr[q] * sc_old + w;
-          acc4[q][0] = acc4[q][0] * sc_old + w * ov.x;
-          acc4[q][1] = acc4[q][1] * sc_old + w * ov.y;
-          acc4[q][2] = acc4[q][2] * sc_old + w * ov.z;
-          acc4[q][3] = acc4[q][3] * sc_old + w * ov.w;
-          Mr[q] = Mn;
+        const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
+        if (i >= gq) continue;
+        const float* mlp = ring + i * 4;                  // (m, l) of row i, record stride rec
+        const float* src = ring + G * 4 + i * D + 4 * cc;  // this thread's chunk, record stride rec
+        float mx = kNegInf;
+        for (int k = 0; k < nk; ++k) mx = fmaxf(mx, mlp[static_cast<size_t>(k) * rec]);
+        const float Mn = fmaxf(Mrun[q], mx);
+        const float sc = exp2f(Mrun[q] - Mn);  // 0 on the first round
+        Mrun[q] = Mn;
+        float l = Lrun[q] * sc, a0 = acc[q][0] * sc, a1 = acc[q][1] * sc, a2 = acc[q][2] * sc,
+              a3 = acc[q][3] * sc;
+        int k = 0;
+        for (; k + 4 <= nk; k += 4) {
+          float4 ov[4];
+          float2 ml[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            ml[u] = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k + u) * rec);
+            ov[u] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k + u) * rec);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float w = ml[u].y * exp2f(ml[u].x - Mn);
+            l += w;
+            a0 = fmaf(w, ov[u].x, a0);
+            a1 = fmaf(w, ov[u].y, a1);
+            a2 = fmaf(w, ov[u].z, a2);
+            a3 = fmaf(w, ov[u].w, a3);
+          }
         }
+        for (; k < nk; ++k) {
+          const float2 ml = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k) * rec);
+          const float4 ov = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k) * rec);
+          const float w = ml.y * exp2f(ml.x - Mn);
+          l += w;
+          a0 = fmaf(w, ov.x, a0);
+          a1 = fmaf(w, ov.y, a1);
+          a2 = fmaf(w, ov.z, a2);
+          a3 = fmaf(w, ov.w, a3);
+        }
+        Lrun[q] = l;
+        acc[q][0] = a0;
+        acc[q][1] = a1;
+        acc[q][2] = a2;
+        acc[q][3] = a3;
       }
     }
 #pragma unroll
-    for (int q = 0; q < kMaxOwn; ++q) {
+    for (int q = 0; q < kOwn; ++q) {
       const int oc = ct + q * NC;
-      if (oc >= gq * kChunksPerRow) continue;
-      const int i = oc / kChunksPerRow, cc = oc - i * kChunksPerRow;
-      const float inv = 1.f / Lr[q];
+      const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
+      if (i >= gq) continue;
+      const float inv = 1.f / Lrun[q];
       T* row = static_cast<T*>(a.out) + (static_cast<size_t>(pc.b) * a.num_q_heads + q_row0 + i) * D + 4 * cc;
       if constexpr (sizeof(T) == 2) {
-        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(acc4[q][0] * inv, acc4[q][1] * inv),
-                                                    pack_bf16(acc4[q][2] * inv, acc4[q][3] * inv));
+        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(acc[q][0] * inv, acc[q][1] * inv),
+                                                    pack_bf16(acc[q][2] * inv, acc[q][3] * inv));
       } else {
         *reinterpret_cast<float4*>(row) =
-            make_float4(acc4[q][0] * inv, acc4[q][1] * inv, acc4[q][2] * inv, acc4[q][3] * inv);
+            make_float4(acc[q][0] * inv, acc[q][1] * inv, acc[q][2] * inv, acc[q][3] * inv);
       }
     }
   }

@@ -69,20 +69,18 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // arrival counters, which every kernel leaves at zero; partials start after it.
 struct WsNeed {
   size_t counters_bytes;  // counters this call uses
-  size_t ml_bytes;        // partial (m, l) pairs
-  size_t o_bytes;         // partial rows
+  size_t part_bytes;      // partial records: per row (m, l, 0, 0), then the rows
 };
 
 WsNeed ws_need(int num_seqs, int nvh, int grid, int group_tile, int head_dim) {
   WsNeed n;
   n.counters_bytes = static_cast<size_t>(num_seqs) * nvh * sizeof(int);
   const size_t slots = 2 * static_cast<size_t>(grid);
-  n.ml_bytes = align_up(slots * group_tile * 4 * sizeof(float), 256);
-  n.o_bytes = slots * group_tile * head_dim * sizeof(float);
+  n.part_bytes = slots * group_tile * (4 + head_dim) * sizeof(float);
   return n;
 }
 
-size_t ws_total(const WsNeed& n) { return 256 + align_up(n.counters_bytes, 256) + n.ml_bytes + n.o_bytes; }
+size_t ws_total(const WsNeed& n) { return 256 + align_up(n.counters_bytes, 256) + n.part_bytes; }
 
 // ---------------------------------------------------------------------------
 // Per-device state
@@ -139,10 +137,10 @@ vt_status prepare_variant(DeviceState& ds, const VariantInfo& v, int* ctas_per_s
 // Grows (never shrinks) the device's workspace.  A new buffer is zeroed on
 // `stream` before any kernel that uses it, so all counters start at 0.
 vt_status ensure_workspace(DeviceState& ds, const WsNeed& n, cudaStream_t stream) {
-  if (ds.ws && ds.counters_cap >= n.counters_bytes && ds.partial_cap >= n.ml_bytes + n.o_bytes) return VT_OK;
+  if (ds.ws && ds.counters_cap >= n.counters_bytes && ds.partial_cap >= n.part_bytes) return VT_OK;
   size_t counters = ds.counters_cap > n.counters_bytes ? ds.counters_cap : n.counters_bytes;
   counters = align_up(counters + counters / 4 + 1024, 256);
-  size_t partial = ds.partial_cap > n.ml_bytes + n.o_bytes ? ds.partial_cap : n.ml_bytes + n.o_bytes;
+  size_t partial = ds.partial_cap > n.part_bytes ? ds.partial_cap : n.part_bytes;
   partial = align_up(partial + partial / 4, 1 << 16);
   const size_t bytes = 256 + counters + partial;
   if (ds.ws) {
@@ -353,8 +351,7 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
     char* base = static_cast<char*>(ds.ws);
     args.status = reinterpret_cast<unsigned*>(base);
     args.counters = reinterpret_cast<int*>(base + 256);
-    args.part_ml = reinterpret_cast<float*>(base + 256 + ds.counters_cap);
-    args.part_o = reinterpret_cast<float*>(base + 256 + ds.counters_cap + need.ml_bytes);
+    args.part = reinterpret_cast<float*>(base + 256 + ds.counters_cap);
     g_last_plan.num_sms = ds.num_sms;
   }
 
@@ -476,10 +473,10 @@ vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_c
     min_units = g_override_min_units > 0 ? g_override_min_units : kDefaultMinUnits;
     num_sms = ds.num_sms;
   }
-  // Layout inside the fixed array: [status 256 B | counters | partial (m, l) | partial rows].
+  // Layout inside the fixed array: [status 256 B | counters | partial records].
   const WsNeed need = ws_need(num_seqs, static_cast<int>(nvh), grid, gt, head_dim);
   const size_t counters_region = align_up(need.counters_bytes, 256);
-  const size_t total = 256 + counters_region + need.ml_bytes + need.o_bytes;
+  const size_t total = 256 + counters_region + need.part_bytes;
   if (total > kNoAllocScratchBytes) {
     g_last_cuda_error = "vt_paged_attn_decode_noalloc: this call needs " + std::to_string(total) +
                         " bytes of scratch; the static buffer holds " + std::to_string(kNoAllocScratchBytes);
@@ -503,8 +500,7 @@ vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_c
   DecodeArgs args{};
   args.status = reinterpret_cast<unsigned*>(base);
   args.counters = reinterpret_cast<int*>(base + 256);
-  args.part_ml = reinterpret_cast<float*>(base + 256 + counters_region);
-  args.part_o = reinterpret_cast<float*>(base + 256 + counters_region + need.ml_bytes);
+  args.part = reinterpret_cast<float*>(base + 256 + counters_region);
   args.out = out;
   args.q = q;
   args.block_tables = block_tables;
