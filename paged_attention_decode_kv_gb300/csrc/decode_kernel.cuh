@@ -205,6 +205,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // Plain bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           unsigned long long* bar) {
@@ -598,16 +607,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               mbar_arrive_expect_tx(&s.full[stage], bytes);
             }
             __syncwarp();
-            // Each copy is issued by its own lane: a TMA instruction occupies its
-            // issuing thread for tens of cycles, so one lane issuing them all
-            // would serialise the page gather.
-            constexpr int kBoxes = kMma ? D / kSwizzleCols : 1;  // boxes per K (or V) tile
-            if (!bad && lane < 2 * kBoxes) {
-              const int sb = lane >> 1;
-              const bool is_v = (lane & 1) != 0;
-              T* dst = (is_v ? s.v[stage] : s.k[stage]) + (kMma ? sb * kPageTokens * kSwizzleCols : 0);
-              tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, kMma ? sb * kSwizzleCols : 0, h, pid * kPageTokens,
-                          &s.full[stage]);
+            // One tensor copy per K (or V) tile, each issued by its own lane: a
+            // TMA instruction occupies its issuing thread for a hundred cycles
+            // or more, so the fewer and larger the boxes the faster the gather.
+            // bf16 boxes cover (64 columns, 32 tokens, D/64 column blocks) of one
+            // head, landing as D/64 swizzled [token][64] sub-tiles.
+            if (!bad && lane < 2) {
+              const bool is_v = lane == 1;
+              T* dst = is_v ? s.v[stage] : s.k[stage];
+              if constexpr (kMma)
+                tma_load_4d(dst, is_v ? &tmap_v : &tmap_k, 0, pid * kPageTokens, 0, h, &s.full[stage]);
+              else
+                tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, 0, h, pid * kPageTokens, &s.full[stage]);
             }
             if (p == pa && lane == 31) {
               const T* qsrc = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.num_q_heads + q_row0) * D;

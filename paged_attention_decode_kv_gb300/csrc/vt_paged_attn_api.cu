@@ -169,7 +169,7 @@ vt_status ensure_workspace(DeviceState& ds, const WsNeed& n, cudaStream_t stream
 }
 
 // ---------------------------------------------------------------------------
-// TMA descriptors: 3-D view (head_dim, kv head, token row) of a page pool.
+// TMA descriptors: tiled views of a page pool (4-D for bf16, 3-D for fp32).
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -214,22 +214,36 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
     return VT_ERR_CUDA;
   }
   const size_t es = k.dtype == VT_BF16 ? 2 : 4;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k.head_dim), static_cast<cuuint64_t>(k.num_kv_heads),
-                              static_cast<cuuint64_t>(k.num_blocks) * vt::kPageTokens};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k.head_dim) * es,
-                                 static_cast<cuuint64_t>(k.head_dim) * k.num_kv_heads * es};
-  // bf16 (tensor-core consumer): boxes of 64 columns (128 bytes) x 32 tokens
-  // with the 128-byte swizzle, so ldmatrix reads are bank-conflict free.
-  // fp32 (CUDA-core consumer): one unswizzled box of head_dim x 32 tokens.
-  const bool swz = k.dtype == VT_BF16;
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(swz ? vt::kSwizzleCols : k.head_dim), 1u,
-                             static_cast<cuuint32_t>(vt::kPageTokens)};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const cuuint64_t tokens = static_cast<cuuint64_t>(k.num_blocks) * vt::kPageTokens;
+  const cuuint64_t row = static_cast<cuuint64_t>(k.head_dim) * k.num_kv_heads * es;  // bytes per token
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUtensorMap m;
-  CUresult r = fn(&m, swz ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-                  const_cast<void*>(k.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (k.dtype == VT_BF16) {
+    // Tensor-core consumer: a 4-D view (64 columns, token, column block, kv
+    // head) so one box brings a whole [32 tokens][head_dim] tile of one head,
+    // stored as head_dim/64 sub-tiles of [token][64 columns] with the 128-byte
+    // swizzle (bank-conflict-free ldmatrix reads).
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(vt::kSwizzleCols), tokens,
+                                static_cast<cuuint64_t>(k.head_dim / vt::kSwizzleCols),
+                                static_cast<cuuint64_t>(k.num_kv_heads)};
+    const cuuint64_t strides[3] = {row, static_cast<cuuint64_t>(vt::kSwizzleCols) * es,
+                                   static_cast<cuuint64_t>(k.head_dim) * es};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(vt::kSwizzleCols), static_cast<cuuint32_t>(vt::kPageTokens),
+                               static_cast<cuuint32_t>(k.head_dim / vt::kSwizzleCols), 1u};
+    r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k.ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // CUDA-core consumer: a 3-D view (column, kv head, token) and one
+    // unswizzled box of head_dim x 32 tokens.
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(k.head_dim), static_cast<cuuint64_t>(k.num_kv_heads), tokens};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k.head_dim) * es, row};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(k.head_dim), 1u, static_cast<cuuint32_t>(vt::kPageTokens)};
+    r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(k.ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) {
     g_last_cuda_error = "cuTensorMapEncodeTiled failed (code " + std::to_string(static_cast<int>(r)) + ")";
     return VT_ERR_CUDA;
