@@ -150,6 +150,7 @@ typedef struct {
   int dtype;              /* vt_dtype */
   size_t smem_bytes;      /* dynamic shared memory per CTA */
   size_t workspace_bytes; /* split-KV workspace used (partials + arrival counters) */
+  int launch_overlap;     /* 1: launched as a programmatic dependent (vt_paged_attn_set_overlap) */
 } vt_plan;
 
 VT_API vt_status vt_paged_attn_last_plan(vt_plan* plan);
@@ -161,6 +162,28 @@ VT_API vt_status vt_paged_attn_last_plan(vt_plan* plan);
  * the default lower bound on work per CTA.  0 restores the automatic choice.
  */
 VT_API vt_status vt_paged_attn_set_override(int grid_ctas, int min_units_per_cta);
+
+/*
+ * Launch overlap for this host thread, read on every call (default 0).  Not
+ * an operation of the pages: a launch choice of this library.
+ *
+ * enabled = 1 launches each decode as a programmatic dependent of the kernel
+ * before it on the same stream (CUDA programmatic dependent launch; it also
+ * applies inside stream capture).  The decode's CTAs may then start while
+ * that kernel finishes: they read context_lens and block_tables and plan the
+ * split at once, and wait for it to complete before they read q, k_cache or
+ * v_cache, or touch out and the workspace.  The decode itself lets the next
+ * kernel start the same way.  Back-to-back decode steps (CUDA graphs of
+ * layers or steps) overlap one call's start-up with the previous call's
+ * tail.
+ *
+ * Contract: with enabled = 1, the kernel launched immediately before the
+ * decode on its stream must not write context_lens or block_tables (step
+ * metadata usually comes from host copies, which do not overlap).  Results
+ * are identical either way.  Returns VT_ERR_INVALID_ARG unless enabled is 0
+ * or 1.
+ */
+VT_API vt_status vt_paged_attn_set_overlap(int enabled);
 
 /*
  * Reads and clears the device status word that kernels set when a bounded

@@ -224,6 +224,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream (if it was launched as a programmatic dependent) start its CTAs
+// once every CTA of this grid has issued it; wait blocks until the grids this
+// one depends on have completed and their memory is visible.  Both are no-ops
+// for an ordinary launch.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -468,6 +476,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nvh = a.num_kv_heads * a.subgroups;
+  // The next decode on the stream may start its CTAs as SMs free up; it reads
+  // nothing this grid writes before its own grid_dependency_wait.
+  grid_launch_dependents();
+  // Sequences without tiles (empty context: zero rows; invalid length: NaN
+  // rows) are filled by CTA b mod grid, after the dependency wait: the
+  // previous kernel on the stream may still read or write `out`.
+  auto fill_empty_rows = [&](int nthreads, int t) {
+    for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
+      const SeqSpan sp = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks);
+      if (sp.np != 0) continue;
+      const float fill = sp.bad ? __int_as_float(0x7fc00000) : 0.f;
+      float vals[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vals[e] = fill;
+      T* row0 = static_cast<T*>(a.out) + static_cast<size_t>(b) * a.num_q_heads * D;
+      for (int e = t * 8; e < a.num_q_heads * D; e += nthreads * 8) LaneMap<T, D>::store(row0, e, vals);
+    }
+  };
 
   if (tid == 0) {
     for (int st = 0; st < NSTAGE; ++st) {
@@ -492,15 +518,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     if (b < a.num_seqs) {
       const SeqSpan sp = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks);
       units = static_cast<long long>(sp.np) * nvh;
-      if (sp.np == 0 && (b % gridDim.x) == blockIdx.x) {
-        // empty context -> zero rows; invalid context -> NaN rows
-        const float fill = sp.bad ? __int_as_float(0x7fc00000) : 0.f;
-        float vals[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) vals[e] = fill;
-        T* row0 = static_cast<T*>(a.out) + static_cast<size_t>(b) * a.num_q_heads * D;
-        for (int e = 0; e < a.num_q_heads * D; e += 8) LaneMap<T, D>::store(row0, e, vals);
-      }
     }
     long long tot;
     const long long excl = block_exclusive_scan<NT>(units, s.scan, tot);
@@ -508,10 +525,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     my_units = units;
     U += tot;
   }
-  if (U == 0) return;
+  if (U == 0) {
+    grid_dependency_wait();
+    fill_empty_rows(NT, tid);
+    return;
+  }
   const long long cap = (U + a.min_units - 1) / a.min_units;
   const int C = static_cast<int>(cap < gridDim.x ? cap : gridDim.x);
-  if (static_cast<int>(blockIdx.x) >= C) return;
+  if (static_cast<int>(blockIdx.x) >= C) {
+    grid_dependency_wait();
+    fill_empty_rows(NT, tid);
+    return;
+  }
   const Partition part{U, C};
   const long long u0 = part.start(blockIdx.x), u1 = part.start(blockIdx.x + 1);
 
@@ -581,6 +606,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         for (int p0 = pa; ok && p0 < pb; p0 += 32) {
           const int my_p = p0 + lane;
           const int my_id = (my_p < pb) ? __ldg(bt_row + my_p) : 0;
+          // q, K and V may be written by the previous kernel on the stream;
+          // the first copies wait for it (context lengths and block tables
+          // were read before: the caller keeps them unchanged across it).
+          if (issued == 0) grid_dependency_wait();
           const int n = min(32, pb - p0);
           for (int jj = 0; jj < n; ++jj) {
             const int pid = __shfl_sync(0xffffffffu, my_id, jj);
@@ -678,6 +707,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     return r;
   };
   if (ct == 0) s.pend_n = 0;  // only thread 0 touches it until the final rendezvous
+  // Global memory this grid shares with the previous kernel on the stream
+  // (out, the workspace) is touched only after this point.
+  grid_dependency_wait();
+  fill_empty_rows(NC, ct);
 
   // ---- per-consumer constants ----------------------------------------------
   // CUDA-core consumer (fp32): row group j (GS lanes), lane c owns 8 columns.

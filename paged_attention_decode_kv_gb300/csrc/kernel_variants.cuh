@@ -17,7 +17,7 @@ struct VariantInfo {
   size_t smem_bytes;   // dynamic shared memory (includes 1 KB alignment slack)
   const void* func;
   cudaError_t (*launch)(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& args, int grid,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool overlap);
 };
 
 // Shared memory an SM offers (228 KB) less the 1 KB the hardware reserves per CTA.
@@ -43,10 +43,22 @@ struct Variant {
   using S = Smem<D, T, G, NCW, NSTAGE, M>;
   static constexpr size_t smem = sizeof(S) + 1024;
 
+  // overlap: launch as a programmatic dependent of the previous kernel on the
+  // stream, so this grid's CTAs may start (and read context lengths and block
+  // tables) while that kernel finishes.
   static cudaError_t launch(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& args, int grid,
-                            cudaStream_t stream) {
-    paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M><<<grid, (NCW + 1) * 32, smem, stream>>>(tk, tv, args);
-    return cudaGetLastError();
+                            cudaStream_t stream, bool overlap) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((NCW + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M>, tk, tv, args);
   }
 
   static VariantInfo info() {

@@ -26,6 +26,7 @@ constexpr int kMaxGroupTile = 8;
 constexpr int kDefaultMinUnits = 2;
 
 thread_local int g_override_grid = 0;
+thread_local bool g_overlap = false;
 thread_local int g_override_min_units = 0;
 thread_local vt_plan g_last_plan{};
 thread_local bool g_have_plan = false;
@@ -287,6 +288,12 @@ vt_status vt_paged_attn_set_override(int grid_ctas, int min_units_per_cta) {
   return VT_OK;
 }
 
+vt_status vt_paged_attn_set_overlap(int enabled) {
+  if (enabled != 0 && enabled != 1) return VT_ERR_INVALID_ARG;
+  g_overlap = enabled != 0;
+  return VT_OK;
+}
+
 vt_status vt_paged_attn_last_plan(vt_plan* plan) {
   if (!plan) return VT_ERR_INVALID_ARG;
   if (!g_have_plan) return VT_ERR_INVALID_ARG;
@@ -390,8 +397,9 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   args.scale_log2 = scale * 1.4426950408889634f;
   args.min_units = min_units;
 
-  e = v->launch(tk, tv, args, grid, stream);
+  e = v->launch(tk, tv, args, grid, stream, g_overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  g_last_plan.launch_overlap = g_overlap ? 1 : 0;
 
   g_last_plan.grid_ctas = grid;
   g_last_plan.ctas_per_sm = per_sm;
@@ -530,8 +538,9 @@ vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_c
   args.scale_log2 = scale * 1.4426950408889634f;
   args.min_units = min_units;
 
-  e = v->launch(tk, tv, args, grid, stream);
+  e = v->launch(tk, tv, args, grid, stream, g_overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  g_last_plan.launch_overlap = g_overlap ? 1 : 0;
 
   g_last_plan.num_sms = num_sms;
   g_last_plan.grid_ctas = grid;
