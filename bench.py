@@ -227,41 +227,67 @@ def time_graph(vt, case, t, steps, warmup):
 
 
 def time_e2e(vt, case, t, steps, warmup):
-    """Through the C-ABI with host buffers: pinned H2D of the step's inputs
-    (q, block table, context lengths), the decode, D2H of the output.  The KV
-    pool is resident state (rotated across copies as in time_calls)."""
+    """Through the C-ABI with host buffers, every step: one pinned host->device
+    copy of the step's inputs (q, block table and context lengths packed in
+    one buffer), the decode, and a device->host copy of the output.  The KV
+    pool is resident state (rotated across copies as in time_graph).  Steps
+    are launched from CUDA graphs like the device-only timing; one event pair
+    brackets all of them.  Returns (mean seconds per step, h2d bytes, d2h bytes)."""
     import torch
     w = case.workload
-    hq = case.q.pin_memory()
-    hbt = case.block_tables.pin_memory()
-    hcl = case.context_lens.pin_memory()
+
+    def align(x):
+        return (x + 255) // 256 * 256
+
+    parts = [case.q.contiguous(), case.block_tables.contiguous(), case.context_lens.contiguous()]
+    sizes = [p.numel() * p.element_size() for p in parts]
+    offs = [0, align(sizes[0]), align(sizes[0]) + align(sizes[1])]
+    total = offs[2] + sizes[2]
+    hbuf = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for p, o, n in zip(parts, offs, sizes):
+        hbuf[o:o + n].copy_(p.view(-1).view(torch.uint8))
+    dbuf = torch.empty(total, dtype=torch.uint8, device=t["q"].device)
+    dq, dbt, dcl = (dbuf[o:o + n].view(p.dtype).view(p.shape) for p, o, n in zip(parts, offs, sizes))
     hout = torch.empty_like(case.q).pin_memory()
-    dq, dbt, dcl = torch.empty_like(t["q"]), torch.empty_like(t["bt"]), torch.empty_like(t["cl"])
     out = torch.empty_like(t["q"])
-    stream = torch.cuda.current_stream()
     pools = t["pools"]
+    n = len(pools)
+    chunk = n * -(-16 // n)
 
-    def step(i):
-        k, v = pools[i % len(pools)]
-        dq.copy_(hq, non_blocking=True)
-        dbt.copy_(hbt, non_blocking=True)
-        dcl.copy_(hcl, non_blocking=True)
-        vt.decode(dq, k, v, dbt, dcl, w.scale, w.window, out=out)
-        hout.copy_(out, non_blocking=True)
+    def steps_of(count):
+        for i in range(count):
+            k, v = pools[i % n]
+            dbuf.copy_(hbuf, non_blocking=True)
+            vt.decode(dq, k, v, dbt, dcl, w.scale, w.window, out=out)
+            hout.copy_(out, non_blocking=True)
 
-    for i in range(warmup):
-        step(i)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        steps_of(max(warmup, 3))
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for s in range(steps):
-        starts[s].record(stream)
-        step(warmup + s)
-        ends[s].record(stream)
+    full, rem = divmod(steps, chunk)
+    g_full, g_rem = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full):
+        steps_of(chunk)
+    if rem:
+        with torch.cuda.graph(g_rem):
+            steps_of(rem)
+    g_full.replay()
     torch.cuda.synchronize()
-    h2d = hq.numel() * hq.element_size() + hbt.numel() * 4 + hcl.numel() * 4
-    d2h = hout.numel() * hout.element_size()
-    return [a.elapsed_time(b) * 1e-3 for a, b in zip(starts, ends)], h2d, d2h
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(full):
+        g_full.replay()
+    if rem:
+        g_rem.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if not torch.equal(hout, out.cpu()):
+        raise RuntimeError("end-to-end output differs from the device output")
+    return a.elapsed_time(b) * 1e-3 / steps, sum(sizes), hout.numel() * hout.element_size()
 
 
 def oracle_baseline(case, budget_s: float):
@@ -396,8 +422,8 @@ def run_ours(args, rank, world, dist):
     mean_s = max_over_ranks(graph_s, dist, dev)
     # the same calls launched one by one from Python (per-call event pairs)
     times = time_calls(vt, case, t, max(200, args.steps // 10), args.warmup)
-    e2e_times, h2d, d2h = time_e2e(vt, case, t, max(50, args.steps // 10), args.warmup)
-    e2e_s = max_over_ranks(statistics.mean(e2e_times), dist, dev)
+    e2e_step_s, h2d, d2h = time_e2e(vt, case, t, max(200, args.steps // 5), args.warmup)
+    e2e_s = max_over_ranks(e2e_step_s, dist, dev)
 
     host_case = case
     n_pool_copies = len(t["pools"])
