@@ -84,9 +84,12 @@ struct DecodeArgs {
   float scale_log2; // scale * log2(e)
   int min_units;    // lower bound on tiles per CTA
   int* counters;    // [num_seqs * num_kv_heads * subgroups] arrival counters, zero between calls
-  // Split partials, one record per slot ([2 * grid] slots of G * (4 + D)
-  // floats): (m, l, 0, 0) per row in the log2 domain, then the G normalised
-  // rows, so one bulk copy fetches a record's used part.
+  // Split partials: one record per slot, G * 4 + min(G, group) * D floats,
+  // holding (m, l, 0, 0) per row in the log2 domain, then the normalised
+  // rows.  Slots [0, grid) hold each CTA's first segment (an item that
+  // started before its slice), slots [grid, 2 grid) its last (an item that
+  // starts inside its slice): the partials of one item then sit in one run
+  // of consecutive records, plus at most one record of the second half.
   float* part;
   unsigned* status; // status words
 };
@@ -99,6 +102,7 @@ struct StageHeader {
   int gq;       // live query rows of this virtual head (<= G)
   int nsplit;   // CTAs sharing this (sequence, virtual head)
   int slot;     // this CTA's partial slot for it
+  int c_first;  // first CTA sharing it
   long long item_u;  // first tile index of the (sequence, virtual head)
 };
 
@@ -107,7 +111,7 @@ enum class Math { kSimt, kMma };
 
 // A combine the CTA owes: it was the last to finish a split item.
 struct PendingCombine {
-  int b, vh, nsplit, gq;
+  int b, vh, nsplit, gq, c_first;
   long long item_u;
 };
 
@@ -461,7 +465,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int NT = (NCW + 1) * 32;
   constexpr int NC = NCW * 32;  // consumer threads
   constexpr uint32_t kTileBytes = kPageTokens * D * sizeof(T);
-  constexpr int kPartRec = G * (4 + D);  // floats of a partial record
+  const int prec = G * 4 + min(G, a.group) * D;  // floats of a partial record
   constexpr bool kMma = MATH == Math::kMma;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
                 "mma consumer shape");
@@ -501,7 +505,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       mbar_init(&s.empty[st], NCW);
     }
     mbar_init(&s.csync, NCW);  // one arrival per consumer warp
-    mbar_init(&s.comb, NCW);  // one arrival per consumer warp
+    mbar_init(&s.comb, 1);
     s.abort_flag = 0;
     s.b_start_s = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -597,8 +601,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         const long long seg_end = off_end - static_cast<long long>(vh) * sp.np;
         const int pb = static_cast<int>(seg_end < sp.np ? seg_end : sp.np);
         const long long item_u = cum + static_cast<long long>(vh) * sp.np;
-        const int nsplit = part.owner(item_u + sp.np - 1) - part.owner(item_u) + 1;
-        const int slot = 2 * static_cast<int>(blockIdx.x) + (u0 < item_u ? 1 : 0);  // item starts inside our slice
+        const int c_first = part.owner(item_u);
+        const int nsplit = part.owner(item_u + sp.np - 1) - c_first + 1;
+        // first-segment slots, then last-segment slots (the item starts inside our slice)
+        const int slot = static_cast<int>(blockIdx.x) + (u0 < item_u ? static_cast<int>(gridDim.x) : 0);
         const int h = vh / a.subgroups, sub = vh - h * a.subgroups;
         const int q_row0 = h * a.group + sub * G;
         const int gq = min(G, a.group - sub * G);
@@ -630,6 +636,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               hd.gq = gq;
               hd.nsplit = nsplit;
               hd.slot = slot;
+              hd.c_first = c_first;
               hd.item_u = item_u;
               uint32_t bytes = bad ? 0u : 2u * kTileBytes;
               if (p == pa) bytes += static_cast<uint32_t>(gq) * D * sizeof(T);
@@ -1058,11 +1065,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D;
         LaneMap<T, D>::store(row, d0, val);
       } else {
-        float* po = a.part + static_cast<size_t>(hd.slot) * kPartRec + G * 4 + i * D + d0;
+        float* po = a.part + static_cast<size_t>(hd.slot) * prec + G * 4 + i * D + d0;
         *reinterpret_cast<float4*>(po) = make_float4(val[0], val[1], val[2], val[3]);
         *reinterpret_cast<float4*>(po + 4) = make_float4(val[4], val[5], val[6], val[7]);
         if (d0 == 0)
-          *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * kPartRec + i * 4) =
+          *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * prec + i * 4) =
               make_float4(s.fin_m[i], L, 0.f, 0.f);
       }
     }
@@ -1121,7 +1128,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const float L = rl[0][q] * f0[n][jq] + rl[1][q] * f1[n][jq];
             inv[n][jq] = 1.f / L;
             if (split && dp == 0 && gid == 0)
-              *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * kPartRec + q * 4) =
+              *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * prec + q * 4) =
                   make_float4(Ms, L, 0.f, 0.f);
           }
         }
@@ -1156,7 +1163,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         const float4 v4 = *reinterpret_cast<const float4*>(xb + q * kDPart + 4 * c4);
         const int d = dp * kDPart + 4 * c4;
         if (split) {
-          *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * kPartRec + G * 4 + q * D + d) = v4;
+          *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * prec + G * 4 + q * D + d) = v4;
         } else if constexpr (kChunk == 8) {
           // bf16: two neighbouring float4 chunks make one 16-byte store
           if ((c4 & 1) == 0) {
@@ -1184,7 +1191,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     if (prev == hd.nsplit - 1) {
       st_relaxed_gpu(a.counters + item, 0);  // every other CTA has arrived: reset for the next call
       // Only a CTA's first and last segments can be split, so at most two.
-      if (s.pend_n < 2) s.pend[s.pend_n++] = PendingCombine{hd.b, hd.vh, hd.nsplit, hd.gq, hd.item_u};
+      if (s.pend_n < 2) s.pend[s.pend_n++] = PendingCombine{hd.b, hd.vh, hd.nsplit, hd.gq, hd.c_first, hd.item_u};
     }
   }
   }  // segment loop
@@ -1208,11 +1215,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     const int h = pc.vh / a.subgroups, sub = pc.vh - h * a.subgroups;
     const int q_row0 = h * a.group + sub * G;
     const int gq = pc.gq;
-    const int c_first = part.owner(pc.item_u);
-    const int first_bit = part.start(c_first) < pc.item_u ? 1 : 0;
-    // partial slot of the k-th CTA sharing the item (later CTAs start inside it)
-    auto slot_of = [&](int k) { return 2 * (c_first + k) + (k == 0 ? first_bit : 0); };
-    const int rec = G * 4 + gq * D;  // floats of a record's used part
+    const int c_first = pc.c_first;
+    // The k-th CTA sharing the item left its partial in first-segment slot
+    // c_first + k, except the first CTA when the item starts inside its slice
+    // (last-segment slot grid + c_first).
+    const bool first_last = part.start(c_first) < pc.item_u;
+    const int rec = prec;
     const uint32_t rec_bytes = static_cast<uint32_t>(rec) * 4;
     const int per_round = static_cast<int>(kRingBytes / rec_bytes);
     float Mrun[kOwn], Lrun[kOwn], acc[kOwn][4];
@@ -1227,15 +1235,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       if (k0 > 0 || pi > 0) {
         if (!cons_sync()) return;  // everyone is done reading the ring
       }
-      {
-        // warp w copies records w, w + NCW, ...; its arrival announces its bytes first
-        const int n_mine = warp < nk ? (nk - warp + NCW - 1) / NCW : 0;
-        if (lane == 0) mbar_arrive_expect_tx(&s.comb, static_cast<uint32_t>(n_mine) * rec_bytes);
+      if (warp == 0) {
+        // records k0 .. k0 + nk - 1 are one run of first-segment slots, but
+        // for record 0 when it sits in the last-segment half: two copies at most
+        const bool split0 = k0 == 0 && first_last;
+        if (lane == 0) mbar_arrive_expect_tx(&s.comb, static_cast<uint32_t>(nk) * rec_bytes);
         __syncwarp();
-        if (n_mine > 0) fence_proxy_async_global();
-        for (int k = warp + NCW * lane; k < nk; k += 32 * NCW)
-          bulk_load(ring + static_cast<size_t>(k) * rec,
-                    a.part + static_cast<size_t>(slot_of(k0 + k)) * kPartRec, rec_bytes, &s.comb);
+        if (lane < 2) {
+          fence_proxy_async_global();
+          const size_t g = gridDim.x;
+          if (lane == 0 && split0)
+            bulk_load(ring, a.part + (g + c_first) * rec, rec_bytes, &s.comb);
+          const int k_run = split0 ? 1 : 0;  // first record of the run in this round
+          if (lane == (split0 ? 1 : 0) && nk > k_run)
+            bulk_load(ring + static_cast<size_t>(k_run) * rec,
+                      a.part + static_cast<size_t>(c_first + k0 + k_run) * rec,
+                      static_cast<uint32_t>(nk - k_run) * rec_bytes, &s.comb);
+        }
       }
       bool ok = wait_phase(&s.comb, comb_phase, &s.abort_flag, a.status, kStatusCombine);
       comb_phase ^= 1u;
