@@ -1263,25 +1263,36 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         if (i >= gq) continue;
         const float* mlp = ring + i * 4;                  // (m, l) of row i, record stride rec
         const float* src = ring + G * 4 + i * D + 4 * cc;  // this thread's chunk, record stride rec
-        float mx = kNegInf;
-        for (int k = 0; k < nk; ++k) mx = fmaxf(mx, mlp[static_cast<size_t>(k) * rec]);
-        const float Mn = fmaxf(Mrun[q], mx);
-        const float sc = exp2f(Mrun[q] - Mn);  // 0 on the first round
-        Mrun[q] = Mn;
-        float l = Lrun[q] * sc, a0 = acc[q][0] * sc, a1 = acc[q][1] * sc, a2 = acc[q][2] * sc,
-              a3 = acc[q][3] * sc;
-        int k = 0;
-        for (; k + 4 <= nk; k += 4) {
-          float4 ov[4];
-          float2 ml[4];
+        // One pass in batches of kB partials, all loads of a batch in flight:
+        // the batch's largest m rescales what is accumulated so far.
+        constexpr int kB = 8;
+        float M = Mrun[q], l = Lrun[q], a0 = acc[q][0], a1 = acc[q][1], a2 = acc[q][2], a3 = acc[q][3];
+        for (int k = 0; k < nk; k += kB) {
+          float2 ml[kB];
+          float4 ov[kB];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            ml[u] = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k + u) * rec);
-            ov[u] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k + u) * rec);
+          for (int u = 0; u < kB; ++u) {
+            if (k + u < nk) {
+              ml[u] = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k + u) * rec);
+              ov[u] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k + u) * rec);
+            } else {
+              ml[u] = make_float2(kNegInf, 0.f);
+              ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
           }
+          float Mb = M;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float w = ml[u].y * exp2f(ml[u].x - Mn);
+          for (int u = 0; u < kB; ++u) Mb = fmaxf(Mb, ml[u].x);
+          const float sc = exp2f(M - Mb);  // 0 before the first partial (M = -inf)
+          M = Mb;
+          l *= sc;
+          a0 *= sc;
+          a1 *= sc;
+          a2 *= sc;
+          a3 *= sc;
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            const float w = ml[u].y * exp2f(ml[u].x - Mb);  // 0 for the padding entries
             l += w;
             a0 = fmaf(w, ov[u].x, a0);
             a1 = fmaf(w, ov[u].y, a1);
@@ -1289,16 +1300,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             a3 = fmaf(w, ov[u].w, a3);
           }
         }
-        for (; k < nk; ++k) {
-          const float2 ml = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k) * rec);
-          const float4 ov = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k) * rec);
-          const float w = ml.y * exp2f(ml.x - Mn);
-          l += w;
-          a0 = fmaf(w, ov.x, a0);
-          a1 = fmaf(w, ov.y, a1);
-          a2 = fmaf(w, ov.z, a2);
-          a3 = fmaf(w, ov.w, a3);
-        }
+        Mrun[q] = M;
         Lrun[q] = l;
         acc[q][0] = a0;
         acc[q][1] = a1;
