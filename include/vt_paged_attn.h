@@ -151,6 +151,7 @@ typedef struct {
   size_t smem_bytes;      /* dynamic shared memory per CTA */
   size_t workspace_bytes; /* split-KV workspace used (partials + arrival counters) */
   int launch_overlap;     /* 1: launched as a programmatic dependent (vt_paged_attn_set_overlap) */
+  int segment_cost;       /* partition weight of a segment boundary, in tiles (vt_paged_attn_set_segment_cost) */
 } vt_plan;
 
 VT_API vt_status vt_paged_attn_last_plan(vt_plan* plan);
@@ -184,6 +185,23 @@ VT_API vt_status vt_paged_attn_set_override(int grid_ctas, int min_units_per_cta
  * or 1.
  */
 VT_API vt_status vt_paged_attn_set_overlap(int enabled);
+
+/*
+ * Partition weight of a segment boundary for this host thread, read on every
+ * call.  Not an operation of the pages: a scheduling choice of this library.
+ *
+ * The kernel splits the (sequence, kv head, page) tiles evenly over its CTAs.
+ * Every (sequence, kv head) a CTA starts costs it time beyond its pages (an
+ * epilogue, a new query tile, a block-table row), so each one also weighs
+ * `tiles` tiles in the split: CTAs whose share crosses many short sequences
+ * get fewer pages.  The weight applies when the batch gives every CTA at
+ * least 4 pages (below that the split is latency-bound and weights only add
+ * partial results).  tiles < 0 restores the default (2); 0 balances pages
+ * alone.  Results are the same within rounding (split points move, and with
+ * them the order of the log-sum-exp merge).  Returns VT_ERR_INVALID_ARG for
+ * tiles > 64.
+ */
+VT_API vt_status vt_paged_attn_set_segment_cost(int tiles);
 
 /*
  * Reads and clears the device status word that kernels set when a bounded

@@ -21,7 +21,7 @@ VT_BF16, VT_F32 = 0, 1
 BLOCK_SIZE = 32
 
 EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_last_plan", "vt_paged_attn_set_override",
-            "vt_paged_attn_set_overlap",
+            "vt_paged_attn_set_overlap", "vt_paged_attn_set_segment_cost",
             "vt_paged_attn_device_status", "vt_paged_attn_device_status_detail", "vt_paged_attn_workspace_bytes", "vt_paged_attn_release",
             "vt_status_string", "vt_last_cuda_error", "vt_paged_attn_version")
 
@@ -40,7 +40,8 @@ class vt_plan(ctypes.Structure):
                 ("consumer_warps", ctypes.c_int), ("tensor_cores", ctypes.c_int), ("stages", ctypes.c_int), ("group_tile", ctypes.c_int),
                 ("subgroups", ctypes.c_int), ("min_units_per_cta", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
-                ("workspace_bytes", ctypes.c_size_t), ("launch_overlap", ctypes.c_int)]
+                ("workspace_bytes", ctypes.c_size_t), ("launch_overlap", ctypes.c_int),
+                ("segment_cost", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -74,6 +75,8 @@ def library() -> ctypes.CDLL:
             lib.vt_paged_attn_set_override.restype = c_int
             lib.vt_paged_attn_set_overlap.argtypes = [c_int]
             lib.vt_paged_attn_set_overlap.restype = c_int
+            lib.vt_paged_attn_set_segment_cost.argtypes = [c_int]
+            lib.vt_paged_attn_set_segment_cost.restype = c_int
             lib.vt_paged_attn_device_status.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint)]
             lib.vt_paged_attn_device_status.restype = c_int
             lib.vt_paged_attn_device_status_detail.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint), c_int]
@@ -135,6 +138,10 @@ def vt_paged_attn_set_override(grid_ctas: int = 0, min_units_per_cta: int = 0) -
 
 def vt_paged_attn_set_overlap(enabled: bool) -> None:
     _check(library().vt_paged_attn_set_overlap(1 if enabled else 0), "vt_paged_attn_set_overlap")
+
+
+def vt_paged_attn_set_segment_cost(tiles: int = -1) -> None:
+    _check(library().vt_paged_attn_set_segment_cost(tiles), "vt_paged_attn_set_segment_cost")
 
 
 def vt_paged_attn_device_status(stream=None) -> int:

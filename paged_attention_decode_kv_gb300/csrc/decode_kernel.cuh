@@ -56,7 +56,7 @@ constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr long long kDrainLimitCycles = 1ll << 28;
 
 // Stage flags written by the producer.
-enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8 };
+enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8, kEnd = 16 };  // kEnd: no more tiles
 
 // Status bits (global status word).
 enum : unsigned {
@@ -83,6 +83,7 @@ struct DecodeArgs {
   int window;       // <= 0: none
   float scale_log2; // scale * log2(e)
   int min_units;    // lower bound on tiles per CTA
+  int seg_cost;     // tiles' worth of time a segment boundary costs (partition weight)
   int* counters;    // [num_seqs * num_kv_heads * subgroups] arrival counters, zero between calls
   // Split partials: one record per slot, G * 4 + min(G, group) * D floats,
   // holding (m, l, 0, 0) per row in the log2 domain, then the normalised
@@ -513,22 +514,35 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   for (int e = tid; e < G * D; e += NT) (&s.red_acc[0][0])[e] = 0.f;
 
   // ---- S1: request lookup and balanced partition ---------------------------
-  // Pass 1 sums the tiles; when the whole batch fits one pass of the block,
-  // the same scan also locates this CTA's first sequence (no second pass).
-  long long U = 0, my_excl = 0, my_units = 0;
+  // The split balances work units: every page of a (sequence, virtual head)
+  // item is one, and every item also weighs seg_cost units for the time a
+  // segment boundary costs -- when CTAs have pages enough for that to matter
+  // (at least kWeightMinTiles each).  One scan sums pages and items together
+  // (packed: pages << 24 | items); when the whole batch fits one pass of the
+  // block, it also locates this CTA's first sequence.
+  constexpr int kItemBits = 24;
+  constexpr long long kItemMask = (1ll << kItemBits) - 1;
+  constexpr int kWeightMinTiles = 4;
+  const bool weighable = static_cast<long long>(a.num_seqs) * nvh <= kItemMask;
+  auto packed_units = [&](int b) -> long long {
+    const int np = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks).np;
+    if (np <= 0) return 0;
+    return (static_cast<long long>(np) * nvh << kItemBits) + (weighable ? nvh : 0);
+  };
+  long long P = 0, my_pexcl = 0, my_punits = 0;  // packed
   for (int base = 0; base < a.num_seqs; base += NT) {
     const int b = base + tid;
-    long long units = 0;
-    if (b < a.num_seqs) {
-      const SeqSpan sp = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks);
-      units = static_cast<long long>(sp.np) * nvh;
-    }
+    const long long pu = b < a.num_seqs ? packed_units(b) : 0;
     long long tot;
-    const long long excl = block_exclusive_scan<NT>(units, s.scan, tot);
-    my_excl = U + excl;
-    my_units = units;
-    U += tot;
+    const long long excl = block_exclusive_scan<NT>(pu, s.scan, tot);
+    my_pexcl = P + excl;
+    my_punits = pu;
+    P += tot;
   }
+  const long long U_pages = P >> kItemBits;
+  const int X = weighable && U_pages >= static_cast<long long>(kWeightMinTiles) * gridDim.x ? a.seg_cost : 0;
+  auto unpack = [&](long long v) { return (v >> kItemBits) + X * (v & kItemMask); };
+  const long long U = unpack(P), my_excl = unpack(my_pexcl), my_units = unpack(my_punits);
   if (U == 0) {
     grid_dependency_wait();
     fill_empty_rows(NT, tid);
@@ -553,9 +567,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     long long carry = 0;
     for (int base = 0; base < a.num_seqs; base += NT) {
       const int b = base + tid;
-      long long units = 0;
-      if (b < a.num_seqs)
-        units = static_cast<long long>(seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks).np) * nvh;
+      const long long units = b < a.num_seqs ? unpack(packed_units(b)) : 0;
       long long tot;
       const long long excl = carry + block_exclusive_scan<NT>(units, s.scan, tot);
       if (units > 0 && excl <= u0 && u0 < excl + units) {
@@ -590,17 +602,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       return __shfl_sync(0xffffffffu, win_len, bb - win_base);
     };
     bool ok = b >= 0;
+    long long covered = 0;  // units walked, for the self-check
     while (ok && u < u1) {
       const SeqSpan sp = seq_span(length_of(b), a.window, a.max_blocks);
-      const long long ub = static_cast<long long>(sp.np) * nvh;
+      const int w = sp.np + X;  // units of one (sequence, virtual head) item
+      const long long ub = static_cast<long long>(w) * nvh;
       long long off = u - cum;
       const long long off_end = (u1 - cum < ub) ? (u1 - cum) : ub;
-      while (ok && off < off_end) {
-        const int vh = static_cast<int>(off / sp.np);
-        const int pa = static_cast<int>(off - static_cast<long long>(vh) * sp.np);
-        const long long seg_end = off_end - static_cast<long long>(vh) * sp.np;
-        const int pb = static_cast<int>(seg_end < sp.np ? seg_end : sp.np);
-        const long long item_u = cum + static_cast<long long>(vh) * sp.np;
+      for (int vh = static_cast<int>(off / w); ok && off < off_end; ++vh) {
+        // An item's first seg_cost units stand for the time a segment boundary
+        // costs and hold no tile; its pages are the units after them.
+        const long long ibase = static_cast<long long>(vh) * w;
+        const int r0 = static_cast<int>(off - ibase);
+        const int r1 = static_cast<int>(off_end - ibase < w ? off_end - ibase : w);
+        covered += r1 - r0;
+        off = ibase + r1;
+        const int pa = max(r0 - X, 0), pb = r1 - X;
+        if (pb <= pa) continue;  // only the item's weight falls in this slice
+        const long long item_u = cum + ibase + X;  // the item's first page unit
         const int c_first = part.owner(item_u);
         const int nsplit = part.owner(item_u + sp.np - 1) - c_first + 1;
         // first-segment slots, then last-segment slots (the item starts inside our slice)
@@ -668,7 +687,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             }
           }
         }
-        off = static_cast<long long>(vh) * sp.np + pb;
       }
       u = cum + off_end;
       cum += ub;
@@ -678,14 +696,29 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       } while (ok && u < u1 && b < a.num_seqs && seq_span(length_of(b), a.window, a.max_blocks).np == 0);
       if (b >= a.num_seqs) break;
     }
-    // Self-check: the walk must have produced exactly this CTA's tiles.
-    if (issued != u1 - u0 && !s.abort_flag && lane == 0) {
+    // Self-check: the walk must have covered exactly this CTA's slice.
+    if (covered != u1 - u0 && !s.abort_flag && lane == 0) {
       atomicOr(a.status, kStatusWalk);
       s.abort_flag = 1;
     }
-    // Let every copy this warp issued land before the CTA can exit.
+    // The consumers learn that the work is over from one more stage that
+    // carries no tiles (how many pages the slice holds depends on the items
+    // it crosses).
+    bool end_sent = false;
+    if (ok && __all_sync(0xffffffffu, !s.abort_flag)) {
+      ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty);
+      end_sent = __all_sync(0xffffffffu, ok);
+      if (end_sent && lane == 0) {
+        s.hdr[stage].flags = kEnd;
+        mbar_arrive(&s.full[stage]);
+      }
+    }
+    // Let every copy this warp issued land before the CTA can exit.  Once the
+    // end stage went out, its own stage's last tile had been released, and
+    // its full barrier has moved on a phase: drain only the others.
     if (lane == 0) {
-      const long long n_drain = issued < NSTAGE ? issued : NSTAGE;
+      const long long cap = end_sent ? NSTAGE - 1 : NSTAGE;
+      const long long n_drain = issued < cap ? issued : cap;
       for (long long k = 1; k <= n_drain; ++k) {
         const long long idx = issued - k;  // stage index of the k-th most recent copy
         const int st = static_cast<int>(idx % NSTAGE);
@@ -743,12 +776,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   int stage = 0;
   uint32_t phase = 0;
   int par = 0, seg_par = 0;
-  const long long n_tiles = u1 - u0;
-  long long it = 0;
-  bool alive = true;
+  bool alive = true, more = true;
   // One iteration per (sequence, virtual head) segment: the query fragments
   // and accumulators are scoped to it, so they are dead in the epilogue.
-  while (alive && it < n_tiles) {
+  while (alive && more) {
   float qf[kMma ? 1 : G][8];
   float acc[kMma ? 1 : G][8];
   uint32_t qb[kMma ? kKSteps : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
@@ -765,6 +796,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       break;
     }
     hd = s.hdr[stage];
+    if (hd.flags & kEnd) {
+      more = false;
+      break;
+    }
 
     if constexpr (!kMma) {
       // ====================== CUDA-core consumer ==============================
@@ -1011,9 +1046,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       stage = 0;
       phase ^= 1u;
     }
-    ++it;
-  } while (!(hd.flags & kLast) && it < n_tiles);
-  if (!alive || !(hd.flags & kLast)) break;
+  } while (!(hd.flags & kLast));
+  if (!alive || !more) break;
 
   // ---- end of a (sequence, virtual head) segment ----------------------------
   const int h = hd.vh / a.subgroups, sub = hd.vh - h * a.subgroups;

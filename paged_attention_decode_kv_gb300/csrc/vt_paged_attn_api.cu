@@ -24,10 +24,12 @@ using vt::VariantInfo;
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr int kMaxGroupTile = 8;
 constexpr int kDefaultMinUnits = 2;
+constexpr int kDefaultSegCost = 2;  // a segment boundary weighs about two tiles of streaming
 
 thread_local int g_override_grid = 0;
 thread_local bool g_overlap = false;
 thread_local int g_override_min_units = 0;
+thread_local int g_seg_cost = -1;  // < 0: default
 thread_local vt_plan g_last_plan{};
 thread_local bool g_have_plan = false;
 thread_local std::string g_last_cuda_error;
@@ -294,6 +296,12 @@ vt_status vt_paged_attn_set_overlap(int enabled) {
   return VT_OK;
 }
 
+vt_status vt_paged_attn_set_segment_cost(int tiles) {
+  if (tiles > 64) return VT_ERR_INVALID_ARG;
+  g_seg_cost = tiles;
+  return VT_OK;
+}
+
 vt_status vt_paged_attn_last_plan(vt_plan* plan) {
   if (!plan) return VT_ERR_INVALID_ARG;
   if (!g_have_plan) return VT_ERR_INVALID_ARG;
@@ -396,10 +404,12 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   args.window = window > 0 ? window : 0;
   args.scale_log2 = scale * 1.4426950408889634f;
   args.min_units = min_units;
+  args.seg_cost = g_seg_cost < 0 ? kDefaultSegCost : g_seg_cost;
 
   e = v->launch(tk, tv, args, grid, stream, g_overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   g_last_plan.launch_overlap = g_overlap ? 1 : 0;
+  g_last_plan.segment_cost = args.seg_cost;
 
   g_last_plan.grid_ctas = grid;
   g_last_plan.ctas_per_sm = per_sm;
@@ -537,10 +547,12 @@ vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_c
   args.window = window > 0 ? window : 0;
   args.scale_log2 = scale * 1.4426950408889634f;
   args.min_units = min_units;
+  args.seg_cost = g_seg_cost < 0 ? kDefaultSegCost : g_seg_cost;
 
   e = v->launch(tk, tv, args, grid, stream, g_overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   g_last_plan.launch_overlap = g_overlap ? 1 : 0;
+  g_last_plan.segment_cost = args.seg_cost;
 
   g_last_plan.num_sms = num_sms;
   g_last_plan.grid_ctas = grid;

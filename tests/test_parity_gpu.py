@@ -40,6 +40,7 @@ def _reset_override():
     if vt._lib is not None:
         vt.vt_paged_attn_set_override(0, 0)
         vt.vt_paged_attn_set_overlap(False)
+        vt.vt_paged_attn_set_segment_cost(-1)
 
 
 def gpu_run(case, dev, grid=0, min_units=0, window=None, tables=None, lens=None, stream=None):
@@ -230,6 +231,36 @@ def test_scale_zero_gives_mean_of_values(dev):
     mean = vv.mean(0)
     for i in range(4):
         assert (out[0, i].double() - mean[i // 2]).abs().max() < 2e-2
+
+
+@pytest.mark.parametrize("cost", [0, 1, 5, 33])
+@pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_W1024, W.D256_GQA4_F32], ids=lambda w: w.name)
+def test_segment_cost(dev, w, cost):
+    """Segment boundaries weigh `cost` tiles in the split: slices then start
+    and end inside an item's weight as well as inside its pages, and CTAs
+    whose slice is only weight get no tile.  Any weight gives the oracle's
+    result, at several grids."""
+    vt.vt_paged_attn_set_segment_cost(cost)
+    case = W.make_case(w, 20)
+    for grid in (0, 7, 64, 700):
+        (_, _), plan = check_case(case, dev, grid=grid, min_units=1 if grid else 0)
+        assert plan["segment_cost"] == cost
+
+
+def test_segment_cost_ragged(dev):
+    """Empty, one-page and long sequences, a window, and query subgroups,
+    with a heavy segment weight and a grid that leaves CTAs without pages."""
+    vt.vt_paged_attn_set_segment_cost(9)
+    lens = [0, 1, 700, 31, 0, 33, 2000, 64, 5, 1000, 0, 257]
+    case = W.make_case(W.custom("segcost_ragged", lens, 64, 4, 128), 21)
+    for window in (0, 100):
+        for grid in (0, 5, 300):
+            out, _ = gpu_run(case, dev, grid=grid, min_units=1 if grid else 0, window=window)
+            rows = [(b, i) for b in range(len(lens)) if lens[b] > 0 for i in range(64)]
+            idx, ref = oracle_rows(case, rows, window=window)
+            compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16, f"w{window} g{grid}")
+            for b in (0, 4, 10):
+                assert torch.count_nonzero(out[b]) == 0
 
 
 def _overlap_cases():
