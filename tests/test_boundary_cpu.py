@@ -81,6 +81,25 @@ def test_override_validation(lib):
     assert lib.vt_paged_attn_set_override(0, 0) == vt.VT_OK
 
 
+def test_overlap_and_segment_cost_validation(lib):
+    assert lib.vt_paged_attn_set_overlap(2) == vt.VT_ERR_INVALID_ARG
+    assert lib.vt_paged_attn_set_overlap(-1) == vt.VT_ERR_INVALID_ARG
+    assert lib.vt_paged_attn_set_overlap(1) == vt.VT_OK
+    assert lib.vt_paged_attn_set_overlap(0) == vt.VT_OK
+    assert lib.vt_paged_attn_set_segment_cost(65) == vt.VT_ERR_INVALID_ARG
+    for tiles in (-1, 0, 2, 64):
+        assert lib.vt_paged_attn_set_segment_cost(tiles) == vt.VT_OK
+    assert lib.vt_paged_attn_set_segment_cost(-1) == vt.VT_OK
+
+
+def test_plan_struct_matches_header():
+    """The ctypes mirror of vt_plan lists the header's fields in order."""
+    text = (ROOT / "include" / "vt_paged_attn.h").read_text()
+    body = text[text.index("typedef struct {", text.index("What the last successful")):text.index("} vt_plan;")]
+    names = re.findall(r"^\s*(?:int|size_t)\s+(\w+);", body, re.M)
+    assert names == [n for n, _ in vt.vt_plan._fields_]
+
+
 def test_last_plan_before_any_launch(lib):
     p = vt.vt_plan()
     assert lib.vt_paged_attn_last_plan(None) == vt.VT_ERR_INVALID_ARG
