@@ -4,17 +4,19 @@
 //   S1  request lookup   each CTA reads context_lens on the device, forms the
 //                        flattened work space of (sequence, kv head, page)
 //                        tiles and takes an even, contiguous slice of it
-//                        (stream-K style), so long and short sequences are
-//                        balanced without any host-side knowledge of lengths;
+//                        (stream-K style; each (sequence, kv head) also
+//                        weighs a little for its segment overhead), so long
+//                        and short sequences are balanced without any
+//                        host-side knowledge of lengths;
 //   S2  page gather      a producer warp streams each K and V page tile
 //                        (32 tokens x head_dim, NHD, row stride Hkv*head_dim)
-//                        with 3-D TMA copies into a ring of shared-memory
+//                        with one TMA copy each into a ring of shared-memory
 //                        stages guarded by mbarriers;
 //   S3  QK^T (GQA)       the g query rows that share a kv head are computed
 //                        together, so every K/V byte is read from HBM once
 //                        per kv head.  bf16 storage: tensor cores
-//                        (mma.sync m16n8k16, queries as the M dimension);
-//                        fp32 storage: CUDA-core FMAs;
+//                        (mma.sync m16n8k16, the page's tokens as M and the
+//                        query group as N); fp32 storage: CUDA-core FMAs;
 //   S4  mask             tail slots past the context and tokens before the
 //                        window are excluded; pages wholly outside the window
 //                        are never loaded;
@@ -25,8 +27,9 @@
 //                        weights keep ~16 significant bits);
 //   S7  split partials   a (sequence, kv head) whose tiles span several CTAs
 //                        leaves one normalised partial (o, m, l) per CTA;
-//   S8  LSE combine      the last CTA to finish such an item merges the
-//                        partials (found through an arrival counter);
+//   S8  LSE combine      the last CTA to finish such an item (found through
+//                        an arrival counter) stages the partials with bulk
+//                        copies and merges them;
 //   S9  finalize         out = acc / l, rounded once to the storage type.
 //
 // Operation defined by: issue "ROCm gfx1200: PagedAttnOnline is 8.1x slower
@@ -104,7 +107,7 @@ struct StageHeader {
   int nsplit;   // CTAs sharing this (sequence, virtual head)
   int slot;     // this CTA's partial slot for it
   int c_first;  // first CTA sharing it
-  long long item_u;  // first tile index of the (sequence, virtual head)
+  long long item_u;  // work unit of the item's first page
 };
 
 // Consumer kinds.
