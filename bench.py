@@ -39,9 +39,9 @@ METRIC = "µs/call and achieved KV HBM GB/s (fraction of GB300 peak) per decode 
 UNIT = "µs/call"
 DEFAULT_WORKLOAD = "qwen3_1p7b_b8_gqa2_d128"
 SWEEP = ["d256_gqa4_b16", "d256_gqa4_b16_w1024", "d256_gqa4_b16_f32", "large_gqa8_b64_d128",
-         "skewed_b128_gqa4_d128", "batch1_ctx32768_gqa4_d128"]
+         "skewed_b128_gqa4_d128", "batch1_ctx32768_gqa4_d128", "d64_gqa4_b32", "d64_gqa4_b32_f32"]
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "decode_d128_bf16.cu", "decode_d256_bf16.cu",
+KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "decode_d64.cu", "decode_d128_bf16.cu", "decode_d256_bf16.cu",
                   "decode_d128_f32.cu", "decode_d256_f32.cu", "vt_paged_attn_api.cu"]
 
 

@@ -69,7 +69,7 @@ typedef enum { VT_BF16 = 0, VT_F32 = 1 } vt_dtype;
  *   context_lens [num_seqs] int32, 0 <= L_b <= max_blocks_per_seq * block_size.
  * Sizes:
  *   num_seqs >= 0 (0 is a no-op), num_q_heads % num_kv_heads == 0,
- *   head_dim in {128, 256}, block_size == 32, scale finite (1/sqrt(head_dim)
+ *   head_dim in {64, 128, 256}, block_size == 32, scale finite (1/sqrt(head_dim)
  *   is usual), window <= 0 for full context else the number of most recent
  *   tokens attended (query token included).
  * Forced additions to the classic signature:

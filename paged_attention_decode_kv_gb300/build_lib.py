@@ -21,6 +21,7 @@ BUILD = HERE / "_build"
 LIBRARY = BUILD / "libvt_paged_attn.so"
 SOURCES = [
     "vt_paged_attn_api.cu",
+    "decode_d64.cu",
     "decode_d128_bf16.cu",
     "decode_d256_bf16.cu",
     "decode_d128_f32.cu",

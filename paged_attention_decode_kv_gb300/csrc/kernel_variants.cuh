@@ -78,6 +78,8 @@ struct Variant {
 
 // One table per (head_dim, dtype); each defined in its own translation unit
 // so the variants compile in parallel.
+const VariantInfo* variants_d64_bf16(int* count);
+const VariantInfo* variants_d64_f32(int* count);
 const VariantInfo* variants_d128_bf16(int* count);
 const VariantInfo* variants_d256_bf16(int* count);
 const VariantInfo* variants_d128_f32(int* count);

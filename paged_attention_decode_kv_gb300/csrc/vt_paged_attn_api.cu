@@ -45,6 +45,8 @@ vt_status cuda_fail(cudaError_t e, const char* where) {
 const VariantInfo* find_variant(int head_dim, vt_dtype dtype, int group_tile) {
   int n = 0;
   const VariantInfo* table = nullptr;
+  if (head_dim == 64 && dtype == VT_BF16) table = vt::variants_d64_bf16(&n);
+  if (head_dim == 64 && dtype == VT_F32) table = vt::variants_d64_f32(&n);
   if (head_dim == 128 && dtype == VT_BF16) table = vt::variants_d128_bf16(&n);
   if (head_dim == 256 && dtype == VT_BF16) table = vt::variants_d256_bf16(&n);
   if (head_dim == 128 && dtype == VT_F32) table = vt::variants_d128_f32(&n);
@@ -343,7 +345,7 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return VT_ERR_INVALID_ARG;
-  if (head_dim != 128 && head_dim != 256) return VT_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return VT_ERR_UNSUPPORTED;
   if (block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
@@ -475,7 +477,7 @@ vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_c
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(block_tables, 4) || !aligned(context_lens, 4))
     return VT_ERR_INVALID_ARG;
-  if (head_dim != 128 && head_dim != 256) return VT_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return VT_ERR_UNSUPPORTED;
   if (block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;

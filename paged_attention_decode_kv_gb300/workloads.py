@@ -107,6 +107,20 @@ D256_GQA4_F32_W1024 = _register(D256_GQA4.with_(
     name="d256_gqa4_b16_f32_w1024", dtype="f32", window=1024,
     description=D256_GQA4.description + "; fp32 storage; sliding window 1024"))
 
+# head_dim 64 arm: not a configuration of the pages (their kernels cover
+# head_dim 128, 256 and 512); the d256 batch's lengths at a Qwen-like
+# 16 q / 4 kv heads, so every (sequence, kv head) page tile is 4 KB.
+D64_GQA4 = _register(Workload(
+    name="d64_gqa4_b32",
+    description="head_dim 64 GQA-4 decode: 32 seqs, 16 q / 4 kv heads, contexts U[512,4096]; "
+                "8192-page pool",
+    num_seqs=32, num_q_heads=16, num_kv_heads=4, head_dim=64, pool_blocks=8192,
+    contexts="uniform:512,4096", max_blocks_per_seq=128))
+
+D64_GQA4_F32 = _register(D64_GQA4.with_(
+    name="d64_gqa4_b32_f32", dtype="f32",
+    description=D64_GQA4.description + "; fp32 storage"))
+
 LARGE_GQA = _register(Workload(
     name="large_gqa8_b64_d128",
     description="Large-GQA server batch: 64 seqs, 64 q / 8 kv heads, head_dim 128, contexts "

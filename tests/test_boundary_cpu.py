@@ -61,7 +61,7 @@ def _call(**over):
     (dict(context_lens=0x6002), vt.VT_ERR_INVALID_ARG),       # 4-byte alignment
     (dict(num_q_heads=12, num_kv_heads=8), vt.VT_ERR_INVALID_ARG),
     (dict(num_kv_heads=0), vt.VT_ERR_INVALID_ARG),
-    (dict(head_dim=64), vt.VT_ERR_UNSUPPORTED),
+    (dict(head_dim=96), vt.VT_ERR_UNSUPPORTED),
     (dict(head_dim=512), vt.VT_ERR_UNSUPPORTED),
     (dict(block_size=16), vt.VT_ERR_UNSUPPORTED),
     (dict(max_blocks_per_seq=0), vt.VT_ERR_INVALID_ARG),
@@ -110,4 +110,4 @@ def test_last_plan_before_any_launch(lib):
 def test_workspace_bytes_rejects_bad_shapes(lib):
     assert vt.vt_paged_attn_workspace_bytes(0, 16, 8, 128, vt.VT_BF16) == 0
     assert vt.vt_paged_attn_workspace_bytes(4, 12, 8, 128, vt.VT_BF16) == 0
-    assert vt.vt_paged_attn_workspace_bytes(4, 16, 8, 64, vt.VT_BF16) == 0
+    assert vt.vt_paged_attn_workspace_bytes(4, 16, 8, 96, vt.VT_BF16) == 0

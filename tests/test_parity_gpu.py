@@ -92,7 +92,8 @@ def check_case(case, dev, rows=None, **kw):
 
 
 # ---------------------------------------------------------------------------
-SMALL = [W.TINY, W.QWEN3_1P7B, W.D256_GQA4, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D256_GQA4_F32_W1024]
+SMALL = [W.TINY, W.QWEN3_1P7B, W.D256_GQA4, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D256_GQA4_F32_W1024,
+         W.D64_GQA4, W.D64_GQA4_F32]
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -121,7 +122,7 @@ def test_workload_full_size_sampled(dev, w):
 
 
 @pytest.mark.parametrize("grid", [1, 2, 3, 7, 64, 152, 500, 1500])
-@pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_W1024, W.D256_GQA4_F32], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D64_GQA4], ids=lambda w: w.name)
 def test_forced_partitions(dev, w, grid):
     """The split/no-split paths and the combine: any CTA count (with at least
     one tile per CTA) gives the oracle's result."""
@@ -142,7 +143,7 @@ def test_page_boundary_contexts(dev, ctx):
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4), (16, 4), (20, 4), (32, 4), (48, 4), (64, 4), (6, 2)])
-@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (128, "f32")])
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (128, "f32"), (64, "bf16"), (64, "f32")])
 def test_group_sizes(dev, hq, hkv, d, dtype):
     """GQA groups 1..16 including ones that pad the group tile (3, 5) or need
     several query subgroups per kv head (12, 16)."""
@@ -156,6 +157,16 @@ def test_windows(dev, window):
     case = W.make_case(W.custom("win", [1, 33, 300, 1000], 16, 4, 128), 9)
     check_case(case, dev, window=window)
     check_case(case, dev, window=window, grid=11, min_units=1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_head_dim_64_windows_and_boundaries(dev, dtype):
+    """The head_dim 64 arm on the straddling contexts, with and without a
+    window, split and unsplit."""
+    case = W.make_case(W.custom("d64_edges", list(STRADDLE), 16, 8, 64, dtype=dtype), 22)
+    for window in (0, 33, 300):
+        check_case(case, dev, window=window)
+        check_case(case, dev, window=window, grid=13, min_units=1)
 
 
 def test_empty_contexts_give_zero_rows(dev):
