@@ -6,7 +6,8 @@ contents, context lengths and block tables, and lays them out.
 
 The shapes follow the decode workloads the pages measure (Qwen3-family decode
 with 32-token pages, GQA groups of 2 to 8, head_dim 128 and 256), as five
-named configurations plus a batch-1 long-context case.  Recipe, per case:
+named configurations plus a batch-1 long-context case, and a head_dim 64
+batch for that arm of the library.  Recipe, per case:
 
 * one ``torch.Generator`` seeded with ``seed`` draws, in this order: the
   context lengths, a random permutation of the page pool, Q, K (all used
