@@ -140,6 +140,14 @@ def pin_sdpa_fp32_storage_d256(oracle):
     _check_against_sdpa(oracle, rng, [1, 33, 70], 8, 2, 256, 32, "f32", 17, 1e-12)
 
 
+def pin_sdpa_head_dim_64(oracle):
+    """The head_dim 64 shape (the library's third arm): bf16 and fp32 storage,
+    a window, GQA 4, against brute force."""
+    rng = np.random.default_rng(23)
+    _check_against_sdpa(oracle, rng, [1, 31, 33, 100], 8, 2, 64, 32, "bf16", 0, 1e-12)
+    _check_against_sdpa(oracle, rng, [1, 31, 33, 100], 8, 2, 64, 32, "f32", 45, 1e-12)
+
+
 def pin_context_one_returns_v(oracle):
     """softmax over one key is 1: the row is that token's value, bit for bit."""
     rng = np.random.default_rng(14)
