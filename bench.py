@@ -45,10 +45,22 @@ KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "decode_d64.cu", "
                   "decode_d128_f32.cu", "decode_d256_f32.cu", "vt_paged_attn_api.cu"]
 
 
+def _code_only(text: str) -> str:
+    """C++ source with comments and blank lines removed (the sources hold no
+    comment markers inside string literals)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_hash() -> str:
+    """Hash of the kernel and front-end code (comments excluded), stamped on
+    the ncu summaries so a measurement is only reused for the code it was
+    taken on."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        h.update((ROOT / "paged_attention_decode_kv_gb300" / "csrc" / name).read_bytes())
+        h.update(_code_only((ROOT / "paged_attention_decode_kv_gb300" / "csrc" / name).read_text()).encode())
     return h.hexdigest()[:16]
 
 

@@ -665,9 +665,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               mbar_arrive_expect_tx(&s.full[stage], bytes);
             }
             __syncwarp();
-            // One tensor copy per K (or V) tile, each issued by its own lane: a
-            // TMA instruction occupies its issuing thread for a hundred cycles
-            // or more, so the fewer and larger the boxes the faster the gather.
+            // One tensor copy per K (or V) tile, each issued by its own lane.
             // bf16 boxes cover (64 columns, 32 tokens, D/64 column blocks) of one
             // head, landing as D/64 swizzled [token][64] sub-tiles.
             if (!bad && lane < 2) {
@@ -1234,11 +1232,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   }  // segment loop
 
   // ===================== S8: deferred LSE combines ============================
-  // Run after this CTA consumed all its tiles, so the stage ring is free.  One
-  // bulk copy per partial record, spread over the lanes of all consumer
-  // warps and all in flight at once, stages a round of an item's partials.
-  // Each thread then merges its 4-column chunks: the round's largest m first,
-  // then every partial weighted by l * 2^(m - M).
+  // Run after this CTA consumed all its tiles, so the stage ring is free.  An
+  // item's partials are one run of records (see DecodeArgs::part): one or two
+  // bulk copies stage a round of them.  Each thread then merges its 4-column
+  // chunks, weighting every partial by l * 2^(m - M).
   if (!alive) return;
   if (!cons_sync()) return;  // pend_n was written by thread 0
   const int n_pend = s.pend_n;
