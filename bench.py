@@ -41,8 +41,7 @@ DEFAULT_WORKLOAD = "qwen3_1p7b_b8_gqa2_d128"
 SWEEP = ["d256_gqa4_b16", "d256_gqa4_b16_w1024", "d256_gqa4_b16_f32", "large_gqa8_b64_d128",
          "skewed_b128_gqa4_d128", "batch1_ctx32768_gqa4_d128", "d64_gqa4_b32", "d64_gqa4_b32_f32"]
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "decode_d64.cu", "decode_d128_bf16.cu", "decode_d256_bf16.cu",
-                  "decode_d128_f32.cu", "decode_d256_f32.cu", "vt_paged_attn_api.cu"]
+KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "vt_paged_attn_api.cu"]  # shared by every variant
 
 
 def _code_only(text: str) -> str:
@@ -54,12 +53,20 @@ def _code_only(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
-def kernel_hash() -> str:
-    """Hash of the kernel and front-end code (comments excluded), stamped on
-    the ncu summaries so a measurement is only reused for the code it was
-    taken on."""
+def variant_source(workload: str) -> str:
+    """The translation unit holding the kernel variants a workload runs on."""
+    from paged_attention_decode_kv_gb300 import workloads as W
+    w = W.WORKLOADS[workload]
+    return "decode_d64.cu" if w.head_dim == 64 else f"decode_d{w.head_dim}_{w.dtype}.cu"
+
+
+def kernel_hash(workload: str = DEFAULT_WORKLOAD) -> str:
+    """Hash of the code a workload's kernel is built from (the shared kernel
+    and front end plus its variant unit; comments excluded), stamped on the
+    ncu summaries so a measurement is only reused for the code it was taken
+    on."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES + [variant_source(workload)]:
         h.update(_code_only((ROOT / "paged_attention_decode_kv_gb300" / "csrc" / name).read_text()).encode())
     return h.hexdigest()[:16]
 
@@ -85,7 +92,7 @@ def recorded_traffic(workload: str):
     except Exception:
         return None
     entry = data.get(workload)
-    if not entry or entry.get("kernel_hash") != kernel_hash():
+    if not entry or entry.get("kernel_hash") != kernel_hash(workload):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -489,7 +496,7 @@ def run_ours(args, rank, world, dist):
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"]},
         "plan": plan,
-        "kernel_hash": kernel_hash(),
+        "kernel_hash": kernel_hash(w.name),
         "sweep": sweep,
     }
     print(json.dumps(line), flush=True)

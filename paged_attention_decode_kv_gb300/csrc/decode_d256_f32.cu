@@ -1,15 +1,16 @@
 // Decode kernel variants for head_dim 256, f32 storage, CUDA-core consumer:
-// group tiles 1, 2, 4, 8.
+// group tiles 1, 2, 4, 8.  A 2-stage ring (1 CTA/SM, 128 KB of pages in flight
+// per SM): 3 stages measured slower on GB300.
 #include "kernel_variants.cuh"
 
 namespace vt {
 
 const VariantInfo* variants_d256_f32(int* count) {
   static const VariantInfo table[] = {
-      Variant<256, float, 1, 8, 1, 4, Math::kSimt>::info(),
-      Variant<256, float, 2, 8, 1, 4, Math::kSimt>::info(),
-      Variant<256, float, 4, 8, 1, 4, Math::kSimt>::info(),
-      Variant<256, float, 8, 8, 1, 4, Math::kSimt>::info(),
+      Variant<256, float, 1, 8, 1, 2, Math::kSimt>::info(),
+      Variant<256, float, 2, 8, 1, 2, Math::kSimt>::info(),
+      Variant<256, float, 4, 8, 1, 2, Math::kSimt>::info(),
+      Variant<256, float, 8, 8, 1, 2, Math::kSimt>::info(),
   };
   *count = 4;
   return table;
