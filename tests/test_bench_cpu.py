@@ -27,7 +27,7 @@ def test_every_workload_maps_to_an_existing_variant_unit():
         assert len(bench.kernel_hash(name)) == 16
 
 
-def test_recorded_traffic_only_for_matching_code(tmp_path, monkeypatch):
+def test_recorded_traffic_only_for_matching_code():
     """A stored DRAM figure is reported only while its stamp matches the code
     of that workload's kernel."""
     data = json.loads((ROOT / "profiles" / "traffic.json").read_text())
