@@ -145,7 +145,7 @@ typedef struct {
   int stages;             /* K/V page tiles in flight per CTA */
   int group_tile;         /* query heads computed per kv head and CTA (padded) */
   int subgroups;          /* ceil(group / group_tile) */
-  int min_units_per_cta;  /* lower bound on (page, kv head) tiles per CTA */
+  int min_units_per_cta;  /* lower bound on work units per CTA (page tiles plus item weights) */
   int head_dim;
   int dtype;              /* vt_dtype */
   size_t smem_bytes;      /* dynamic shared memory per CTA */
