@@ -86,6 +86,12 @@ def compare(got, ref, dtype, what=""):
 
 def check_case(case, dev, rows=None, **kw):
     out, plan = gpu_run(case, dev, **kw)
+    # the intended variant ran: head_dim, storage type and consumer kind
+    w = case.workload
+    bf16 = case.q.dtype == torch.bfloat16
+    assert plan["head_dim"] == w.head_dim and plan["dtype"] == (vt.VT_BF16 if bf16 else vt.VT_F32)
+    assert plan["tensor_cores"] == (1 if bf16 else 0)
+    assert plan["group_tile"] * plan["subgroups"] >= w.num_q_heads // w.num_kv_heads
     idx, ref = oracle_rows(case, rows, window=kw.get("window"))
     got = out[idx[:, 0], idx[:, 1]].to(torch.float64).numpy()
     return compare(got, ref, case.q.dtype, case.workload.name), plan
