@@ -133,14 +133,18 @@ def vt_paged_attn_last_plan() -> dict:
 
 
 def vt_paged_attn_set_override(grid_ctas: int = 0, min_units_per_cta: int = 0) -> None:
+    """Force the CTA count and/or the minimum work per CTA (0: automatic)."""
     _check(library().vt_paged_attn_set_override(grid_ctas, min_units_per_cta), "vt_paged_attn_set_override")
 
 
 def vt_paged_attn_set_overlap(enabled: bool) -> None:
+    """Launch decodes as programmatic dependents of the previous kernel on the
+    stream (that kernel must not write context_lens or block_tables)."""
     _check(library().vt_paged_attn_set_overlap(1 if enabled else 0), "vt_paged_attn_set_overlap")
 
 
 def vt_paged_attn_set_segment_cost(tiles: int = -1) -> None:
+    """Partition weight of a (sequence, kv head) boundary in tiles (-1: default 2)."""
     _check(library().vt_paged_attn_set_segment_cost(tiles), "vt_paged_attn_set_segment_cost")
 
 
