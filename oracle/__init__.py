@@ -26,7 +26,7 @@ SOURCE = HERE / "paged_attn_oracle.c"
 BUILD_DIR = HERE / "_build"
 LIBRARY = BUILD_DIR / "libpaged_attn_oracle.so"
 
-ELEM_BF16, ELEM_F32, ELEM_F64 = 0, 1, 2
+ELEM_BF16, ELEM_F32, ELEM_F64, ELEM_E4M3 = 0, 1, 2, 3
 ERRORS = {0: "ok", -1: "bad argument", -2: "bad context length",
           -3: "page id out of range", -4: "out of memory"}
 
@@ -81,6 +81,9 @@ class Oracle:
         self._lib.oracle_decode.restype = c_int
         self._lib.oracle_decode_rows.argtypes = [c_void, c_void, c_int] + common
         self._lib.oracle_decode_rows.restype = c_int
+        self._lib.oracle_decode_rows_kv.argtypes = [c_void, c_void, c_int, c_void, c_int, c_void, c_void, c_int,
+                                                    c_void, c_void] + common[4:]
+        self._lib.oracle_decode_rows_kv.restype = c_int
 
     @staticmethod
     def _prepare(q, k_cache, v_cache, block_tables, context_lens):
@@ -143,6 +146,35 @@ class Oracle:
         for rc in rcs:
             if rc != 0:
                 raise OracleError(ERRORS.get(rc, str(rc)))
+        return out
+
+
+    def decode_rows_e4m3(self, rows, q, k_codes, v_codes, k_scale, v_scale, block_tables,
+                         context_lens, scale, window=0):
+        """Selected rows of a decode over an FP8 (E4M3) KV cache: k_codes and
+        v_codes are uint8 code arrays [blocks][P][Hkv][D]; element (.., h, d)
+        stands for its E4M3 value times k_scale[h] (v_scale[h]).  q is bf16 bits
+        (uint16), float32 or float64.  Returns float64 [len(rows)][D]."""
+        q = np.ascontiguousarray(q)
+        q_elem = _elem_code(q)
+        k_codes = np.ascontiguousarray(k_codes, dtype=np.uint8)
+        v_codes = np.ascontiguousarray(v_codes, dtype=np.uint8)
+        if q.ndim != 3 or k_codes.ndim != 4 or k_codes.shape != v_codes.shape:
+            raise ValueError("q is [B][Hq][D]; k_codes and v_codes are [blocks][P][Hkv][D]")
+        B, Hq, D = q.shape
+        nb, P, Hkv, D2 = k_codes.shape
+        ks = np.ascontiguousarray(k_scale, dtype=np.float64).reshape(Hkv)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float64).reshape(Hkv)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        assert D2 == D and bt.shape[0] == B and cl.shape == (B,)
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros((rows.shape[0], D), dtype=np.float64)
+        rc = self._lib.oracle_decode_rows_kv(
+            _ptr(out), _ptr(rows), rows.shape[0], _ptr(q), q_elem, _ptr(k_codes), _ptr(v_codes), ELEM_E4M3,
+            _ptr(ks), _ptr(vs), _ptr(bt), _ptr(cl), B, Hq, Hkv, D, P, bt.shape[1], nb, float(scale), int(window))
+        if rc != 0:
+            raise OracleError(ERRORS.get(rc, str(rc)))
         return out
 
 

@@ -32,6 +32,9 @@
  * binary64) and all arithmetic is double.
  *
  * Readings taken where the pages are silent:
+ *   - a quantised KV cache (FP8 E4M3 codes, a storage extension beyond the
+ *     pages) stands for its code values times one scale per kv head, one set
+ *     of scales for keys and one for values (oracle_decode_row_kv);
  *   - kv head of query head i is i / g (contiguous query groups);
  *   - cache layout [num_blocks][block_size][num_kv_heads][head_dim], head_dim
  *     contiguous ("NHD");
@@ -58,6 +61,7 @@
 #define ORACLE_ELEM_BF16 0 /* uint16 bit patterns of bfloat16 */
 #define ORACLE_ELEM_F32 1
 #define ORACLE_ELEM_F64 2
+#define ORACLE_ELEM_E4M3 3 /* uint8 codes of OCP FP8 E4M3 (KV cache storage only) */
 
 /* bfloat16 is the upper half of an IEEE binary32 word: shifting the 16 stored
  * bits into the top of a 32-bit word gives that binary32 value exactly. */
@@ -68,6 +72,20 @@ static double widen_bf16(uint16_t bits) {
   return (double)f;
 }
 
+/* OCP 8-bit floating point, E4M3 flavour: sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits.  Exponent field 0 holds the subnormals m/8 * 2^-6; the
+ * pattern with all exponent and mantissa bits set is NaN; there is no
+ * infinity, so exponent field 15 with mantissa 0..6 is an ordinary value
+ * (the largest, 1.75 * 2^8 = 448). */
+static double widen_e4m3(uint8_t code) {
+  const int sign = code >> 7;
+  const int ex = (code >> 3) & 0xF;
+  const int man = code & 0x7;
+  if (ex == 0xF && man == 0x7) return NAN;
+  const double mag = (ex == 0) ? ldexp((double)man / 8.0, 1 - 7) : ldexp(1.0 + (double)man / 8.0, ex - 7);
+  return sign ? -mag : mag;
+}
+
 /* Element e of an array stored with code `elem`, widened to double. */
 static double element(const void* base, int elem, size_t e) {
   switch (elem) {
@@ -75,6 +93,8 @@ static double element(const void* base, int elem, size_t e) {
       return widen_bf16(((const uint16_t*)base)[e]);
     case ORACLE_ELEM_F32:
       return (double)((const float*)base)[e];
+    case ORACLE_ELEM_E4M3:
+      return widen_e4m3(((const uint8_t*)base)[e]);
     default:
       return ((const double*)base)[e];
   }
@@ -87,23 +107,31 @@ static size_t cache_index(int page, int slot, int h, int d, int block_size,
   return (((size_t)page * block_size + slot) * num_kv_heads + h) * head_dim + d;
 }
 
-/* One output row: sequence b, query head i.  out_row has head_dim doubles. */
-int oracle_decode_row(double* out_row, const void* q, const void* k_cache,
-                      const void* v_cache, int elem,
-                      const int32_t* block_tables, const int32_t* context_lens,
-                      int num_seqs, int num_q_heads, int num_kv_heads,
-                      int head_dim, int block_size, int max_blocks_per_seq,
-                      int num_blocks, double scale, int window, int b, int i) {
+/* One output row: sequence b, query head i.  out_row has head_dim doubles.
+ * q is stored with code q_elem, the caches with kv_elem; a cache element of
+ * kv head h stands for its stored value times k_scale[h] (keys) or
+ * v_scale[h] (values), the per-head dequantisation scales of a quantised
+ * cache (NULL: 1). */
+int oracle_decode_row_kv(double* out_row, const void* q, int q_elem,
+                         const void* k_cache, const void* v_cache, int kv_elem,
+                         const double* k_scale, const double* v_scale,
+                         const int32_t* block_tables, const int32_t* context_lens,
+                         int num_seqs, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int max_blocks_per_seq,
+                         int num_blocks, double scale, int window, int b, int i) {
   if (!out_row || !q || !k_cache || !v_cache || !block_tables ||
       !context_lens || num_seqs <= 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
       max_blocks_per_seq <= 0 || num_blocks <= 0 ||
       num_q_heads % num_kv_heads != 0 || b < 0 || b >= num_seqs || i < 0 ||
-      i >= num_q_heads || elem < ORACLE_ELEM_BF16 || elem > ORACLE_ELEM_F64)
+      i >= num_q_heads || q_elem < ORACLE_ELEM_BF16 || q_elem > ORACLE_ELEM_F64 ||
+      kv_elem < ORACLE_ELEM_BF16 || kv_elem > ORACLE_ELEM_E4M3)
     return ORACLE_BAD_ARG;
 
   const int group = num_q_heads / num_kv_heads;
   const int h = i / group;
+  const double ks = k_scale ? k_scale[h] : 1.0;
+  const double vs = v_scale ? v_scale[h] : 1.0;
   const int L = context_lens[b];
   if (L < 0 || (long long)L > (long long)max_blocks_per_seq * block_size)
     return ORACLE_BAD_CONTEXT;
@@ -138,10 +166,10 @@ int oracle_decode_row(double* out_row, const void* q, const void* k_cache,
     const int slot = (t0 + j) % block_size;
     double dot = 0.0;
     for (int d = 0; d < head_dim; ++d) {
-      const double kd = element(k_cache, elem,
+      const double kd = element(k_cache, kv_elem,
                                 cache_index(page_of[j], slot, h, d, block_size,
-                                            num_kv_heads, head_dim));
-      dot += element(q, elem, q_row + d) * kd;
+                                            num_kv_heads, head_dim)) * ks;
+      dot += element(q, q_elem, q_row + d) * kd;
     }
     s[j] = scale * dot;
   }
@@ -158,15 +186,29 @@ int oracle_decode_row(double* out_row, const void* q, const void* k_cache,
     const double w = exp(s[j] - M);
     Z += w;
     for (int d = 0; d < head_dim; ++d)
-      out_row[d] += w * element(v_cache, elem,
+      out_row[d] += w * element(v_cache, kv_elem,
                                 cache_index(page_of[j], slot, h, d, block_size,
-                                            num_kv_heads, head_dim));
+                                            num_kv_heads, head_dim)) * vs;
   }
   for (int d = 0; d < head_dim; ++d) out_row[d] /= Z;
 
   free(page_of);
   free(s);
   return ORACLE_OK;
+}
+
+/* The same with one storage code for q and both caches, and no scales. */
+int oracle_decode_row(double* out_row, const void* q, const void* k_cache,
+                      const void* v_cache, int elem,
+                      const int32_t* block_tables, const int32_t* context_lens,
+                      int num_seqs, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int max_blocks_per_seq,
+                      int num_blocks, double scale, int window, int b, int i) {
+  if (elem > ORACLE_ELEM_F64) return ORACLE_BAD_ARG;
+  return oracle_decode_row_kv(out_row, q, elem, k_cache, v_cache, elem, NULL, NULL,
+                              block_tables, context_lens, num_seqs, num_q_heads,
+                              num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                              num_blocks, scale, window, b, i);
 }
 
 /* Every row: out is [num_seqs][num_q_heads][head_dim] doubles. */
@@ -206,6 +248,28 @@ int oracle_decode_rows(double* out, const int32_t* rows, int num_rows,
         context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
         block_size, max_blocks_per_seq, num_blocks, scale, window, rows[2 * r],
         rows[2 * r + 1]);
+    if (rc != ORACLE_OK) return rc;
+  }
+  return ORACLE_OK;
+}
+
+/* Chosen rows of a decode whose caches are stored with their own code and
+ * per-head scales (quantised KV cache); see oracle_decode_row_kv. */
+int oracle_decode_rows_kv(double* out, const int32_t* rows, int num_rows,
+                          const void* q, int q_elem, const void* k_cache,
+                          const void* v_cache, int kv_elem, const double* k_scale,
+                          const double* v_scale, const int32_t* block_tables,
+                          const int32_t* context_lens, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int max_blocks_per_seq, int num_blocks,
+                          double scale, int window) {
+  if (!out || !rows || num_rows < 0 || head_dim <= 0) return ORACLE_BAD_ARG;
+  for (int r = 0; r < num_rows; ++r) {
+    const int rc = oracle_decode_row_kv(
+        out + (size_t)r * head_dim, q, q_elem, k_cache, v_cache, kv_elem, k_scale,
+        v_scale, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+        head_dim, block_size, max_blocks_per_seq, num_blocks, scale, window,
+        rows[2 * r], rows[2 * r + 1]);
     if (rc != ORACLE_OK) return rc;
   }
   return ORACLE_OK;

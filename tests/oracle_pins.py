@@ -9,7 +9,8 @@ when the oracle disagrees with:
     returns the last token; two tokens give a logistic blend; a hand-worked
     fixture under tests/golden/),
   * an invariance (physical page order, block size, splitting query heads),
-  * the bfloat16 format (bit patterns whose values are fixed by the format).
+  * the bfloat16 and FP8 E4M3 formats (codes whose values are fixed by the
+    format; torch's float8_e4m3fn as an independent decoder).
 ``test_oracle.py`` runs them on the real oracle and ``test_oracle_mutants.py``
 runs them on deliberately broken copies to show each plausible mistake is
 caught by at least one of them.
@@ -42,7 +43,8 @@ def paginate(dense_k, dense_v, block_size, rng, num_blocks=None, pad_pages=3):
     nb = num_blocks if num_blocks is not None else used + pad_pages
     perm = rng.permutation(nb)
     dtype = dense_k[0].dtype
-    fill = 0x7FC0 if dtype == np.uint16 else np.nan  # bf16 NaN bits / float NaN
+    # NaN: bf16 bits, E4M3 code, float
+    fill = 0x7FC0 if dtype == np.uint16 else (0x7F if dtype == np.uint8 else np.nan)
     k_cache = np.full((nb, block_size, hkv, d), fill, dtype=dtype)
     v_cache = np.full((nb, block_size, hkv, d), fill, dtype=dtype)
     maxb = max(max(pages), 1)
@@ -146,6 +148,94 @@ def pin_sdpa_head_dim_64(oracle):
     rng = np.random.default_rng(23)
     _check_against_sdpa(oracle, rng, [1, 31, 33, 100], 8, 2, 64, 32, "bf16", 0, 1e-12)
     _check_against_sdpa(oracle, rng, [1, 31, 33, 100], 8, 2, 64, 32, "f32", 45, 1e-12)
+
+
+def _e4m3_value(codes):
+    """Values of E4M3 codes by torch's float8_e4m3fn (independent of the oracle)."""
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _e4m3_encode(x):
+    """Nearest E4M3 codes of values within +-448 (torch's conversion)."""
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_every_code(oracle):
+    """A one-token context returns V exactly, so V holding all 256 E4M3 codes
+    reads back each code's value: torch's decoder, and the format's closed
+    forms (1, 2, 0.5, the largest 448, the smallest subnormal 2^-9, the
+    smallest normal 2^-6, NaN for S.1111.111)."""
+    D = 256
+    q = np.zeros((1, 1, D))
+    k = np.zeros((1, 32, 1, D), dtype=np.uint8)
+    v = np.zeros((1, 32, 1, D), dtype=np.uint8)
+    v[0, 0, 0] = np.arange(256, dtype=np.uint8)
+    out = oracle.decode_rows_e4m3([(0, 0)], q, k, v, [1.0], [1.0], np.zeros((1, 1), np.int32),
+                                  np.array([1], np.int32), 1.0)[0]
+    want = _e4m3_value(np.arange(256))
+    assert np.array_equal(np.isnan(out), np.isnan(want))
+    assert np.array_equal(out[~np.isnan(out)], want[~np.isnan(want)])
+    closed = {0x38: 1.0, 0x40: 2.0, 0x30: 0.5, 0x7E: 448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6,
+              0x07: 7 * 2.0 ** -9, 0x78: 256.0, 0xB8: -1.0, 0xFE: -448.0, 0x00: 0.0}
+    for c, val in closed.items():
+        assert out[c] == val, (hex(c), out[c], val)
+    assert np.isnan(out[0x7F]) and np.isnan(out[0xFF])
+
+
+def _e4m3_case(rng, lens, hq, hkv, d):
+    """bf16 queries; K/V drawn N(0,1), quantised per kv head so the largest
+    magnitude maps to 448; returns codes, scales and the dequantised values."""
+    q = _rand(rng, (len(lens), hq, d), "bf16")
+    dk = [rng.standard_normal((L, hkv, d)) for L in lens]
+    dv = [rng.standard_normal((L, hkv, d)) for L in lens]
+    ks = np.array([max(np.abs(x[:, h]).max() for x in dk) / 448.0 for h in range(hkv)])
+    vs = np.array([max(np.abs(x[:, h]).max() for x in dv) / 448.0 for h in range(hkv)])
+    ck = [_e4m3_encode(x / ks[None, :, None]) for x in dk]
+    cv = [_e4m3_encode(x / vs[None, :, None]) for x in dv]
+    deq_k = [_e4m3_value(c) * ks[None, :, None] for c in ck]
+    deq_v = [_e4m3_value(c) * vs[None, :, None] for c in cv]
+    return q, ck, cv, ks, vs, deq_k, deq_v
+
+
+def pin_e4m3_kv_against_sdpa(oracle):
+    """FP8 (E4M3) KV cache with per-head scales: brute force on the
+    dequantised K/V (code value times its head's scale), with and without a
+    window, at GQA 4."""
+    rng = np.random.default_rng(24)
+    lens, hq, hkv, d = [1, 33, 70, 5], 8, 2, 64
+    q, ck, cv, ks, vs, deq_k, deq_v = _e4m3_case(rng, lens, hq, hkv, d)
+    kc, vc, bt, cl = paginate(ck, cv, 32, rng)
+    rows = [(b, i) for b in range(len(lens)) for i in range(hq)]
+    scale = 1.0 / math.sqrt(d)
+    for window in (0, 20):
+        got = oracle.decode_rows_e4m3(rows, q, kc, vc, ks, vs, bt, cl, scale, window)
+        want = sdpa_reference(widen(q), deq_k, deq_v, scale, window).reshape(-1, d)
+        err = np.abs(got - want).max()
+        assert err <= 1e-12, f"E4M3 oracle vs SDPA max |err| {err:.3e} (W {window})"
+
+
+def pin_e4m3_scales_act_per_head(oracle):
+    """Doubling one kv head's value scale doubles exactly its query heads'
+    rows and leaves the others; doubling a key scale equals doubling the
+    softmax scale for that head's rows."""
+    rng = np.random.default_rng(25)
+    lens, hq, hkv, d = [9, 40], 4, 2, 32
+    q, ck, cv, ks, vs, _, _ = _e4m3_case(rng, lens, hq, hkv, d)
+    kc, vc, bt, cl = paginate(ck, cv, 32, rng)
+    rows = [(b, i) for b in range(len(lens)) for i in range(hq)]
+    base = oracle.decode_rows_e4m3(rows, q, kc, vc, ks, vs, bt, cl, 0.2)
+    vs2 = vs.copy()
+    vs2[1] *= 2
+    doubled = oracle.decode_rows_e4m3(rows, q, kc, vc, ks, vs2, bt, cl, 0.2)
+    for r, (b, i) in enumerate(rows):
+        factor = 2.0 if i // (hq // hkv) == 1 else 1.0
+        assert np.array_equal(doubled[r], base[r] * factor)
+    ks2 = ks * 2
+    got = oracle.decode_rows_e4m3(rows, q, kc, vc, ks2, vs, bt, cl, 0.2)
+    want = oracle.decode_rows_e4m3(rows, q, kc, vc, ks, vs, bt, cl, 0.4)
+    assert np.abs(got - want).max() <= 1e-15
 
 
 def pin_context_one_returns_v(oracle):

@@ -45,6 +45,14 @@ MUTANTS = {
     "last_token_dropped": ("const int n = L - t0;", "const int n = L - t0 - (L > t0 + 1);", 0),
     "bf16_shift_15": ("((uint32_t)bits) << 16", "((uint32_t)bits) << 15", 0),
     "bf16_low_half": ("((uint32_t)bits) << 16", "((uint32_t)bits)", 0),
+    "e4m3_bias_8": ("ldexp(1.0 + (double)man / 8.0, ex - 7)", "ldexp(1.0 + (double)man / 8.0, ex - 8)", 0),
+    "e4m3_no_subnormals": ("(ex == 0) ? ldexp", "(0) ? ldexp", 0),
+    "e4m3_nan_is_a_value": ("if (ex == 0xF && man == 0x7) return NAN;", "if (0) return NAN;", 0),
+    "e4m3_sign_dropped": ("return sign ? -mag : mag;", "return mag;", 0),
+    "value_scale_on_keys": ("num_kv_heads, head_dim)) * ks;", "num_kv_heads, head_dim)) * vs;", 0),
+    "key_scale_dropped": ("num_kv_heads, head_dim)) * ks;", "num_kv_heads, head_dim));", 0),
+    "value_scale_dropped": ("num_kv_heads, head_dim)) * vs;", "num_kv_heads, head_dim));", 0),
+    "scale_of_kv_head_zero": ("const double ks = k_scale ? k_scale[h] : 1.0;", "const double ks = k_scale ? k_scale[0] : 1.0;", 0),
 }
 
 
