@@ -44,3 +44,13 @@ def test_sweep_and_default_workloads_exist():
     assert bench.DEFAULT_WORKLOAD in W.WORKLOADS
     for name in bench.SWEEP:
         assert name in W.WORKLOADS
+
+
+def test_clock_gate():
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}
+    assert bench.clocks_acceptable(ok)
+    assert bench.clocks_acceptable({**ok, "reasons": ["sw_power_cap"], "sm_mhz": 1500.0})
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert not bench.clocks_acceptable({**ok, "reasons": [r]})
+    assert not bench.clocks_acceptable({**ok, "sm_mhz": 1200.0})  # locked low, no reason
+    assert bench.clocks_acceptable({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0})
