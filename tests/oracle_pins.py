@@ -399,6 +399,30 @@ def pin_scores_scale_by_scale(oracle):
     assert np.abs(a - c).max() > 1e-3
 
 
+def pin_decode_rows_matches_decode(oracle):
+    """The row-sampling entry (what every large GPU parity check compares
+    against) returns, for any list of (sequence, query head) pairs, exactly the
+    rows of the whole-batch decode: pairs shuffled, repeated and out of order,
+    a window, bf16 and fp32 storage, on one host thread and split over seven
+    (a row count seven does not divide, so the split is uneven)."""
+    rng = np.random.default_rng(30)
+    hq, hkv, d = 6, 2, 16
+    lens = [1, 33, 70, 5, 64]
+    for kind in ("bf16", "f32"):
+        q, dk, dv = _case(rng, lens, hq, hkv, d, kind)
+        kc, vc, bt, cl = paginate(dk, dv, 32, rng)
+        for window in (0, 20):
+            full = oracle.decode(q, kc, vc, bt, cl, 0.3, window)
+            pairs = [(b, i) for b in range(len(lens)) for i in range(hq)]
+            order = rng.permutation(len(pairs))
+            rows = [pairs[j] for j in order] + [(3, 5), (0, 0), (3, 5), (4, 1), (1, 4)]
+            for threads in (1, 7):
+                got = oracle.decode_rows(rows, q, kc, vc, bt, cl, 0.3, window, threads=threads)
+                assert got.shape == (len(rows), d)
+                for r, (b, i) in enumerate(rows):
+                    assert np.array_equal(got[r], full[b, i]), (kind, window, threads, r, b, i)
+
+
 def pin_query_heads_independent(oracle):
     """Each query head alone (Hq = Hkv = 1, its kv head's pages) gives the same
     bits as inside the full GQA problem."""

@@ -4,7 +4,9 @@ Every mutant is a one-line textual change to ``oracle/paged_attn_oracle.c``,
 compiled with gcc into a temporary library and run through all pins in its own
 process.  A mutant survives only if every pin passes; the test fails if any
 survives, or if a mutant's anchor text no longer matches the source (so this
-file stays in step with the oracle).  The real oracle is never modified.
+file stays in step with the oracle).  A few more mutants change the oracle's
+Python front end (the split of sampled rows over host threads) and run the
+pin that covers it.  The real oracle is never modified.
 """
 from __future__ import annotations
 
@@ -52,6 +54,9 @@ MUTANTS = {
     "value_scale_on_keys": ("num_kv_heads, head_dim)) * ks;", "num_kv_heads, head_dim)) * vs;", 0),
     "key_scale_dropped": ("num_kv_heads, head_dim)) * ks;", "num_kv_heads, head_dim));", 0),
     "value_scale_dropped": ("num_kv_heads, head_dim)) * vs;", "num_kv_heads, head_dim));", 0),
+    "rows_pair_swapped": ("window, rows[2 * r],\n        rows[2 * r + 1]);", "window, rows[2 * r + 1],\n        rows[2 * r]);", 0),
+    "rows_kv_pair_swapped": ("rows[2 * r], rows[2 * r + 1]);", "rows[2 * r + 1], rows[2 * r]);", 0),
+    "rows_output_not_advanced": ("out + (size_t)r * head_dim, q, k_cache", "out, q, k_cache", 0),
     "scale_of_kv_head_zero": ("const double ks = k_scale ? k_scale[h] : 1.0;", "const double ks = k_scale ? k_scale[0] : 1.0;", 0),
 }
 
@@ -116,3 +121,41 @@ def test_unmutated_copy_passes_all_pins(tmp_path):
     code = RUNNER.format(tests=str(ROOT / "tests"), root=str(ROOT), lib=str(lib))
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True)
     assert json.loads(out.stdout.strip().splitlines()[-1]) == []
+
+
+# Mistakes planted in a copy of the oracle's Python front end (the host-thread
+# split of the row-sampling entry), run through the pin that covers it.
+PY_MUTANTS = {
+    "thread_split_results_dropped": ("sub_out = out[lo:hi]", "sub_out = out[lo:hi].copy()"),
+    "thread_split_rows_shifted": ("sub_rows = np.ascontiguousarray(rows[lo:hi])",
+                                  "sub_rows = np.ascontiguousarray(rows[max(lo - 1, 0):hi - (lo > 0)])"),
+    "thread_split_last_part_dropped": ("range(threads)))", "range(threads - 1)))"),
+}
+
+PY_RUNNER = textwrap.dedent("""
+    import importlib.util, json, sys
+    sys.path.insert(0, {tests!r}); sys.path.insert(0, {root!r})
+    spec = importlib.util.spec_from_file_location("oracle_mut", {init!r})
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    from oracle_pins import pin_decode_rows_matches_decode
+    o = mod.Oracle({lib!r})
+    try:
+        pin_decode_rows_matches_decode(o)
+        print(json.dumps([]))
+    except Exception:
+        print(json.dumps(["pin_decode_rows_matches_decode"]))
+""")
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_python_front_end_mutant_is_caught(tmp_path, name):
+    import oracle
+    anchor, repl = PY_MUTANTS[name]
+    src = (ROOT / "oracle" / "__init__.py").read_text()
+    init = tmp_path / "oracle_mut.py"
+    init.write_text(_mutate(src, anchor, repl, 0))
+    lib = oracle.build()
+    code = PY_RUNNER.format(tests=str(ROOT / "tests"), root=str(ROOT), init=str(init), lib=str(lib))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True)
+    assert json.loads(out.stdout.strip().splitlines()[-1]) != [], f"mutant {name} survived"
