@@ -19,9 +19,10 @@
  *
  * Threading / ordering: every call only enqueues work on `stream` and
  * returns; it never synchronises the device.  The library keeps one
- * split-KV workspace per device; calls that share a device must be ordered
- * on the GPU (same stream, or streams ordered by events), otherwise they race
- * on that workspace.
+ * split-KV workspace per device (its own, or one the caller hands it with
+ * vt_paged_attn_set_workspace); calls that share a device must be ordered on
+ * the GPU (same stream, or streams ordered by events), otherwise they race on
+ * that workspace.
  */
 #ifndef VT_PAGED_ATTN_H
 #define VT_PAGED_ATTN_H
@@ -49,7 +50,8 @@ typedef enum {
   VT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see vt_last_cuda_error() */
   VT_ERR_OOM = 4,           /* the split workspace could not be allocated */
   VT_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up a bounded wait (see vt_paged_attn_device_status) */
-  VT_ERR_SCRATCH_LIMIT = 6   /* vt_paged_attn_decode_noalloc: the call needs more than its fixed scratch */
+  VT_ERR_SCRATCH_LIMIT = 6   /* the call needs more scratch than a fixed buffer holds (the static array
+                                of vt_paged_attn_decode_noalloc, or the caller's vt_paged_attn_set_workspace) */
 } vt_status;
 
 typedef enum { VT_BF16 = 0, VT_F32 = 1 } vt_dtype;
@@ -122,8 +124,11 @@ VT_API vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_ca
  *   arrival counters) on its stream first.  Calls that overlap on the GPU
  *   (concurrent streams, or several host threads) race on the array and
  *   produce wrong results: order them.
- * - The status word of bounded waits lives in the array and is cleared by
- *   the next call; vt_paged_attn_device_status does not read it.
+ * - The status words of bounded waits live in the array; the next call
+ *   clears them.  vt_paged_attn_device_status and
+ *   vt_paged_attn_device_status_detail read them (with the other scratch
+ *   areas of the device), so a give-up on this path is reported like any
+ *   other.
  * - Nothing here calls cudaMalloc, cudaFree or any allocating routine.
  */
 #define VT_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -152,6 +157,8 @@ typedef struct {
   size_t workspace_bytes; /* split-KV workspace used (partials + arrival counters) */
   int launch_overlap;     /* 1: launched as a programmatic dependent (vt_paged_attn_set_overlap) */
   int segment_cost;       /* partition weight of a segment boundary, in tiles (vt_paged_attn_set_segment_cost) */
+  int scratch_source;     /* split scratch used: 0 library-owned, 1 the caller's (vt_paged_attn_set_workspace),
+                             2 the static array (vt_paged_attn_decode_noalloc) */
 } vt_plan;
 
 VT_API vt_status vt_paged_attn_last_plan(vt_plan* plan);
@@ -223,6 +230,52 @@ VT_API vt_status vt_paged_attn_device_status(vt_stream_t stream, unsigned* statu
  * parity it waited for.  Synchronises `stream` first.
  */
 VT_API vt_status vt_paged_attn_device_status_detail(vt_stream_t stream, unsigned* words, int n_words);
+
+/*
+ * vt_paged_attn_set_workspace -- hand the library a caller-owned split-KV
+ * workspace for the current device (the boundary's optional workspace; the
+ * operation itself is unchanged).
+ *
+ * vt_paged_attn_decode needs device scratch for split-KV partial results and
+ * arrival counters.  By default the library allocates it lazily with
+ * cudaMallocAsync on the call's stream and grows it when a call needs more.
+ * After this call, decodes on the current device use [dev_ptr, dev_ptr +
+ * bytes) instead and never allocate:
+ *   dev_ptr  device memory, 256-byte aligned, owned by the caller; it must
+ *            stay allocated and be touched by nothing else while it is set.
+ *            NULL returns the device to the library-owned workspace.
+ *   bytes    >= VT_MIN_WORKSPACE_BYTES.  The arrival counters must stay
+ *            zeroed between calls, so their region only grows: a call needs
+ *            256 bytes, plus the largest counter region any call on this
+ *            workspace used, plus its own partial records.  For one model
+ *            shape (heads, head_dim, dtype) the partials do not depend on the
+ *            batch, so vt_paged_attn_workspace_bytes() of the largest
+ *            num_seqs in use is enough for every call; for several shapes,
+ *            the sum of their largest needs is.
+ *   stream   the first 256 bytes (status words) are zeroed on it; later
+ *            calls zero newly used counter space on their own streams.
+ * A decode that needs more than `bytes` returns VT_ERR_SCRATCH_LIMIT before
+ * launching anything.  Calls that share the workspace must be ordered on
+ * the GPU.  vt_paged_attn_device_status reads its status words.
+ * Returns VT_ERR_INVALID_ARG for a misaligned pointer or a too-small size.
+ */
+#define VT_MIN_WORKSPACE_BYTES 4096u
+VT_API vt_status vt_paged_attn_set_workspace(void* dev_ptr, size_t bytes, vt_stream_t stream);
+
+/*
+ * Test hook for the failure path of bounded waits (this host thread, read on
+ * every call; not an operation of the pages).  Every wait on an mbarrier in
+ * the kernel gives up after a limit of about one second of SM clock cycles,
+ * sets a status bit and lets the CTA exit; this hook shortens the limit to
+ * wait_limit_cycles (<= 0: the default) and, when withhold_tile >= 0, makes
+ * CTA withhold_cta stop feeding its consumers before its withhold_tile-th
+ * tile.  The consumers' wait for that tile then runs out, the kernel returns
+ * without faulting, and vt_paged_attn_device_status reports
+ * VT_ERR_DEVICE_TIMEOUT (bit 0); the output of that call is incomplete.
+ * vt_paged_attn_set_test_wait(0, -1, -1) restores normal operation.
+ * Returns VT_ERR_INVALID_ARG when withhold_tile >= 0 and withhold_cta < 0.
+ */
+VT_API vt_status vt_paged_attn_set_test_wait(long long wait_limit_cycles, int withhold_cta, int withhold_tile);
 
 /* Bytes of split-KV workspace a call with these sizes uses on the current device. */
 VT_API size_t vt_paged_attn_workspace_bytes(int num_seqs, int num_q_heads,

@@ -20,10 +20,13 @@ LIBRARY_PATH = Path(__file__).resolve().parent / "_build" / "libvt_paged_attn.so
 VT_BF16, VT_F32 = 0, 1
 BLOCK_SIZE = 32
 
-EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_last_plan", "vt_paged_attn_set_override",
-            "vt_paged_attn_set_overlap", "vt_paged_attn_set_segment_cost",
-            "vt_paged_attn_device_status", "vt_paged_attn_device_status_detail", "vt_paged_attn_workspace_bytes", "vt_paged_attn_release",
-            "vt_status_string", "vt_last_cuda_error", "vt_paged_attn_version")
+EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_last_plan",
+            "vt_paged_attn_set_override", "vt_paged_attn_set_overlap", "vt_paged_attn_set_segment_cost",
+            "vt_paged_attn_set_workspace", "vt_paged_attn_set_test_wait",
+            "vt_paged_attn_device_status", "vt_paged_attn_device_status_detail", "vt_paged_attn_workspace_bytes",
+            "vt_paged_attn_release", "vt_status_string", "vt_last_cuda_error", "vt_paged_attn_version")
+VT_NOALLOC_SCRATCH_BYTES = 8 << 20
+VT_MIN_WORKSPACE_BYTES = 4096
 
 
 class VtError(RuntimeError):
@@ -41,7 +44,7 @@ class vt_plan(ctypes.Structure):
                 ("subgroups", ctypes.c_int), ("min_units_per_cta", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
                 ("workspace_bytes", ctypes.c_size_t), ("launch_overlap", ctypes.c_int),
-                ("segment_cost", ctypes.c_int)]
+                ("segment_cost", ctypes.c_int), ("scratch_source", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -77,6 +80,10 @@ def library() -> ctypes.CDLL:
             lib.vt_paged_attn_set_overlap.restype = c_int
             lib.vt_paged_attn_set_segment_cost.argtypes = [c_int]
             lib.vt_paged_attn_set_segment_cost.restype = c_int
+            lib.vt_paged_attn_set_workspace.argtypes = [c_void, c_size, c_void]
+            lib.vt_paged_attn_set_workspace.restype = c_int
+            lib.vt_paged_attn_set_test_wait.argtypes = [ctypes.c_longlong, c_int, c_int]
+            lib.vt_paged_attn_set_test_wait.restype = c_int
             lib.vt_paged_attn_device_status.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint)]
             lib.vt_paged_attn_device_status.restype = c_int
             lib.vt_paged_attn_device_status_detail.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint), c_int]
@@ -146,6 +153,20 @@ def vt_paged_attn_set_overlap(enabled: bool) -> None:
 def vt_paged_attn_set_segment_cost(tiles: int = -1) -> None:
     """Partition weight of a (sequence, kv head) boundary in tiles (-1: default 2)."""
     _check(library().vt_paged_attn_set_segment_cost(tiles), "vt_paged_attn_set_segment_cost")
+
+
+def vt_paged_attn_set_workspace(dev_ptr: int, nbytes: int, stream=None) -> None:
+    """Use caller-owned device memory [dev_ptr, dev_ptr + nbytes) as the split
+    workspace of the current device (dev_ptr 0: back to the library's own)."""
+    _check(library().vt_paged_attn_set_workspace(dev_ptr or None, nbytes, _stream_handle(stream)),
+           "vt_paged_attn_set_workspace")
+
+
+def vt_paged_attn_set_test_wait(wait_limit_cycles: int = 0, withhold_cta: int = -1, withhold_tile: int = -1) -> None:
+    """Test hook: shorten the kernel's bounded waits and make one CTA withhold
+    a tile, so a wait gives up (0, -1, -1 restores normal operation)."""
+    _check(library().vt_paged_attn_set_test_wait(wait_limit_cycles, withhold_cta, withhold_tile),
+           "vt_paged_attn_set_test_wait")
 
 
 def vt_paged_attn_device_status(stream=None) -> int:

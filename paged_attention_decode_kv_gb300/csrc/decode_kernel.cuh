@@ -96,6 +96,13 @@ struct DecodeArgs {
   // of consecutive records, plus at most one record of the second half.
   float* part;
   unsigned* status; // status words
+  // Bounded waits give up after wait_limit clock cycles (kWaitLimitCycles
+  // unless a test shortens it).  Test hook: CTA withhold_cta stops feeding
+  // its consumers before its withhold_tile-th tile (-1: never), so their
+  // wait for that tile runs out and reports through the status word.
+  long long wait_limit;
+  int withhold_cta;
+  int withhold_tile;
 };
 
 struct StageHeader {
@@ -132,10 +139,6 @@ struct Smem {
   alignas(1024) T k[NSTAGE][kPageTokens * D];
   alignas(1024) T v[NSTAGE][kPageTokens * D];
   alignas(128) T q[NSTAGE][G * D];
-  // CUDA-core epilogue: the row groups' states summed by shared atomics.
-  static constexpr int RG = (M == Math::kSimt) ? G : 1;
-  static constexpr int RD = (M == Math::kSimt) ? D : 4;
-  alignas(16) float red_acc[RG][RD];
   // Tensor-core epilogue: warps of token half 1 hand their O^T accumulator
   // fragments to the warps of token half 0 ([segment parity][dp][m-tile][lane]);
   // token half 0 then reuses its slice to stage rows for coalesced stores.
@@ -250,6 +253,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// The same for this thread's shared-memory accesses (a stage's tiles that
+// consumers wrote before the producer's next copy into them).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // Arrival counter increment with acquire-release semantics at GPU scope: the
 // release orders every store the CTA made before the preceding rendezvous,
@@ -308,8 +316,7 @@ __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(
 // probe and would sit on the critical path of every wait that does not
 // complete at once.
 __device__ __forceinline__ bool wait_phase(unsigned long long* bar, uint32_t parity, volatile int* abort_flag,
-                                           unsigned* status, unsigned code,
-                                           long long limit = kWaitLimitCycles) {
+                                           unsigned* status, unsigned code, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
@@ -514,7 +521,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     s.b_start_s = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  for (int e = tid; e < G * D; e += NT) (&s.red_acc[0][0])[e] = 0.f;
 
   // ---- S1: request lookup and balanced partition ---------------------------
   // The split balances work units: every page of a (sequence, virtual head)
@@ -605,6 +611,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       return __shfl_sync(0xffffffffu, win_len, bb - win_base);
     };
     bool ok = b >= 0;
+    bool withheld = false;
     long long covered = 0;  // units walked, for the self-check
     while (ok && u < u1) {
       const SeqSpan sp = seq_span(length_of(b), a.window, a.max_blocks);
@@ -642,7 +649,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           for (int jj = 0; jj < n; ++jj) {
             const int pid = __shfl_sync(0xffffffffu, my_id, jj);
             const int p = p0 + jj;
-            ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty);
+            if (static_cast<int>(blockIdx.x) == a.withhold_cta && issued == a.withhold_tile) {
+              withheld = true;  // test hook: this tile never arrives
+              ok = false;
+              break;
+            }
+            ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty, a.wait_limit);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const bool bad = pid < 0 || pid >= a.num_blocks;
@@ -698,7 +710,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       if (b >= a.num_seqs) break;
     }
     // Self-check: the walk must have covered exactly this CTA's slice.
-    if (covered != u1 - u0 && !s.abort_flag && lane == 0) {
+    if (covered != u1 - u0 && !withheld && !s.abort_flag && lane == 0) {
       atomicOr(a.status, kStatusWalk);
       s.abort_flag = 1;
     }
@@ -707,7 +719,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     // it crosses).
     bool end_sent = false;
     if (ok && __all_sync(0xffffffffu, !s.abort_flag)) {
-      ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty);
+      ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty, a.wait_limit);
       end_sent = __all_sync(0xffffffffu, ok);
       if (end_sent && lane == 0) {
         s.hdr[stage].flags = kEnd;
@@ -742,7 +754,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   auto cons_sync = [&]() -> bool {
     __syncwarp();
     if (lane == 0) mbar_arrive(&s.csync);
-    bool r = wait_phase(&s.csync, sync_phase, &s.abort_flag, a.status, kStatusSync);
+    bool r = wait_phase(&s.csync, sync_phase, &s.abort_flag, a.status, kStatusSync, a.wait_limit);
     r = __all_sync(0xffffffffu, r);
     sync_phase ^= 1u;
     return r;
@@ -788,9 +800,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   float m_run = kNegInf, l_run = 0.f;       // simt: the lane's query
   float mq[NQT][2], lq[NQT][2];             // mma: queries 8n + 2tig + {0,1}
   bool poison = false;
+  int hold_stage = 0;
   StageHeader hd;
   do {
-    bool ok = wait_phase(&s.full[stage], phase, &s.abort_flag, a.status, kStatusFull);
+    bool ok = wait_phase(&s.full[stage], phase, &s.abort_flag, a.status, kStatusFull, a.wait_limit);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) {
       alive = false;
@@ -1040,9 +1053,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       }
     }
 
-    // release the stage to the producer
+    // release the stage to the producer (the CUDA-core consumer keeps a
+    // segment's last stage: its tiles hold the row-group merge, after which
+    // the stage is released)
     __syncwarp();
-    if (lane == 0) mbar_arrive(&s.empty[stage]);
+    if (!kMma && (hd.flags & kLast))
+      hold_stage = stage;
+    else if (lane == 0)
+      mbar_arrive(&s.empty[stage]);
     if (++stage == NSTAGE) {
       stage = 0;
       phase ^= 1u;
@@ -1061,12 +1079,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   const int xp = seg_par;
   seg_par ^= 1;
   if constexpr (!kMma) {
-    // ---- merge the row groups through shared atomics ----
+    // ---- merge the row groups in a fixed order ----
+    // The row groups of a warp are summed with shuffles; each warp leaves its
+    // [G][D] sum in the held stage's K (then V) tile, and every output adds
+    // the warps' sums in warp order, so the bits are the same on every run.
     if (owner) {
       rm[j][iq] = m_run;
       rl[j][iq] = poison ? kNaN : l_run;
     }
     if (!cons_sync()) break;
+    constexpr int kRegions = kPageTokens * static_cast<int>(sizeof(T)) / (4 * G);  // [G][D] sums per tile
+    static_assert(2 * kRegions >= NCW, "a stage's K and V tiles must hold every warp's sum");
+    auto region = [&](int w) -> float* {
+      return (w < kRegions) ? reinterpret_cast<float*>(s.k[hold_stage]) + w * G * D
+                            : reinterpret_cast<float*>(s.v[hold_stage]) + (w - kRegions) * G * D;
+    };
+    float* wsum = region(warp);
 #pragma unroll
     for (int i = 0; i < G; ++i) {
       float Mx = kNegInf;
@@ -1074,8 +1102,17 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       for (int g2 = 0; g2 < NG; ++g2) Mx = fmaxf(Mx, rm[g2][i]);
       const float Ms = (Mx == kNegInf) ? 0.f : Mx;
       const float f = exp2f(rm[j][i] - Ms);
+      float x[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) atomicAdd(&s.red_acc[i][LaneMap<T, D>::col(c, e)], acc[i][e] * f);
+      for (int e = 0; e < 8; ++e) x[e] = acc[i][e] * f;
+#pragma unroll
+      for (int o = GS; o < 32; o <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] += __shfl_xor_sync(0xffffffffu, x[e], o);
+      if (lane < GS) {
+        *reinterpret_cast<float4*>(wsum + i * D + LaneMap<T, D>::col(c, 0)) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(wsum + i * D + LaneMap<T, D>::col(c, 4)) = make_float4(x[4], x[5], x[6], x[7]);
+      }
       if (ct == i) {
         float L = 0.f;
 #pragma unroll
@@ -1090,11 +1127,21 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       const int i = e0 / D, d0 = e0 - i * D;
       const float L = s.fin_l[i];
       float val[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        val[e] = s.red_acc[i][d0 + e] / L;
-        s.red_acc[i][d0 + e] = 0.f;
+      {
+        const float4 a4 = *reinterpret_cast<const float4*>(region(0) + e0);
+        const float4 b4 = *reinterpret_cast<const float4*>(region(0) + e0 + 4);
+        val[0] = a4.x; val[1] = a4.y; val[2] = a4.z; val[3] = a4.w;
+        val[4] = b4.x; val[5] = b4.y; val[6] = b4.z; val[7] = b4.w;
       }
+#pragma unroll
+      for (int w = 1; w < NCW; ++w) {
+        const float4 a4 = *reinterpret_cast<const float4*>(region(w) + e0);
+        const float4 b4 = *reinterpret_cast<const float4*>(region(w) + e0 + 4);
+        val[0] += a4.x; val[1] += a4.y; val[2] += a4.z; val[3] += a4.w;
+        val[4] += b4.x; val[5] += b4.y; val[6] += b4.z; val[7] += b4.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) val[e] /= L;
       if (i >= hd.gq) continue;
       if (!split) {
         T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D;
@@ -1108,6 +1155,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               make_float4(s.fin_m[i], L, 0.f, 0.f);
       }
     }
+    // The held stage goes back to the producer, whose next copy into it is
+    // an async-proxy write after these generic ones.
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.empty[hold_stage]);
   } else {
     // ---- token-half 1 hands its O^T fragments to token-half 0 ----
     // l: each lane summed its two tokens; the column sums run over the 8
@@ -1287,7 +1339,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
                       static_cast<uint32_t>(nk - k_run) * rec_bytes, &s.comb);
         }
       }
-      bool ok = wait_phase(&s.comb, comb_phase, &s.abort_flag, a.status, kStatusCombine);
+      bool ok = wait_phase(&s.comb, comb_phase, &s.abort_flag, a.status, kStatusCombine, a.wait_limit);
       comb_phase ^= 1u;
       if (!__all_sync(0xffffffffu, ok)) return;
 #pragma unroll

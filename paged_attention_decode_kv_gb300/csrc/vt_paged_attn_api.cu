@@ -1,5 +1,12 @@
 // C-ABI front end of the paged decode library: argument validation, launch
-// plan, per-device split workspace, TMA descriptors, launch.
+// plan, the split scratch (library-owned, caller-owned or static), TMA
+// descriptors, launch, and the device status word.
+//
+// Every decode entry point goes through the same three steps, so they cannot
+// drift apart: validate() checks the arguments, make_plan() picks the kernel
+// variant and the grid, launch() encodes the tensor maps, fills the kernel
+// arguments and records the plan.  The entry points differ only in where the
+// split scratch comes from.
 //
 // Declarations and the contract of every entry point: include/vt_paged_attn.h.
 #include <cuda.h>
@@ -21,15 +28,19 @@ namespace {
 using vt::DecodeArgs;
 using vt::VariantInfo;
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0
 constexpr int kMaxGroupTile = 8;
 constexpr int kDefaultMinUnits = 2;
 constexpr int kDefaultSegCost = 2;  // a segment boundary weighs about two tiles of streaming
+constexpr size_t kStatusBytes = 256;
 
 thread_local int g_override_grid = 0;
 thread_local bool g_overlap = false;
 thread_local int g_override_min_units = 0;
 thread_local int g_seg_cost = -1;  // < 0: default
+thread_local long long g_test_wait_limit = 0;  // <= 0: kWaitLimitCycles
+thread_local int g_test_withhold_cta = -1;
+thread_local int g_test_withhold_tile = -1;
 thread_local vt_plan g_last_plan{};
 thread_local bool g_have_plan = false;
 thread_local std::string g_last_cuda_error;
@@ -57,11 +68,11 @@ const VariantInfo* find_variant(int head_dim, vt_dtype dtype, int group_tile) {
 }
 
 // Query rows computed per kv head and CTA.  bf16 runs on tensor cores with
-// the queries as the M dimension of m16n8k16: one tile of 8 (or 16) rows
+// the queries as the N dimension of m16n8k16: one tile of 8 (or 16) rows
 // covers any group up to that size.  fp32 runs on CUDA cores, where every
 // padded row costs FMAs: the next power of two, at most 8.
 int group_tile_for(int group, vt_dtype dtype) {
-  if (dtype == VT_BF16) return group <= 8 ? 8 : 16;
+  if (dtype != VT_F32) return group <= 8 ? 8 : 16;
   int g = 1;
   while (g < group && g < kMaxGroupTile) g <<= 1;
   return g;
@@ -69,9 +80,11 @@ int group_tile_for(int group, vt_dtype dtype) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout: [status word (256 B) | counter region | partial (m, l, 0, 0) | partial rows].
-// The counter region is reserved at allocation and never holds anything but
-// arrival counters, which every kernel leaves at zero; partials start after it.
+// Split scratch layout: [status words (256 B) | arrival counters | partial
+// records].  Arrival counters are zero between calls (every kernel leaves
+// them so; vt_paged_attn_device_status clears them after a give-up), so the
+// region that held counters must never receive partials: partials start
+// after the largest counter region the scratch has served.
 struct WsNeed {
   size_t counters_bytes;  // counters this call uses
   size_t part_bytes;      // partial records: per row (m, l, 0, 0), then the rows
@@ -85,7 +98,13 @@ WsNeed ws_need(int num_seqs, int nvh, int grid, int group_tile, int head_dim) {
   return n;
 }
 
-size_t ws_total(const WsNeed& n) { return 256 + align_up(n.counters_bytes, 256) + n.part_bytes; }
+size_t ws_total(const WsNeed& n) { return kStatusBytes + align_up(n.counters_bytes, 256) + n.part_bytes; }
+
+struct Scratch {
+  char* base = nullptr;
+  size_t bytes = 0;
+  size_t counters_cap = 0;  // bytes after the status words that hold zeroed counters
+};
 
 // ---------------------------------------------------------------------------
 // Per-device state
@@ -93,10 +112,9 @@ size_t ws_total(const WsNeed& n) { return 256 + align_up(n.counters_bytes, 256) 
 struct DeviceState {
   bool init = false;
   int num_sms = 0;
-  void* ws = nullptr;
-  size_t ws_bytes = 0;
-  size_t counters_cap = 0;  // bytes reserved for arrival counters (after the status word)
-  size_t partial_cap = 0;   // bytes for partials, starting at 256 + counters_cap
+  Scratch lib;               // library-owned (cudaMallocAsync, grows)
+  Scratch user;              // caller-owned (vt_paged_attn_set_workspace)
+  char* noalloc = nullptr;   // device address of the static array, once looked up
   std::vector<std::pair<const void*, int>> occupancy;
 };
 
@@ -139,19 +157,21 @@ vt_status prepare_variant(DeviceState& ds, const VariantInfo& v, int* ctas_per_s
   return VT_OK;
 }
 
-// Grows (never shrinks) the device's workspace.  A new buffer is zeroed on
-// `stream` before any kernel that uses it, so all counters start at 0.
-vt_status ensure_workspace(DeviceState& ds, const WsNeed& n, cudaStream_t stream) {
-  if (ds.ws && ds.counters_cap >= n.counters_bytes && ds.partial_cap >= n.part_bytes) return VT_OK;
-  size_t counters = ds.counters_cap > n.counters_bytes ? ds.counters_cap : n.counters_bytes;
+// Library-owned scratch: grows (never shrinks).  A new buffer's status words
+// and counter region are zeroed on `stream` before any kernel uses them.
+vt_status ensure_library_scratch(Scratch& w, const WsNeed& n, cudaStream_t stream) {
+  if (w.base && w.counters_cap >= n.counters_bytes &&
+      w.bytes - kStatusBytes - w.counters_cap >= n.part_bytes)
+    return VT_OK;
+  const size_t old_part = w.base ? w.bytes - kStatusBytes - w.counters_cap : 0;
+  size_t counters = w.counters_cap > n.counters_bytes ? w.counters_cap : n.counters_bytes;
   counters = align_up(counters + counters / 4 + 1024, 256);
-  size_t partial = ds.partial_cap > n.part_bytes ? ds.partial_cap : n.part_bytes;
+  size_t partial = old_part > n.part_bytes ? old_part : n.part_bytes;
   partial = align_up(partial + partial / 4, 1 << 16);
-  const size_t bytes = 256 + counters + partial;
-  if (ds.ws) {
-    cudaError_t e = cudaFreeAsync(ds.ws, stream);
-    ds.ws = nullptr;
-    ds.ws_bytes = ds.counters_cap = ds.partial_cap = 0;
+  const size_t bytes = kStatusBytes + counters + partial;
+  if (w.base) {
+    cudaError_t e = cudaFreeAsync(w.base, stream);
+    w = Scratch{};
     if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync");
   }
   void* p = nullptr;
@@ -161,15 +181,34 @@ vt_status ensure_workspace(DeviceState& ds, const WsNeed& n, cudaStream_t stream
     g_last_cuda_error = std::string("cudaMallocAsync: ") + cudaGetErrorString(e);
     return VT_ERR_OOM;
   }
-  e = cudaMemsetAsync(p, 0, 256 + counters, stream);
+  e = cudaMemsetAsync(p, 0, kStatusBytes + counters, stream);
   if (e != cudaSuccess) {
     cudaFreeAsync(p, stream);
     return cuda_fail(e, "cudaMemsetAsync");
   }
-  ds.ws = p;
-  ds.ws_bytes = bytes;
-  ds.counters_cap = counters;
-  ds.partial_cap = partial;
+  w.base = static_cast<char*>(p);
+  w.bytes = bytes;
+  w.counters_cap = counters;
+  return VT_OK;
+}
+
+// Caller-owned scratch of fixed size: the counter region grows in place (its
+// new part zeroed on `stream`, ahead of the kernel) as long as the buffer
+// holds it and the call's partials after it.
+vt_status fit_user_scratch(Scratch& w, const WsNeed& n, cudaStream_t stream) {
+  const size_t counters = align_up(n.counters_bytes, 256);
+  const size_t cap = counters > w.counters_cap ? counters : w.counters_cap;
+  const size_t total = kStatusBytes + cap + n.part_bytes;
+  if (total > w.bytes) {
+    g_last_cuda_error = "vt_paged_attn_decode: this call needs " + std::to_string(total) +
+                        " bytes of workspace; the caller's workspace holds " + std::to_string(w.bytes);
+    return VT_ERR_SCRATCH_LIMIT;
+  }
+  if (cap > w.counters_cap) {
+    cudaError_t e = cudaMemsetAsync(w.base + kStatusBytes + w.counters_cap, 0, cap - w.counters_cap, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    w.counters_cap = cap;
+  }
   return VT_OK;
 }
 
@@ -264,6 +303,174 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// ---------------------------------------------------------------------------
+// The shared call path
+// ---------------------------------------------------------------------------
+struct Call {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+  float scale;
+  int window;
+  cudaStream_t stream;
+  int max_blocks_per_seq, num_blocks;
+  vt_dtype dtype;
+};
+
+struct Plan {
+  const VariantInfo* v = nullptr;
+  int dev = 0, grid = 0, per_sm = 0, min_units = 0, num_sms = 0;
+  int group = 0, gt = 0, subgroups = 0;
+  long long nvh = 0;
+  WsNeed need{};
+};
+
+// Argument checks that need no device: every error returns before any
+// launch.  (num_seqs == 0 is handled by the caller as a no-op.)
+vt_status validate(const Call& c) {
+  if (c.num_seqs < 0) return VT_ERR_INVALID_ARG;
+  if (!c.out || !c.q || !c.k_cache || !c.v_cache || !c.block_tables || !c.context_lens) return VT_ERR_INVALID_ARG;
+  if (c.dtype != VT_BF16 && c.dtype != VT_F32) return VT_ERR_INVALID_ARG;
+  if (c.num_q_heads <= 0 || c.num_kv_heads <= 0 || c.num_q_heads % c.num_kv_heads != 0) return VT_ERR_INVALID_ARG;
+  if (c.max_blocks_per_seq <= 0 || c.num_blocks <= 0 || c.block_size <= 0 || c.head_dim <= 0)
+    return VT_ERR_INVALID_ARG;
+  if (!std::isfinite(c.scale)) return VT_ERR_INVALID_ARG;
+  if (!aligned(c.out, 16) || !aligned(c.q, 16) || !aligned(c.k_cache, 16) || !aligned(c.v_cache, 16) ||
+      !aligned(c.block_tables, 4) || !aligned(c.context_lens, 4))
+    return VT_ERR_INVALID_ARG;
+  if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256) return VT_ERR_UNSUPPORTED;
+  if (c.block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c.num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c.max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
+  return VT_OK;
+}
+
+// Variant, grid and scratch need of a validated call on the current device.
+// Caller holds g_mutex.
+vt_status make_plan(const Call& c, Plan* p) {
+  p->group = c.num_q_heads / c.num_kv_heads;
+  p->gt = group_tile_for(p->group, c.dtype);
+  p->subgroups = (p->group + p->gt - 1) / p->gt;
+  p->nvh = static_cast<long long>(c.num_kv_heads) * p->subgroups;
+  if (p->nvh * c.num_seqs > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
+  p->v = find_variant(c.head_dim, c.dtype, p->gt);
+  if (!p->v) return VT_ERR_UNSUPPORTED;
+  cudaError_t e = cudaGetDevice(&p->dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceState& ds = device_state(p->dev);
+  vt_status st = prepare_device(p->dev, ds);
+  if (st != VT_OK) return st;
+  st = prepare_variant(ds, *p->v, &p->per_sm);
+  if (st != VT_OK) return st;
+  p->num_sms = ds.num_sms;
+  p->grid = g_override_grid > 0 ? g_override_grid : ds.num_sms * p->per_sm;
+  p->min_units = g_override_min_units > 0 ? g_override_min_units : kDefaultMinUnits;
+  p->need = ws_need(c.num_seqs, static_cast<int>(p->nvh), p->grid, p->gt, c.head_dim);
+  return VT_OK;
+}
+
+// Encodes the tensor maps, fills the kernel arguments from the plan and the
+// chosen scratch (status words at `base`, counters after them, partials at
+// `base + 256 + counters_region`), launches, and records the plan.
+vt_status launch(const Call& c, const Plan& p, char* base, size_t counters_region, size_t scratch_used,
+                 int scratch_source) {
+  CUtensorMap tk, tv;
+  vt_status st = tensor_map(MapKey{c.k_cache, c.head_dim, c.num_kv_heads, c.num_blocks, c.dtype, p.dev}, &tk);
+  if (st != VT_OK) return st;
+  st = tensor_map(MapKey{c.v_cache, c.head_dim, c.num_kv_heads, c.num_blocks, c.dtype, p.dev}, &tv);
+  if (st != VT_OK) return st;
+
+  DecodeArgs args{};
+  args.status = reinterpret_cast<unsigned*>(base);
+  args.counters = reinterpret_cast<int*>(base + kStatusBytes);
+  args.part = reinterpret_cast<float*>(base + kStatusBytes + counters_region);
+  args.out = c.out;
+  args.q = c.q;
+  args.block_tables = c.block_tables;
+  args.context_lens = c.context_lens;
+  args.num_seqs = c.num_seqs;
+  args.num_q_heads = c.num_q_heads;
+  args.num_kv_heads = c.num_kv_heads;
+  args.group = p.group;
+  args.subgroups = p.subgroups;
+  args.max_blocks = c.max_blocks_per_seq;
+  args.num_blocks = c.num_blocks;
+  args.window = c.window > 0 ? c.window : 0;
+  args.scale_log2 = c.scale * 1.4426950408889634f;
+  args.min_units = p.min_units;
+  args.seg_cost = g_seg_cost < 0 ? kDefaultSegCost : g_seg_cost;
+  args.wait_limit = g_test_wait_limit > 0 ? g_test_wait_limit : vt::kWaitLimitCycles;
+  args.withhold_cta = g_test_withhold_tile >= 0 ? g_test_withhold_cta : -1;
+  args.withhold_tile = g_test_withhold_tile;
+
+  cudaError_t e = p.v->launch(tk, tv, args, p.grid, c.stream, g_overlap);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+
+  vt_plan& r = g_last_plan;
+  r.grid_ctas = p.grid;
+  r.ctas_per_sm = p.per_sm;
+  r.num_sms = p.num_sms;
+  r.consumer_warps = p.v->consumer_warps;
+  r.tensor_cores = p.v->tensor_cores;
+  r.stages = p.v->stages;
+  r.group_tile = p.gt;
+  r.subgroups = p.subgroups;
+  r.min_units_per_cta = p.min_units;
+  r.head_dim = c.head_dim;
+  r.dtype = c.dtype;
+  r.smem_bytes = p.v->smem_bytes;
+  r.workspace_bytes = scratch_used;
+  r.launch_overlap = g_overlap ? 1 : 0;
+  r.segment_cost = args.seg_cost;
+  r.scratch_source = scratch_source;
+  g_have_plan = true;
+  return VT_OK;
+}
+
+Call make_call(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+               const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+               int block_size, float scale, int window, vt_stream_t stream, int max_blocks_per_seq,
+               int num_blocks, vt_dtype dtype) {
+  return Call{out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+              head_dim, block_size, scale, window, reinterpret_cast<cudaStream_t>(stream), max_blocks_per_seq,
+              num_blocks, dtype};
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the split scratch is a fixed, file-scope device
+// array instead of the library's lazily allocated per-device workspace.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = VT_NOALLOC_SCRATCH_BYTES;  // held on every device that loads the library
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// In host code the array's name is only a host-side stand-in: its device
+// address must be looked up, once per device, with that device current.
+// Caller holds g_mutex.
+vt_status noalloc_scratch(DeviceState& ds, char** ptr) {
+  if (!ds.noalloc) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    ds.noalloc = static_cast<char*>(p);
+  }
+  *ptr = ds.noalloc;
+  return VT_OK;
+}
+
+// The status areas a kernel on this device may have written, library-owned
+// scratch first.  Caller holds g_mutex.
+std::vector<std::pair<char*, size_t>> status_areas(DeviceState& ds) {
+  std::vector<std::pair<char*, size_t>> areas;  // (base, bytes to clear on a give-up)
+  if (ds.lib.base) areas.emplace_back(ds.lib.base, kStatusBytes + ds.lib.counters_cap);
+  if (ds.user.base) areas.emplace_back(ds.user.base, kStatusBytes + ds.user.counters_cap);
+  if (ds.noalloc) areas.emplace_back(ds.noalloc, kStatusBytes);  // its calls clear their counters themselves
+  return areas;
+}
+
 }  // namespace
 
 extern "C" {
@@ -276,7 +483,7 @@ const char* vt_status_string(vt_status s) {
     case VT_ERR_CUDA: return "CUDA error";
     case VT_ERR_OOM: return "out of device memory";
     case VT_ERR_DEVICE_TIMEOUT: return "device wait timed out";
-    case VT_ERR_SCRATCH_LIMIT: return "call needs more scratch than the static buffer holds";
+    case VT_ERR_SCRATCH_LIMIT: return "call needs more scratch than the fixed buffer (static or caller's) holds";
   }
   return "unknown status";
 }
@@ -301,6 +508,14 @@ vt_status vt_paged_attn_set_overlap(int enabled) {
 vt_status vt_paged_attn_set_segment_cost(int tiles) {
   if (tiles > 64) return VT_ERR_INVALID_ARG;
   g_seg_cost = tiles;
+  return VT_OK;
+}
+
+vt_status vt_paged_attn_set_test_wait(long long wait_limit_cycles, int withhold_cta, int withhold_tile) {
+  if (withhold_tile >= 0 && withhold_cta < 0) return VT_ERR_INVALID_ARG;
+  g_test_wait_limit = wait_limit_cycles > 0 ? wait_limit_cycles : 0;
+  g_test_withhold_cta = withhold_tile >= 0 ? withhold_cta : -1;
+  g_test_withhold_tile = withhold_tile >= 0 ? withhold_tile : -1;
   return VT_OK;
 }
 
@@ -330,247 +545,89 @@ size_t vt_paged_attn_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_h
   return ws_total(ws_need(num_seqs, nvh, grid, gt, head_dim));
 }
 
-vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
-                               int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
-                               int window, vt_stream_t stream_handle, int max_blocks_per_seq, int num_blocks,
-                               vt_dtype dtype) {
-  if (num_seqs < 0) return VT_ERR_INVALID_ARG;
-  if (num_seqs == 0) return VT_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return VT_ERR_INVALID_ARG;
-  if (dtype != VT_BF16 && dtype != VT_F32) return VT_ERR_INVALID_ARG;
-  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return VT_ERR_INVALID_ARG;
-  if (max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0 || head_dim <= 0) return VT_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return VT_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4))
-    return VT_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return VT_ERR_UNSUPPORTED;
-  if (block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
-  if (static_cast<long long>(num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
-  if (static_cast<long long>(max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
-
-  const int group = num_q_heads / num_kv_heads;
-  const int gt = group_tile_for(group, dtype);
-  const int subgroups = (group + gt - 1) / gt;
-  const long long nvh = static_cast<long long>(num_kv_heads) * subgroups;
-  if (nvh * num_seqs > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
-  const VariantInfo* v = find_variant(head_dim, dtype, gt);
-  if (!v) return VT_ERR_UNSUPPORTED;
-
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+vt_status vt_paged_attn_set_workspace(void* dev_ptr, size_t bytes, vt_stream_t stream_handle) {
+  if (dev_ptr && (!aligned(dev_ptr, 256) || bytes < VT_MIN_WORKSPACE_BYTES)) return VT_ERR_INVALID_ARG;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& ds = device_state(dev);
+  if (!dev_ptr) {
+    ds.user = Scratch{};
+    return VT_OK;
+  }
+  e = cudaMemsetAsync(dev_ptr, 0, kStatusBytes, reinterpret_cast<cudaStream_t>(stream_handle));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  ds.user = Scratch{static_cast<char*>(dev_ptr), bytes, 0};
+  return VT_OK;
+}
 
-  DecodeArgs args{};
-  int grid = 0, per_sm = 0, min_units = 0;
-  size_t ws_used = 0;
+vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                               int window, vt_stream_t stream, int max_blocks_per_seq, int num_blocks,
+                               vt_dtype dtype) {
+  const Call c = make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                           num_kv_heads, head_dim, block_size, scale, window, stream, max_blocks_per_seq,
+                           num_blocks, dtype);
+  if (num_seqs == 0) return VT_OK;
+  vt_status st = validate(c);
+  if (st != VT_OK) return st;
+  Plan p;
+  Scratch w;
+  int source = 0;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceState& ds = device_state(dev);
-    vt_status st = prepare_device(dev, ds);
+    st = make_plan(c, &p);
     if (st != VT_OK) return st;
-    st = prepare_variant(ds, *v, &per_sm);
+    DeviceState& ds = device_state(p.dev);
+    if (ds.user.base) {
+      st = fit_user_scratch(ds.user, p.need, c.stream);
+      w = ds.user;
+      source = 1;
+    } else {
+      st = ensure_library_scratch(ds.lib, p.need, c.stream);
+      w = ds.lib;
+    }
     if (st != VT_OK) return st;
-    grid = g_override_grid > 0 ? g_override_grid : ds.num_sms * per_sm;
-    min_units = g_override_min_units > 0 ? g_override_min_units : kDefaultMinUnits;
-    const WsNeed need = ws_need(num_seqs, static_cast<int>(nvh), grid, gt, head_dim);
-    st = ensure_workspace(ds, need, stream);
-    if (st != VT_OK) return st;
-    ws_used = ws_total(need);
-    char* base = static_cast<char*>(ds.ws);
-    args.status = reinterpret_cast<unsigned*>(base);
-    args.counters = reinterpret_cast<int*>(base + 256);
-    args.part = reinterpret_cast<float*>(base + 256 + ds.counters_cap);
-    g_last_plan.num_sms = ds.num_sms;
   }
-
-  CUtensorMap tk, tv;
-  vt_status st = tensor_map(MapKey{k_cache, head_dim, num_kv_heads, num_blocks, dtype, dev}, &tk);
-  if (st != VT_OK) return st;
-  st = tensor_map(MapKey{v_cache, head_dim, num_kv_heads, num_blocks, dtype, dev}, &tv);
-  if (st != VT_OK) return st;
-
-  args.out = out;
-  args.q = q;
-  args.block_tables = block_tables;
-  args.context_lens = context_lens;
-  args.num_seqs = num_seqs;
-  args.num_q_heads = num_q_heads;
-  args.num_kv_heads = num_kv_heads;
-  args.group = group;
-  args.subgroups = subgroups;
-  args.max_blocks = max_blocks_per_seq;
-  args.num_blocks = num_blocks;
-  args.window = window > 0 ? window : 0;
-  args.scale_log2 = scale * 1.4426950408889634f;
-  args.min_units = min_units;
-  args.seg_cost = g_seg_cost < 0 ? kDefaultSegCost : g_seg_cost;
-
-  e = v->launch(tk, tv, args, grid, stream, g_overlap);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  g_last_plan.launch_overlap = g_overlap ? 1 : 0;
-  g_last_plan.segment_cost = args.seg_cost;
-
-  g_last_plan.grid_ctas = grid;
-  g_last_plan.ctas_per_sm = per_sm;
-  g_last_plan.consumer_warps = v->consumer_warps;
-  g_last_plan.tensor_cores = v->tensor_cores;
-  g_last_plan.stages = v->stages;
-  g_last_plan.group_tile = gt;
-  g_last_plan.subgroups = subgroups;
-  g_last_plan.min_units_per_cta = min_units;
-  g_last_plan.head_dim = head_dim;
-  g_last_plan.dtype = dtype;
-  g_last_plan.smem_bytes = v->smem_bytes;
-  g_last_plan.workspace_bytes = ws_used;
-  g_have_plan = true;
-  return VT_OK;
+  const size_t used = kStatusBytes + w.counters_cap + p.need.part_bytes;
+  return launch(c, p, w.base, w.counters_cap, used, source);
 }
-
-}  // extern "C"
-
-// ---------------------------------------------------------------------------
-// Allocation-free variant: the split scratch is a fixed, file-scope device
-// array instead of the library's lazily allocated per-device workspace.
-// ---------------------------------------------------------------------------
-namespace {
-
-constexpr size_t kNoAllocScratchBytes = VT_NOALLOC_SCRATCH_BYTES;  // held on every device that loads the library
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-std::mutex g_noalloc_mutex;
-std::vector<void*> g_noalloc_ptr;  // device address of the array, per device
-
-// In host code the array's name is only a host-side stand-in: its device
-// address must be looked up, once per device, with that device current.
-vt_status noalloc_scratch(int dev, void** ptr) {
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (static_cast<int>(g_noalloc_ptr.size()) <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
-    g_noalloc_ptr[dev] = p;
-  }
-  *ptr = g_noalloc_ptr[dev];
-  return VT_OK;
-}
-
-}  // namespace
-
-extern "C" {
 
 vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                       float scale, int window, vt_stream_t stream_handle, int max_blocks_per_seq,
+                                       float scale, int window, vt_stream_t stream, int max_blocks_per_seq,
                                        int num_blocks, vt_dtype dtype) {
-  if (num_seqs < 0) return VT_ERR_INVALID_ARG;
+  const Call c = make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                           num_kv_heads, head_dim, block_size, scale, window, stream, max_blocks_per_seq,
+                           num_blocks, dtype);
   if (num_seqs == 0) return VT_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return VT_ERR_INVALID_ARG;
-  if (dtype != VT_BF16 && dtype != VT_F32) return VT_ERR_INVALID_ARG;
-  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return VT_ERR_INVALID_ARG;
-  if (max_blocks_per_seq <= 0 || num_blocks <= 0 || block_size <= 0 || head_dim <= 0) return VT_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return VT_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4))
-    return VT_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return VT_ERR_UNSUPPORTED;
-  if (block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
-  if (static_cast<long long>(num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
-  if (static_cast<long long>(max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
-
-  const int group = num_q_heads / num_kv_heads;
-  const int gt = group_tile_for(group, dtype);
-  const int subgroups = (group + gt - 1) / gt;
-  const long long nvh = static_cast<long long>(num_kv_heads) * subgroups;
-  if (nvh * num_seqs > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
-  const VariantInfo* v = find_variant(head_dim, dtype, gt);
-  if (!v) return VT_ERR_UNSUPPORTED;
-
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-
-  int grid = 0, per_sm = 0, min_units = 0, num_sms = 0;
+  vt_status st = validate(c);
+  if (st != VT_OK) return st;
+  Plan p;
+  char* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceState& ds = device_state(dev);
-    vt_status st = prepare_device(dev, ds);
+    st = make_plan(c, &p);
     if (st != VT_OK) return st;
-    st = prepare_variant(ds, *v, &per_sm);
+    const size_t total = ws_total(p.need);
+    if (total > kNoAllocScratchBytes) {
+      g_last_cuda_error = "vt_paged_attn_decode_noalloc: this call needs " + std::to_string(total) +
+                          " bytes of scratch; the static buffer holds " + std::to_string(kNoAllocScratchBytes);
+      return VT_ERR_SCRATCH_LIMIT;
+    }
+    st = noalloc_scratch(device_state(p.dev), &base);
     if (st != VT_OK) return st;
-    grid = g_override_grid > 0 ? g_override_grid : ds.num_sms * per_sm;
-    min_units = g_override_min_units > 0 ? g_override_min_units : kDefaultMinUnits;
-    num_sms = ds.num_sms;
   }
-  // Layout inside the fixed array: [status 256 B | counters | partial records].
-  const WsNeed need = ws_need(num_seqs, static_cast<int>(nvh), grid, gt, head_dim);
-  const size_t counters_region = align_up(need.counters_bytes, 256);
-  const size_t total = 256 + counters_region + need.part_bytes;
-  if (total > kNoAllocScratchBytes) {
-    g_last_cuda_error = "vt_paged_attn_decode_noalloc: this call needs " + std::to_string(total) +
-                        " bytes of scratch; the static buffer holds " + std::to_string(kNoAllocScratchBytes);
-    return VT_ERR_SCRATCH_LIMIT;
-  }
-  void* base_ptr = nullptr;
-  vt_status st = noalloc_scratch(dev, &base_ptr);
-  if (st != VT_OK) return st;
-  char* base = static_cast<char*>(base_ptr);
-  // The array keeps the previous call's contents: the status word and the
+  // The array keeps the previous call's contents (partials of any earlier
+  // call may sit where this call's counters go): the status words and the
   // arrival counters must start at zero.
-  e = cudaMemsetAsync(base, 0, 256 + counters_region, stream);
+  const size_t counters_region = align_up(p.need.counters_bytes, 256);
+  cudaError_t e = cudaMemsetAsync(base, 0, kStatusBytes + counters_region, c.stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
-
-  CUtensorMap tk, tv;
-  st = tensor_map(MapKey{k_cache, head_dim, num_kv_heads, num_blocks, dtype, dev}, &tk);
-  if (st != VT_OK) return st;
-  st = tensor_map(MapKey{v_cache, head_dim, num_kv_heads, num_blocks, dtype, dev}, &tv);
-  if (st != VT_OK) return st;
-
-  DecodeArgs args{};
-  args.status = reinterpret_cast<unsigned*>(base);
-  args.counters = reinterpret_cast<int*>(base + 256);
-  args.part = reinterpret_cast<float*>(base + 256 + counters_region);
-  args.out = out;
-  args.q = q;
-  args.block_tables = block_tables;
-  args.context_lens = context_lens;
-  args.num_seqs = num_seqs;
-  args.num_q_heads = num_q_heads;
-  args.num_kv_heads = num_kv_heads;
-  args.group = group;
-  args.subgroups = subgroups;
-  args.max_blocks = max_blocks_per_seq;
-  args.num_blocks = num_blocks;
-  args.window = window > 0 ? window : 0;
-  args.scale_log2 = scale * 1.4426950408889634f;
-  args.min_units = min_units;
-  args.seg_cost = g_seg_cost < 0 ? kDefaultSegCost : g_seg_cost;
-
-  e = v->launch(tk, tv, args, grid, stream, g_overlap);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  g_last_plan.launch_overlap = g_overlap ? 1 : 0;
-  g_last_plan.segment_cost = args.seg_cost;
-
-  g_last_plan.num_sms = num_sms;
-  g_last_plan.grid_ctas = grid;
-  g_last_plan.ctas_per_sm = per_sm;
-  g_last_plan.consumer_warps = v->consumer_warps;
-  g_last_plan.tensor_cores = v->tensor_cores;
-  g_last_plan.stages = v->stages;
-  g_last_plan.group_tile = gt;
-  g_last_plan.subgroups = subgroups;
-  g_last_plan.min_units_per_cta = min_units;
-  g_last_plan.head_dim = head_dim;
-  g_last_plan.dtype = dtype;
-  g_last_plan.smem_bytes = v->smem_bytes;
-  g_last_plan.workspace_bytes = total;
-  g_have_plan = true;
-  return VT_OK;
+  return launch(c, p, base, counters_region, ws_total(p.need), 2);
 }
 
 vt_status vt_paged_attn_device_status(vt_stream_t stream_handle, unsigned* status) {
@@ -583,17 +640,20 @@ vt_status vt_paged_attn_device_status(vt_stream_t stream_handle, unsigned* statu
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   std::lock_guard<std::mutex> lock(g_mutex);
-  DeviceState& ds = device_state(dev);
-  if (!ds.ws) return VT_OK;
-  unsigned word = 0;
-  e = cudaMemcpy(&word, ds.ws, sizeof(word), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
-  *status = word;
-  if (word == 0) return VT_OK;
-  // A kernel gave up: clear the word and every arrival counter it may have left behind.
-  e = cudaMemset(ds.ws, 0, 256 + ds.counters_cap);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
-  return VT_ERR_DEVICE_TIMEOUT;
+  unsigned all = 0;
+  for (const auto& area : status_areas(device_state(dev))) {
+    unsigned word = 0;
+    e = cudaMemcpy(&word, area.first, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+    if (word == 0) continue;
+    all |= word;
+    // A kernel gave up: clear its status words and every arrival counter it
+    // may have left behind.
+    e = cudaMemset(area.first, 0, area.second);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  }
+  *status = all;
+  return all ? VT_ERR_DEVICE_TIMEOUT : VT_OK;
 }
 
 vt_status vt_paged_attn_device_status_detail(vt_stream_t stream_handle, unsigned* words, int n_words) {
@@ -605,11 +665,17 @@ vt_status vt_paged_attn_device_status_detail(vt_stream_t stream_handle, unsigned
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (n_words == 0) return VT_OK;
   std::lock_guard<std::mutex> lock(g_mutex);
-  DeviceState& ds = device_state(dev);
-  if (!ds.ws || n_words == 0) return VT_OK;
-  e = cudaMemcpy(words, ds.ws, sizeof(unsigned) * n_words, cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+  // the first area whose status word is set (else all zeros)
+  for (const auto& area : status_areas(device_state(dev))) {
+    unsigned buf[8] = {0};
+    e = cudaMemcpy(buf, area.first, sizeof(unsigned) * n_words, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+    if (buf[0] == 0) continue;
+    for (int k = 0; k < n_words; ++k) words[k] = buf[k];
+    break;
+  }
   return VT_OK;
 }
 
@@ -619,11 +685,10 @@ void vt_paged_attn_release(void) {
   cudaGetDevice(&cur);
   for (size_t d = 0; d < g_devices.size(); ++d) {
     DeviceState& ds = g_devices[d];
-    if (ds.ws) {
+    if (ds.lib.base) {
       cudaSetDevice(static_cast<int>(d));
-      cudaFree(ds.ws);
-      ds.ws = nullptr;
-      ds.ws_bytes = ds.counters_cap = ds.partial_cap = 0;
+      cudaFree(ds.lib.base);
+      ds.lib = Scratch{};
     }
   }
   cudaSetDevice(cur);

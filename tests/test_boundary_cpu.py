@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert vt.vt_paged_attn_version() == 10000
+    assert vt.vt_paged_attn_version() == 10100
     assert vt.vt_status_string(vt.VT_OK) == "ok"
     assert "unsupported" in vt.vt_status_string(vt.VT_ERR_UNSUPPORTED)
     assert vt.vt_status_string(99) == "unknown status"
@@ -111,3 +111,22 @@ def test_workspace_bytes_rejects_bad_shapes(lib):
     assert vt.vt_paged_attn_workspace_bytes(0, 16, 8, 128, vt.VT_BF16) == 0
     assert vt.vt_paged_attn_workspace_bytes(4, 12, 8, 128, vt.VT_BF16) == 0
     assert vt.vt_paged_attn_workspace_bytes(4, 16, 8, 96, vt.VT_BF16) == 0
+
+
+def test_workspace_and_test_wait_validation(lib):
+    """Arguments of the caller-owned workspace and of the wait test hook are
+    checked on the host before CUDA is touched."""
+    c_void = ctypes.c_void_p
+    assert lib.vt_paged_attn_set_workspace(c_void(0x1000 + 16), 1 << 20, None) == vt.VT_ERR_INVALID_ARG
+    assert lib.vt_paged_attn_set_workspace(c_void(0x1000), vt.VT_MIN_WORKSPACE_BYTES - 1, None) == \
+        vt.VT_ERR_INVALID_ARG
+    assert lib.vt_paged_attn_set_test_wait(1000, -1, 3) == vt.VT_ERR_INVALID_ARG
+    assert lib.vt_paged_attn_set_test_wait(1000, 0, 3) == vt.VT_OK
+    assert lib.vt_paged_attn_set_test_wait(0, -1, -1) == vt.VT_OK
+
+
+def test_header_constants_match_binding():
+    text = HEADER.read_text()
+    assert re.search(r"#define VT_NOALLOC_SCRATCH_BYTES \(8u << 20\)", text)
+    assert vt.VT_NOALLOC_SCRATCH_BYTES == 8 << 20
+    assert re.search(r"#define VT_MIN_WORKSPACE_BYTES 4096u", text) and vt.VT_MIN_WORKSPACE_BYTES == 4096

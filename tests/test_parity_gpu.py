@@ -41,6 +41,8 @@ def _reset_override():
         vt.vt_paged_attn_set_override(0, 0)
         vt.vt_paged_attn_set_overlap(False)
         vt.vt_paged_attn_set_segment_cost(-1)
+        vt.vt_paged_attn_set_test_wait(0, -1, -1)
+        vt.vt_paged_attn_set_workspace(0, 0)
 
 
 def gpu_run(case, dev, grid=0, min_units=0, window=None, tables=None, lens=None, stream=None):
@@ -208,11 +210,18 @@ def test_invalid_device_data_poisons_only_its_rows(dev):
     assert torch.isnan(out[0].float()).all()
 
 
-def test_deterministic_bits(dev):
-    case = W.make_case(W.QWEN3_1P7B, 12)
-    a, _ = gpu_run(case, dev, grid=40, min_units=1)
-    b, _ = gpu_run(case, dev, grid=40, min_units=1)
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+@pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_F32, W.D64_GQA4_F32,
+                               W.custom("f32_d128_g8", [1, 33, 700, 2000], 64, 8, 128, dtype="f32")],
+                         ids=lambda w: w.name)
+def test_deterministic_bits(dev, w):
+    """Same inputs and plan, same bits: bf16 and fp32 storage (the fp32 row
+    groups merge in a fixed order), several grids, repeated calls."""
+    case = W.make_case(w, 12)
+    for grid in (0, 40, 301):
+        a, _ = gpu_run(case, dev, grid=grid, min_units=1 if grid else 0)
+        for _ in range(3):
+            b, _ = gpu_run(case, dev, grid=grid, min_units=1 if grid else 0)
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), grid
 
 
 def test_default_plan(dev):
@@ -317,8 +326,7 @@ def test_overlap_back_to_back(dev):
         for r in range(3):
             got = outs[(r, j)].cpu()
             compare(got[idx[:, 0], idx[:, 1]].double().numpy(), ref, case.q.dtype, f"{case.workload.name} rep {r}")
-        if case.q.dtype == torch.bfloat16:  # the fp32 path merges row groups with shared atomics
-            assert torch.equal(outs[(0, j)].cpu().view(torch.uint8), outs[(2, j)].cpu().view(torch.uint8))
+        assert torch.equal(outs[(0, j)].cpu().view(torch.uint8), outs[(2, j)].cpu().view(torch.uint8))
     idx, ref = oracle_rows(other)
     compare(shared.cpu()[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16, "overwritten buffer")
 
@@ -360,3 +368,103 @@ def test_overlap_in_cuda_graph(dev):
 
 def test_device_status_clean(dev):
     assert vt.vt_paged_attn_device_status() == 0
+
+
+def test_caller_workspace(dev):
+    """vt_paged_attn_set_workspace: decodes on a caller-owned workspace give the
+    oracle's results (split and unsplit, shapes growing and shrinking, so the
+    counter region grows in place), report it in the plan, refuse a call the
+    buffer cannot hold, and the library's own workspace takes over again
+    after the buffer is withdrawn."""
+    cases = [W.make_case(W.QWEN3_1P7B, 23), W.make_case(W.custom("ws_many", [3] * 700, 8, 8, 128), 23),
+             W.make_case(W.D256_GQA4_F32_W1024, 23), W.make_case(W.QWEN3_1P7B, 24)]
+    # the counter region only grows, so a buffer for calls of several shapes
+    # holds the largest counter region plus the largest partials: the sum of
+    # the calls' needs is more than enough
+    need = sum(vt.vt_paged_attn_workspace_bytes(c.workload.num_seqs, c.workload.num_q_heads,
+                                                 c.workload.num_kv_heads, c.workload.head_dim,
+                                                 vt.VT_BF16 if c.q.dtype == torch.bfloat16 else vt.VT_F32)
+               for c in cases)
+    buf = torch.full((need,), 0x5A, dtype=torch.uint8, device=dev)  # dirty on purpose
+    vt.vt_paged_attn_set_workspace(buf.data_ptr(), buf.numel())
+    try:
+        for case in cases:
+            for grid in (0, 77):
+                (_, _), plan = check_case(case, dev, grid=grid, min_units=1 if grid else 0)
+                assert plan["scratch_source"] == 1 and plan["workspace_bytes"] <= buf.numel()
+        small = torch.empty(vt.VT_MIN_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+        vt.vt_paged_attn_set_workspace(small.data_ptr(), small.numel())
+        case = cases[0]
+        k, v = case.pool(dev)
+        with pytest.raises(vt.VtError) as err:
+            vt.decode(case.q.to(dev), k, v, case.block_tables.to(dev), case.context_lens.to(dev))
+        assert err.value.status == vt.VT_ERR_SCRATCH_LIMIT
+        torch.cuda.synchronize()
+    finally:
+        vt.vt_paged_attn_set_workspace(0, 0)
+    (_, _), plan = check_case(cases[0], dev)
+    assert plan["scratch_source"] == 0
+
+
+def _give_up(case, dev, entry):
+    """One call whose CTA 0 withholds its second tile under a short wait limit
+    (about 2 ms): returns the status word, the detail words and the output."""
+    w = case.workload
+    k, v = case.pool(dev)
+    q, bt, cl = case.q.to(dev), case.block_tables.to(dev), case.context_lens.to(dev)
+    out = torch.zeros_like(q)
+    vt.vt_paged_attn_set_override(1, 1)  # one CTA holds every tile
+    vt.vt_paged_attn_set_test_wait(1 << 22, 0, 1)
+    try:
+        B, Hq, D = q.shape
+        st = entry(out.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), bt.data_ptr(), cl.data_ptr(), B, Hq,
+                   w.num_kv_heads, D, 32, w.scale, w.window, torch.cuda.current_stream().cuda_stream,
+                   bt.shape[1], case.num_blocks, vt.dtype_code(q))
+        assert st == vt.VT_OK
+    finally:
+        vt.vt_paged_attn_set_test_wait(0, -1, -1)
+        vt.vt_paged_attn_set_override(0, 0)
+    torch.cuda.synchronize()
+    detail = vt.vt_paged_attn_device_status_detail(n_words=5)
+    status = vt.vt_paged_attn_device_status()
+    return status, detail, out
+
+
+@pytest.mark.parametrize("path", ["library", "caller_workspace", "noalloc"])
+def test_bounded_wait_gives_up_and_reports(dev, path):
+    """The failure path of a bounded wait, made to happen without any fault:
+    a test hook shortens the wait limit and has CTA 0 withhold a tile.  The
+    consumers' wait for it runs out, the kernel returns, the status reads
+    back as a timeout of the page-tile wait (bit 0) with CTA 0 and a consumer
+    thread recorded, on each scratch path; reading it clears it, and the next
+    normal call is exact against the oracle."""
+    case = W.make_case(W.custom("giveup", [100, 700], 16, 4, 128), 25)
+    entry = vt.vt_paged_attn_decode_noalloc if path == "noalloc" else vt.vt_paged_attn_decode
+    buf = None
+    if path == "caller_workspace":
+        buf = torch.empty(8 << 20, dtype=torch.uint8, device=dev)
+        vt.vt_paged_attn_set_workspace(buf.data_ptr(), buf.numel())
+    try:
+        status, detail, _ = _give_up(case, dev, entry)
+        assert status & 1, f"status {status:#x}"
+        assert detail[0] & 1 and detail[1] == 1, detail   # CTA 0 gave up first
+        assert detail[2] & 0xFF == 1 and (detail[2] >> 8) < 128, detail  # a consumer thread's tile wait
+        assert vt.vt_paged_attn_device_status() == 0     # reading cleared it
+        # the same path, normal operation again: exact against the oracle
+        k, v = case.pool(dev)
+        q, bt, cl = case.q.to(dev), case.block_tables.to(dev), case.context_lens.to(dev)
+        out = torch.full_like(q, float("nan"))
+        for grid in (0, 3):
+            vt.vt_paged_attn_set_override(grid, 1 if grid else 0)
+            st = entry(out.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), bt.data_ptr(), cl.data_ptr(), 2,
+                       16, 4, 128, 32, case.workload.scale, 0, torch.cuda.current_stream().cuda_stream,
+                       bt.shape[1], case.num_blocks, vt.VT_BF16)
+            assert st == vt.VT_OK
+            torch.cuda.synchronize()
+            assert vt.vt_paged_attn_device_status() == 0
+            idx, ref = oracle_rows(case)
+            compare(out.cpu()[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16, f"{path} grid {grid}")
+    finally:
+        vt.vt_paged_attn_set_override(0, 0)
+        if buf is not None:
+            vt.vt_paged_attn_set_workspace(0, 0)
