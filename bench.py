@@ -42,7 +42,8 @@ UNIT = "µs/call"
 DEFAULT_WORKLOAD = "skewed_b128_gqa4_d128"
 SWEEP = ["batch1_ctx32768_gqa4_d128", "large_gqa8_b64_d128", "d256_gqa4_b16", "d256_gqa4_b16_w1024",
          "d256_gqa4_b16_f32", "d256_gqa4_b16_f32_w1024", "qwen3_1p7b_b8_gqa2_d128", "d64_gqa4_b32",
-         "d64_gqa4_b32_f32"]
+         "d64_gqa4_b32_f32", "skewed_b128_gqa4_d128_fp8", "batch1_ctx32768_gqa4_d128_fp8",
+         "large_gqa8_b64_d128_fp8", "d256_gqa4_b16_fp8"]
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "vt_paged_attn_api.cu"]  # shared by every variant
 
@@ -60,6 +61,8 @@ def variant_source(workload: str) -> str:
     """The translation unit holding the kernel variants a workload runs on."""
     from paged_attention_decode_kv_gb300 import workloads as W
     w = W.WORKLOADS[workload]
+    if w.dtype == "e4m3":
+        return "decode_e4m3.cu"
     return "decode_d64.cu" if w.head_dim == 64 else f"decode_d{w.head_dim}_{w.dtype}.cu"
 
 
@@ -181,8 +184,20 @@ def make_device_case(name: str, seed: int, device, pool_blocks: int = 0):
     k, v = case.pool(device)
     n_copies = max(2, -(-ROTATE_BYTES // max(case.kv_bytes(), 1)) + 1)
     pools = [(k, v)] + [(k.clone(), v.clone()) for _ in range(n_copies - 1)]
-    return case, {"q": case.q.to(device), "pools": pools, "k": k, "v": v,
-                  "bt": case.block_tables.to(device), "cl": case.context_lens.to(device)}
+    t = {"q": case.q.to(device), "pools": pools, "k": k, "v": v,
+         "bt": case.block_tables.to(device), "cl": case.context_lens.to(device)}
+    if case.fp8:
+        t["ks"], t["vs"] = case.scales(device)
+    return case, t
+
+
+def decode_step(vt, case, t, q, k, v, bt, cl, out):
+    """One decode call through the entry point for the workload's storage
+    (FP8 caches take their per-kv-head scales from ``t``)."""
+    w = case.workload
+    if case.fp8:
+        return vt.decode_fp8(q, k, v, t["ks"], t["vs"], bt, cl, w.scale, w.window, out=out)
+    return vt.decode(q, k, v, bt, cl, w.scale, w.window, out=out)
 
 
 def time_calls(vt, case, t, steps, warmup):
@@ -195,14 +210,14 @@ def time_calls(vt, case, t, steps, warmup):
     pools = t["pools"]
     for i in range(warmup):
         k, v = pools[i % len(pools)]
-        vt.decode(t["q"], k, v, t["bt"], t["cl"], w.scale, w.window, out=out)
+        decode_step(vt, case, t, t["q"], k, v, t["bt"], t["cl"], out)
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for s in range(steps):
         k, v = pools[(warmup + s) % len(pools)]
         starts[s].record(stream)
-        vt.decode(t["q"], k, v, t["bt"], t["cl"], w.scale, w.window, out=out)
+        decode_step(vt, case, t, t["q"], k, v, t["bt"], t["cl"], out)
         ends[s].record(stream)
     torch.cuda.synchronize()
     status = vt.vt_paged_attn_device_status()
@@ -227,7 +242,7 @@ def time_graph(vt, case, t, steps, warmup):
     def calls(count):
         for i in range(count):
             k, v = pools[i % n]
-            vt.decode(t["q"], k, v, t["bt"], t["cl"], w.scale, w.window, out=out)
+            decode_step(vt, case, t, t["q"], k, v, t["bt"], t["cl"], out)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -292,7 +307,7 @@ def time_e2e(vt, case, t, steps, warmup):
         for i in range(count):
             k, v = pools[i % n]
             dbuf.copy_(hbuf, non_blocking=True)
-            vt.decode(dq, k, v, dbt, dcl, w.scale, w.window, out=out)
+            decode_step(vt, case, t, dq, k, v, dbt, dcl, out)
             hout.copy_(out, non_blocking=True)
 
     side = torch.cuda.Stream()
@@ -344,8 +359,15 @@ def oracle_baseline(case, budget_s: float, threads: int = 1):
     o = oracle.default_oracle()
     w = case.workload
     k, v, bt = case.compact()
-    args = (W.to_oracle_array(case.q), W.to_oracle_array(k), W.to_oracle_array(v), bt.numpy(),
-            case.context_lens.numpy(), w.scale, w.window)
+    qa, ka, va = W.to_oracle_array(case.q), W.to_oracle_array(k), W.to_oracle_array(v)
+    tail = (bt.numpy(), case.context_lens.numpy(), w.scale, w.window)
+
+    def decode_rows(rows, threads=1):
+        if case.fp8:
+            ks, vs = case.scales()
+            return o.decode_rows_e4m3(rows, qa, ka, va, ks.numpy(), vs.numpy(), *tail, threads=threads)
+        return o.decode_rows(rows, qa, ka, va, *tail, threads=threads)
+
     rows_all = [(b, i) for b in range(w.num_seqs) for i in range(w.num_q_heads)]
     # cost of a whole call from a probe of 8 rows: oracle time grows with the
     # tokens a row attends to, so the probe's time is scaled by tokens
@@ -354,7 +376,7 @@ def oracle_baseline(case, budget_s: float, threads: int = 1):
     tokens_all = float(L_eff.sum()) * w.num_q_heads
     probe = [rows_all[j] for j in np.linspace(0, len(rows_all) - 1, 8).astype(int)]
     t0 = time.perf_counter()
-    o.decode_rows(probe, *args)
+    decode_rows(probe)
     probe_s = time.perf_counter() - t0
     tokens_probe = float(sum(L_eff[b] for b, _ in probe))
     whole_est = max(probe_s, 1e-7) * tokens_all / max(tokens_probe, 1.0)
@@ -362,7 +384,7 @@ def oracle_baseline(case, budget_s: float, threads: int = 1):
     if whole_est / threads <= budget_s:
         calls, t0 = 0, time.perf_counter()
         while True:
-            o.decode_rows(rows_all, *args, threads=threads)
+            decode_rows(rows_all, threads)
             calls += 1
             el = time.perf_counter() - t0
             if el >= budget_s or calls >= 1000:
@@ -373,7 +395,7 @@ def oracle_baseline(case, budget_s: float, threads: int = 1):
     pick = np.random.default_rng(0).permutation(pick)
     rows = [rows_all[p] for p in pick]
     t0 = time.perf_counter()
-    o.decode_rows(rows, *args, threads=threads)
+    decode_rows(rows, threads)
     el = time.perf_counter() - t0
     return el / len(rows) * len(rows_all), (f"{len(rows)} of {len(rows_all)} rows of one call of {w.name} "
                                             f"(spread evenly over the batch), {who}, scaled to a whole call")
@@ -435,7 +457,7 @@ def run_profile_only(args):
     out = torch.empty_like(t["q"])
     for i in range(args.warmup + args.steps):
         k, v = t["pools"][i % len(t["pools"])]
-        vt.decode(t["q"], k, v, t["bt"], t["cl"], w.scale, w.window, out=out)
+        decode_step(vt, case, t, t["q"], k, v, t["bt"], t["cl"], out)
     torch.cuda.synchronize()
     status = vt.vt_paged_attn_device_status()
     print(f"profile-only {w.name}: {args.warmup} + {args.steps} calls, kv bytes {case.kv_bytes()}, "

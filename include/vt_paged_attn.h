@@ -54,7 +54,9 @@ typedef enum {
                                 of vt_paged_attn_decode_noalloc, or the caller's vt_paged_attn_set_workspace) */
 } vt_status;
 
-typedef enum { VT_BF16 = 0, VT_F32 = 1 } vt_dtype;
+/* Storage types.  VT_E4M3 is an FP8 K/V cache (with bf16 q and out) and is
+ * taken only by vt_paged_attn_decode_fp8. */
+typedef enum { VT_BF16 = 0, VT_F32 = 1, VT_E4M3 = 2 } vt_dtype;
 
 /*
  * vt_paged_attn_decode -- the decode step.
@@ -140,19 +142,54 @@ VT_API vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const vo
                                               vt_stream_t stream, int max_blocks_per_seq,
                                               int num_blocks, vt_dtype dtype);
 
-/* What the last successful vt_paged_attn_decode on this host thread launched. */
+/*
+ * vt_paged_attn_decode_fp8 -- the decode step over an FP8 (E4M3) KV cache
+ * with one dequantisation scale per kv head, for keys and for values.
+ *
+ * A storage extension beyond the pages, whose kernels keep the cache in
+ * bf16: the path reads K/V bytes from HBM, so one-byte codes halve the bytes
+ * of every step.  The operation is the decode of vt_paged_attn_decode with
+ *   k_cache[page][slot][h][d] standing for  e4m3(code) * k_scale[h]
+ *   v_cache[page][slot][h][d] standing for  e4m3(code) * v_scale[h]
+ * where e4m3() is the OCP 8-bit floating-point value of the code (4 exponent
+ * bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN).
+ *
+ * Arguments as for vt_paged_attn_decode, except:
+ *   q, out            bf16 [num_seqs][num_q_heads][head_dim].
+ *   k_cache, v_cache  uint8 E4M3 codes, [num_blocks][block_size][num_kv_heads]
+ *                     [head_dim] (NHD), 16-byte aligned.
+ *   k_scale, v_scale  device float32 [num_kv_heads], 4-byte aligned; NULL is
+ *                     VT_ERR_INVALID_ARG.
+ *   head_dim          128 or 256 (64 is VT_ERR_UNSUPPORTED).
+ * Arithmetic: codes widen exactly to f16 in registers; q is taken as f16
+ * (exact for bf16 magnitudes in [2^-14, 65504]); QK^T and PV run on f16
+ * tensor-core MMAs with fp32 accumulation, the softmax weights entering PV
+ * as f16 (11 significant bits); k_scale folds into the score scale and
+ * v_scale into the final normalisation.  Workspace, plan, status and errors
+ * are those of vt_paged_attn_decode.
+ */
+VT_API vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const float* k_scale,
+                                          const float* v_scale, const int32_t* block_tables,
+                                          const int32_t* context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, float scale, int window,
+                                          vt_stream_t stream, int max_blocks_per_seq,
+                                          int num_blocks);
+
+/* What the last successful decode call on this host thread launched. */
 typedef struct {
   int grid_ctas;          /* CTAs launched (persistent, balanced split of the work) */
   int ctas_per_sm;        /* resident CTAs per SM for this kernel variant */
   int num_sms;            /* SMs of the device */
   int consumer_warps;     /* compute warps per CTA (plus one TMA producer warp) */
-  int tensor_cores;       /* 1: QK^T and PV on tensor cores (bf16), 0: CUDA cores (fp32) */
+  int tensor_cores;       /* 1: QK^T and PV on tensor cores (bf16, fp8), 0: CUDA cores (fp32) */
   int stages;             /* K/V page tiles in flight per CTA */
   int group_tile;         /* query heads computed per kv head and CTA (padded) */
   int subgroups;          /* ceil(group / group_tile) */
   int min_units_per_cta;  /* lower bound on work units per CTA (page tiles plus item weights) */
   int head_dim;
-  int dtype;              /* vt_dtype */
+  int dtype;              /* vt_dtype of the K/V cache */
   size_t smem_bytes;      /* dynamic shared memory per CTA */
   size_t workspace_bytes; /* split-KV workspace used (partials + arrival counters) */
   int launch_overlap;     /* 1: launched as a programmatic dependent (vt_paged_attn_set_overlap) */

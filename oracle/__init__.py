@@ -136,25 +136,16 @@ class Oracle:
                 elem, _ptr(bt), _ptr(cl), B, Hq, Hkv, D, P, bt.shape[1], nb, float(scale),
                 int(window))
 
-        n = rows.shape[0]
-        if threads <= 1 or n < 2:
-            rcs = [run(0, n)]
-        else:
-            bounds = np.linspace(0, n, threads + 1).astype(int)
-            with ThreadPoolExecutor(max_workers=threads) as pool:
-                rcs = list(pool.map(lambda j: run(bounds[j], bounds[j + 1]), range(threads)))
-        for rc in rcs:
-            if rc != 0:
-                raise OracleError(ERRORS.get(rc, str(rc)))
+        _over_threads(run, rows.shape[0], threads)
         return out
 
-
     def decode_rows_e4m3(self, rows, q, k_codes, v_codes, k_scale, v_scale, block_tables,
-                         context_lens, scale, window=0):
+                         context_lens, scale, window=0, threads: int = 1):
         """Selected rows of a decode over an FP8 (E4M3) KV cache: k_codes and
         v_codes are uint8 code arrays [blocks][P][Hkv][D]; element (.., h, d)
         stands for its E4M3 value times k_scale[h] (v_scale[h]).  q is bf16 bits
-        (uint16), float32 or float64.  Returns float64 [len(rows)][D]."""
+        (uint16), float32 or float64.  Returns float64 [len(rows)][D].
+        ``threads`` splits the rows over host threads as in decode_rows."""
         q = np.ascontiguousarray(q)
         q_elem = _elem_code(q)
         k_codes = np.ascontiguousarray(k_codes, dtype=np.uint8)
@@ -170,12 +161,33 @@ class Oracle:
         assert D2 == D and bt.shape[0] == B and cl.shape == (B,)
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
         out = np.zeros((rows.shape[0], D), dtype=np.float64)
-        rc = self._lib.oracle_decode_rows_kv(
-            _ptr(out), _ptr(rows), rows.shape[0], _ptr(q), q_elem, _ptr(k_codes), _ptr(v_codes), ELEM_E4M3,
-            _ptr(ks), _ptr(vs), _ptr(bt), _ptr(cl), B, Hq, Hkv, D, P, bt.shape[1], nb, float(scale), int(window))
+
+        def run(lo, hi):
+            if hi <= lo:
+                return 0
+            sub_rows = np.ascontiguousarray(rows[lo:hi])
+            sub_out = out[lo:hi]
+            return self._lib.oracle_decode_rows_kv(
+                _ptr(sub_out), _ptr(sub_rows), hi - lo, _ptr(q), q_elem, _ptr(k_codes), _ptr(v_codes), ELEM_E4M3,
+                _ptr(ks), _ptr(vs), _ptr(bt), _ptr(cl), B, Hq, Hkv, D, P, bt.shape[1], nb, float(scale),
+                int(window))
+
+        _over_threads(run, rows.shape[0], threads)
+        return out
+
+
+def _over_threads(run, n: int, threads: int) -> None:
+    """run(lo, hi) over [0, n) in one piece, or split into `threads` contiguous
+    pieces run on host threads; raises on the first nonzero return code."""
+    if threads <= 1 or n < 2:
+        rcs = [run(0, n)]
+    else:
+        bounds = np.linspace(0, n, threads + 1).astype(int)
+        with ThreadPoolExecutor(max_workers=threads) as pool:
+            rcs = list(pool.map(lambda j: run(bounds[j], bounds[j + 1]), range(threads)))
+    for rc in rcs:
         if rc != 0:
             raise OracleError(ERRORS.get(rc, str(rc)))
-        return out
 
 
 _default: Oracle | None = None

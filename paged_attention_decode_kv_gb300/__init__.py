@@ -17,10 +17,11 @@ LIBRARY_PATH = Path(__file__).resolve().parent / "_build" / "libvt_paged_attn.so
 
 (VT_OK, VT_ERR_INVALID_ARG, VT_ERR_UNSUPPORTED, VT_ERR_CUDA, VT_ERR_OOM, VT_ERR_DEVICE_TIMEOUT,
  VT_ERR_SCRATCH_LIMIT) = range(7)
-VT_BF16, VT_F32 = 0, 1
+VT_BF16, VT_F32, VT_E4M3 = 0, 1, 2
 BLOCK_SIZE = 32
 
-EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_last_plan",
+EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_decode_fp8",
+            "vt_paged_attn_last_plan",
             "vt_paged_attn_set_override", "vt_paged_attn_set_overlap", "vt_paged_attn_set_segment_cost",
             "vt_paged_attn_set_workspace", "vt_paged_attn_set_test_wait",
             "vt_paged_attn_device_status", "vt_paged_attn_device_status_detail", "vt_paged_attn_workspace_bytes",
@@ -72,6 +73,9 @@ def library() -> ctypes.CDLL:
             lib.vt_paged_attn_decode.restype = c_int
             lib.vt_paged_attn_decode_noalloc.argtypes = lib.vt_paged_attn_decode.argtypes
             lib.vt_paged_attn_decode_noalloc.restype = c_int
+            lib.vt_paged_attn_decode_fp8.argtypes = [c_void] * 8 + [c_int] * 5 + [c_float, c_int, c_void, c_int,
+                                                                                   c_int]
+            lib.vt_paged_attn_decode_fp8.restype = c_int
             lib.vt_paged_attn_last_plan.argtypes = [ctypes.POINTER(vt_plan)]
             lib.vt_paged_attn_last_plan.restype = c_int
             lib.vt_paged_attn_set_override.argtypes = [c_int, c_int]
@@ -131,6 +135,16 @@ def vt_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, context
                                                   num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                                   float(scale), int(window), stream, max_blocks_per_seq,
                                                   num_blocks, dtype)
+
+
+def vt_paged_attn_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, scale, window, stream,
+                             max_blocks_per_seq, num_blocks) -> int:
+    """Raw call of the FP8 (E4M3) KV-cache decode; returns the status code."""
+    return library().vt_paged_attn_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                              context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              block_size, float(scale), int(window), stream, max_blocks_per_seq,
+                                              num_blocks)
 
 
 def vt_paged_attn_last_plan() -> dict:
@@ -254,4 +268,48 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale=None, window: 
                               block_tables.data_ptr(), context_lens.data_ptr(), B, Hq, Hkv, D, P, scale,
                               window, _stream_handle(stream), block_tables.shape[1], nb, dtype_code(q))
     _check(st, "vt_paged_attn_decode")
+    return out
+
+
+def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale=None, window: int = 0,
+               out=None, stream=None):
+    """Decode attention over an FP8 (E4M3) KV cache, for torch CUDA tensors.
+
+    q [B][Hq][D] bf16; k_codes, v_codes [num_blocks][32][Hkv][D] uint8 E4M3
+    codes (or torch.float8_e4m3fn); k_scale, v_scale [Hkv] float32.  Returns
+    out [B][Hq][D] bf16 (allocated unless given).  Asynchronous on ``stream``.
+    """
+    import torch
+    B, Hq, D = q.shape
+    if k_codes.dtype == torch.float8_e4m3fn:
+        k_codes = k_codes.view(torch.uint8)
+    if v_codes.dtype == torch.float8_e4m3fn:
+        v_codes = v_codes.view(torch.uint8)
+    nb, P, Hkv, D2 = k_codes.shape
+    if D2 != D or v_codes.shape != k_codes.shape:
+        raise ValueError("k_codes/v_codes must be [num_blocks][32][Hkv][head_dim] matching q")
+    for name, t in (("q", q), ("k_codes", k_codes), ("v_codes", v_codes), ("k_scale", k_scale),
+                    ("v_scale", v_scale), ("block_tables", block_tables), ("context_lens", context_lens)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dtype != torch.bfloat16 or k_codes.dtype != torch.uint8 or v_codes.dtype != torch.uint8:
+        raise TypeError("q must be bfloat16 and the caches uint8 E4M3 codes")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32 or k_scale.numel() != Hkv or \
+            v_scale.numel() != Hkv:
+        raise TypeError("k_scale and v_scale must be float32 [num_kv_heads]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+    if scale is None:
+        scale = D ** -0.5
+    st = vt_paged_attn_decode_fp8(out.data_ptr(), q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                                  k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
+                                  context_lens.data_ptr(), B, Hq, Hkv, D, P, scale, window, _stream_handle(stream),
+                                  block_tables.shape[1], nb)
+    _check(st, "vt_paged_attn_decode_fp8")
     return out

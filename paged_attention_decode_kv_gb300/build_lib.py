@@ -26,6 +26,7 @@ SOURCES = [
     "decode_d256_bf16.cu",
     "decode_d128_f32.cu",
     "decode_d256_f32.cu",
+    "decode_e4m3.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -46,8 +46,12 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 namespace vt {
 
@@ -103,6 +107,10 @@ struct DecodeArgs {
   long long wait_limit;
   int withhold_cta;
   int withhold_tile;
+  // FP8 E4M3 K/V storage only: per-kv-head dequantisation scales [num_kv_heads]
+  // (a code of kv head h stands for its E4M3 value times k_scale[h] or v_scale[h]).
+  const float* k_scale;
+  const float* v_scale;
 };
 
 struct StageHeader {
@@ -117,8 +125,14 @@ struct StageHeader {
   long long item_u;  // work unit of the item's first page
 };
 
-// Consumer kinds.
-enum class Math { kSimt, kMma };
+// Consumer kinds: CUDA cores (fp32 storage); tensor cores on bf16 K/V
+// (mma.sync bf16); tensor cores on FP8 E4M3 K/V codes widened to f16 in
+// registers (mma.sync f16, bf16 queries and output).
+enum class Math { kSimt, kMma, kMma8 };
+
+// Element type of the K/V page tiles for a consumer kind.
+template <typename T, Math M>
+using KvElem = std::conditional_t<M == Math::kMma8, uint8_t, T>;
 
 // A combine the CTA owes: it was the last to finish a split item.
 struct PendingCombine {
@@ -134,17 +148,17 @@ struct Smem {
   static constexpr int TPG = kPageTokens / NG;
   // mma layout: warps split the page into (token half tg) x (head_dim part dp),
   // NCW / 2 head_dim parts.
-  static constexpr int NDP = (M == Math::kMma) ? NCW / 2 : 1;
+  static constexpr int NDP = (M != Math::kSimt) ? NCW / 2 : 1;
   static constexpr int kRedRows = (M == Math::kSimt) ? NG : 2;
-  alignas(1024) T k[NSTAGE][kPageTokens * D];
-  alignas(1024) T v[NSTAGE][kPageTokens * D];
+  alignas(1024) KvElem<T, M> k[NSTAGE][kPageTokens * D];
+  alignas(1024) KvElem<T, M> v[NSTAGE][kPageTokens * D];
   alignas(128) T q[NSTAGE][G * D];
   // Tensor-core epilogue: warps of token half 1 hand their O^T accumulator
   // fragments to the warps of token half 0 ([segment parity][dp][m-tile][lane]);
   // token half 0 then reuses its slice to stage rows for coalesced stores.
   static constexpr int XV = (G > 8) ? 8 : 4;  // accumulator values per lane and m-tile
-  static constexpr int XP = (M == Math::kMma) ? 2 : 1;
-  static constexpr int XN = (M == Math::kMma) ? D / NDP / 16 : 1;
+  static constexpr int XP = (M != Math::kSimt) ? 2 : 1;
+  static constexpr int XN = (M != Math::kSimt) ? D / NDP / 16 : 1;
   alignas(16) float xbuf[XP][NDP][XN][32][XV];
   // CUDA-core consumer only: per-group broadcast of p and the rescale factor.
   static constexpr int PG = (M == Math::kSimt) ? G : 1;
@@ -290,6 +304,35 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A * B + D, f16 inputs, fp32 accumulators, m16n8k16.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (low byte: element 0) widened to an f16 pair, exactly: every
+// E4M3 value (at most 448 in magnitude, at least 2^-9 apart from zero) is an
+// f16 normal number or zero; the NaN codes give NaN.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// A bf16 pair as an f16 pair (exact for magnitudes in [2^-14, 65504]; smaller
+// ones round to f16 subnormals, larger ones overflow).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Transpose of an 8x8 b16 matrix held one 32-bit pair per lane (row lane/4,
@@ -475,11 +518,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   using S = Smem<D, T, G, NCW, NSTAGE, MATH>;
   constexpr int NT = (NCW + 1) * 32;
   constexpr int NC = NCW * 32;  // consumer threads
-  constexpr uint32_t kTileBytes = kPageTokens * D * sizeof(T);
+  using KV = KvElem<T, MATH>;
+  constexpr uint32_t kTileBytes = kPageTokens * D * sizeof(KV);
   const int prec = G * 4 + min(G, a.group) * D;  // floats of a partial record
-  constexpr bool kMma = MATH == Math::kMma;
+  constexpr bool kMma = MATH != Math::kSimt;
+  constexpr bool kFp8 = MATH == Math::kMma8;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
                 "mma consumer shape");
+  static_assert(!kFp8 || (D % 128 == 0 && (D / (NCW / 2)) % 32 == 0), "fp8 consumer shape");
   static_assert(kMma || (S::GS <= 32 && (32 % S::GS) == 0 && S::NG * S::TPG == kPageTokens &&
                          G <= S::GS && (S::GS % G) == 0), "CUDA-core consumer shape");
 
@@ -679,10 +725,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             __syncwarp();
             // One tensor copy per K (or V) tile, each issued by its own lane.
             // bf16 boxes cover (64 columns, 32 tokens, D/64 column blocks) of one
-            // head, landing as D/64 swizzled [token][64] sub-tiles.
+            // head, landing as D/64 swizzled [token][64] sub-tiles; fp8 boxes
+            // the same with 128-code column blocks.
             if (!bad && lane < 2) {
               const bool is_v = lane == 1;
-              T* dst = is_v ? s.v[stage] : s.k[stage];
+              KV* dst = is_v ? s.v[stage] : s.k[stage];
               if constexpr (kMma)
                 tma_load_4d(dst, is_v ? &tmap_v : &tmap_k, 0, pid * kPageTokens, 0, h, &s.full[stage]);
               else
@@ -798,6 +845,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   uint32_t qb[kMma ? kKSteps : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
   float oacc[kMma ? kMt : 1][NQT][4];       // O^T accumulators
   float m_run = kNegInf, l_run = 0.f;       // simt: the lane's query
+  float sl2 = a.scale_log2;                 // score factor into the log2 domain (fp8: times k_scale[h])
+  float vsc = 1.f;                          // value factor (fp8: v_scale[h])
   float mq[NQT][2], lq[NQT][2];             // mma: queries 8n + 2tig + {0,1}
   bool poison = false;
   int hold_stage = 0;
@@ -913,15 +962,38 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         // 8n + gid, columns 16ks + 2tig (+1) and +8; queries past the live
         // group are zero.
         const uint32_t* q32 = reinterpret_cast<const uint32_t*>(s.q[stage]);
+        if constexpr (kFp8) {
+          // f16 operands.  The K fragments of a k-step carry head_dim columns
+          // 16ks + 4tig .. +3 (four consecutive codes per lane, see S3), so
+          // the contraction index is permuted the same way here: k = 2tig,
+          // 2tig + 1 are columns 16ks + 4tig, +1 and k = 2tig + 8, +9 are
+          // columns 16ks + 4tig + 2, +3.
+          const int h = hd.vh / a.subgroups;
+          sl2 = a.scale_log2 * __ldg(a.k_scale + h);
+          vsc = __ldg(a.v_scale + h);
 #pragma unroll
-        for (int n = 0; n < NQT; ++n) {
-          const int qr = 8 * n + gid;
-          const bool ok = qr < hd.gq;
+          for (int n = 0; n < NQT; ++n) {
+            const int qr = 8 * n + gid;
+            const bool ok = qr < hd.gq;
 #pragma unroll
-          for (int ks = 0; ks < kKSteps; ++ks) {
-            const int col = ks * 16 + 2 * tig;
-            qb[ks][n][0] = ok ? q32[(qr * D + col) >> 1] : 0u;
-            qb[ks][n][1] = ok ? q32[(qr * D + col + 8) >> 1] : 0u;
+            for (int ks = 0; ks < kKSteps; ++ks) {
+              const uint2 w = ok ? *reinterpret_cast<const uint2*>(q32 + ((qr * D + ks * 16 + 4 * tig) >> 1))
+                                 : make_uint2(0u, 0u);
+              qb[ks][n][0] = bf16x2_to_f16x2(w.x);
+              qb[ks][n][1] = bf16x2_to_f16x2(w.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < NQT; ++n) {
+            const int qr = 8 * n + gid;
+            const bool ok = qr < hd.gq;
+#pragma unroll
+            for (int ks = 0; ks < kKSteps; ++ks) {
+              const int col = ks * 16 + 2 * tig;
+              qb[ks][n][0] = ok ? q32[(qr * D + col) >> 1] : 0u;
+              qb[ks][n][1] = ok ? q32[(qr * D + col + 8) >> 1] : 0u;
+            }
           }
         }
 #pragma unroll
@@ -951,7 +1023,31 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sacc[n][hh][e] = 0.f;
-        {
+        if constexpr (kFp8) {
+          // K codes, [token][head_dim] bytes in 128-byte swizzled rows: one
+          // ldmatrix.x4 brings 8 x 16-byte blocks for tokens 0-7 and 8-15 of
+          // the warp and two k-steps (32 columns); lane (gid, tig) gets the
+          // four codes of columns 4tig .. +3 of each block, for token gid
+          // (+ 8).  Widened to f16 pairs they are the A fragment directly.
+          const int mi = lane >> 3, r = lane & 7;
+          const int t = 16 * tg + ((mi & 1) << 3) + r;
+#pragma unroll
+          for (int kp = 0; kp < kKSteps / 2; ++kp) {
+            const int byte = kp * 32 + ((mi >> 1) << 4);
+            const int sb = byte >> 7, chunk = (byte & 127) >> 4;
+            uint32_t c4[4];
+            ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), c4);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {  // k-step 2kp + half: blocks c4[2 half], c4[2 half + 1]
+              const uint32_t lo_tok = c4[2 * half], hi_tok = c4[2 * half + 1];
+              const uint32_t ak[4] = {e4m3x2_to_f16x2(lo_tok), e4m3x2_to_f16x2(hi_tok), e4m3x2_to_f16x2(lo_tok >> 16),
+                                      e4m3x2_to_f16x2(hi_tok >> 16)};
+              const int ks = 2 * kp + half;
+#pragma unroll
+              for (int n = 0; n < NQT; ++n) mma_f16(sacc[n][half], ak, qb[ks][n][0], qb[ks][n][1]);
+            }
+          }
+        } else {
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;  // token row this lane addresses
 #pragma unroll
@@ -978,8 +1074,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           for (int jq = 0; jq < 2; ++jq) {
             const int q = 8 * n + 2 * tig + jq;
             const bool qok = q < hd.gq;
-            const float s_lo = (qok && tok_lo) ? (sacc[n][0][jq] + sacc[n][1][jq]) * a.scale_log2 : kNegInf;
-            const float s_hi = (qok && tok_hi) ? (sacc[n][0][jq + 2] + sacc[n][1][jq + 2]) * a.scale_log2 : kNegInf;
+            const float s_lo = (qok && tok_lo) ? (sacc[n][0][jq] + sacc[n][1][jq]) * sl2 : kNegInf;
+            const float s_hi = (qok && tok_hi) ? (sacc[n][0][jq + 2] + sacc[n][1][jq + 2]) * sl2 : kNegInf;
             float mx = fmaxf(s_lo, s_hi);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -1005,21 +1101,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               oacc[mt][n][3] *= al[n][1];
             }
         }
-        // P^T as the B operand (k = token, n = query): the S^T accumulator
-        // layout transposed per 8x8 block with movmatrix, split bf16 hi + lo so
-        // hi + lo carries ~16 significant bits of p.
-        uint32_t pbh[NQT][2], pbl[NQT][2];
-#pragma unroll
-        for (int n = 0; n < NQT; ++n) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {  // tokens 0-7 then 8-15 of the warp
-            const float p0 = pr[n][2 * hh], p1 = pr[n][2 * hh + 1];
-            const uint32_t h = pack_bf16(p0, p1);
-            const uint32_t l = pack_bf16(p0 - bf16_lo_f(h), p1 - bf16_hi_f(h));
-            pbh[n][hh] = movmatrix_trans(h);
-            pbl[n][hh] = movmatrix_trans(l);
-          }
-        }
         // V rows of masked tokens may hold anything (NaN in unused slots) and
         // 0 * NaN is NaN inside the MMA: clear those tokens in the V^T
         // fragments.  This lane's fragments carry tokens 16tg + 2tig (+1) and
@@ -1029,8 +1110,60 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
                              ((tl + 1 >= hd.lo && tl + 1 < hd.hi) ? 0xffff0000u : 0u);
         const uint32_t mhi = ((tl + 8 >= hd.lo && tl + 8 < hd.hi) ? 0x0000ffffu : 0u) |
                              ((tl + 9 >= hd.lo && tl + 9 < hd.hi) ? 0xffff0000u : 0u);
-        // S6: O^T[this warp's rows] += V^T P^T over the 16 tokens.
-        {
+        if constexpr (kFp8) {
+          // P^T as an f16 B operand (11 significant bits of each weight),
+          // transposed from the S^T accumulator layout with movmatrix.
+          uint32_t pb[NQT][2];
+#pragma unroll
+          for (int n = 0; n < NQT; ++n)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) pb[n][hh] = movmatrix_trans(pack_f16(pr[n][2 * hh], pr[n][2 * hh + 1]));
+          // S6: O^T += V^T P^T.  V^T A fragments pair two tokens of one
+          // column, which sit 128 bytes apart: each lane reads the 4-byte
+          // codes of columns c0 + 4gid .. +3 for tokens 2tig, 2tig + 1,
+          // 2tig + 8, 2tig + 9 (bank-conflict free under the swizzle) and
+          // interleaves them per column with byte permutes.  A 32-column
+          // block makes two m-tiles whose rows are columns c0 + 4gid + {0, 1}
+          // and c0 + 4gid + {2, 3} (gid, gid + 8).
+#pragma unroll
+          for (int cb = 0; cb < kDPart / 32; ++cb) {
+            const int byte = dp * kDPart + cb * 32 + 4 * gid;
+            const int sb = byte >> 7, chunk = (byte & 127) >> 4, within = byte & 15;
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int t = tl + (u & 1) + ((u >> 1) << 3);  // 2tig, +1, +8, +9
+              w[u] = *reinterpret_cast<const uint32_t*>(&s.v[stage][0] + sb * (kPageTokens * 128) + t * 128 +
+                                                        ((chunk ^ (t & 7)) << 4) + within);
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {  // columns {0, 1} then {2, 3} of the lane's four
+              const uint32_t sel = half ? 0x7362u : 0x5140u;
+              const uint32_t lo_pair = __byte_perm(w[0], w[1], sel);  // tokens 2tig, 2tig + 1
+              const uint32_t hi_pair = __byte_perm(w[2], w[3], sel);  // tokens 2tig + 8, + 9
+              const uint32_t av[4] = {e4m3x2_to_f16x2(lo_pair) & mlo, e4m3x2_to_f16x2(lo_pair >> 16) & mlo,
+                                      e4m3x2_to_f16x2(hi_pair) & mhi, e4m3x2_to_f16x2(hi_pair >> 16) & mhi};
+#pragma unroll
+              for (int n = 0; n < NQT; ++n) mma_f16(oacc[2 * cb + half][n], av, pb[n][0], pb[n][1]);
+            }
+          }
+        } else {
+          // P^T as the B operand (k = token, n = query): the S^T accumulator
+          // layout transposed per 8x8 block with movmatrix, split bf16 hi + lo so
+          // hi + lo carries ~16 significant bits of p.
+          uint32_t pbh[NQT][2], pbl[NQT][2];
+#pragma unroll
+          for (int n = 0; n < NQT; ++n) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {  // tokens 0-7 then 8-15 of the warp
+              const float p0 = pr[n][2 * hh], p1 = pr[n][2 * hh + 1];
+              const uint32_t h = pack_bf16(p0, p1);
+              const uint32_t l = pack_bf16(p0 - bf16_lo_f(h), p1 - bf16_hi_f(h));
+              pbh[n][hh] = movmatrix_trans(h);
+              pbl[n][hh] = movmatrix_trans(l);
+            }
+          }
+          // S6: O^T[this warp's rows] += V^T P^T over the 16 tokens.
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi >> 1) << 3) + r;
 #pragma unroll
@@ -1213,7 +1346,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             f0[n][jq] = exp2f(m0 - Ms);
             f1[n][jq] = exp2f(m1 - Ms);
             const float L = rl[0][q] * f0[n][jq] + rl[1][q] * f1[n][jq];
-            inv[n][jq] = 1.f / L;
+            inv[n][jq] = vsc / L;
             if (split && dp == 0 && gid == 0)
               *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * prec + q * 4) =
                   make_float4(Ms, L, 0.f, 0.f);
@@ -1240,7 +1373,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int q = 8 * n + 2 * tig + (e & 1);
-            const int dl = mt * 16 + gid + ((e >> 1) << 3);
+            // bf16: m-tile rows are 16 consecutive head_dim columns; fp8: the
+            // columns of a 32-column block interleave (see S6)
+            const int dl = kFp8 ? 32 * (mt >> 1) + 4 * gid + 2 * (mt & 1) + (e >> 1) : mt * 16 + gid + ((e >> 1) << 3);
             xb[q * kDPart + dl] = o[mt][n][e];
           }
       __syncwarp();
@@ -1292,7 +1427,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   if (!cons_sync()) return;  // pend_n was written by thread 0
   const int n_pend = s.pend_n;
   float* const ring = reinterpret_cast<float*>(&s.k[0][0]);
-  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(T);
+  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(KV);
   constexpr int kRowChunks = D / 4;  // float4 chunks of a row
   constexpr int kOwn = (G * kRowChunks + NC - 1) / NC;
   uint32_t comb_phase = 0;

@@ -7,8 +7,8 @@ namespace vt {
 
 struct VariantInfo {
   int head_dim;
-  int tensor_cores;    // 1: mma.sync consumer (bf16), 0: CUDA-core consumer
-  int dtype;           // 0 bf16, 1 fp32
+  int tensor_cores;    // 1: mma.sync consumer (bf16 or fp8 K/V), 0: CUDA-core consumer
+  int dtype;           // K/V storage: 0 bf16, 1 fp32, 2 FP8 E4M3 codes (bf16 q and out)
   int group_tile;      // G
   int consumer_warps;  // NCW
   int stages;          // NSTAGE
@@ -63,8 +63,8 @@ struct Variant {
 
   static VariantInfo info() {
     return VariantInfo{D,
-                       M == Math::kMma ? 1 : 0,
-                       sizeof(T) == 2 ? 0 : 1,
+                       M != Math::kSimt ? 1 : 0,
+                       M == Math::kMma8 ? 2 : (sizeof(T) == 2 ? 0 : 1),
                        G,
                        NCW,
                        NSTAGE,
@@ -84,5 +84,7 @@ const VariantInfo* variants_d128_bf16(int* count);
 const VariantInfo* variants_d256_bf16(int* count);
 const VariantInfo* variants_d128_f32(int* count);
 const VariantInfo* variants_d256_f32(int* count);
+const VariantInfo* variants_d128_e4m3(int* count);
+const VariantInfo* variants_d256_e4m3(int* count);
 
 }  // namespace vt

@@ -62,6 +62,8 @@ const VariantInfo* find_variant(int head_dim, vt_dtype dtype, int group_tile) {
   if (head_dim == 256 && dtype == VT_BF16) table = vt::variants_d256_bf16(&n);
   if (head_dim == 128 && dtype == VT_F32) table = vt::variants_d128_f32(&n);
   if (head_dim == 256 && dtype == VT_F32) table = vt::variants_d256_f32(&n);
+  if (head_dim == 128 && dtype == VT_E4M3) table = vt::variants_d128_e4m3(&n);
+  if (head_dim == 256 && dtype == VT_E4M3) table = vt::variants_d256_e4m3(&n);
   for (int k = 0; k < n; ++k)
     if (table[k].group_tile == group_tile) return &table[k];
   return nullptr;
@@ -257,13 +259,25 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
     g_last_cuda_error = "cuTensorMapEncodeTiled entry point unavailable";
     return VT_ERR_CUDA;
   }
-  const size_t es = k.dtype == VT_BF16 ? 2 : 4;
+  const size_t es = k.dtype == VT_BF16 ? 2 : (k.dtype == VT_E4M3 ? 1 : 4);
   const cuuint64_t tokens = static_cast<cuuint64_t>(k.num_blocks) * vt::kPageTokens;
   const cuuint64_t row = static_cast<cuuint64_t>(k.head_dim) * k.num_kv_heads * es;  // bytes per token
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUtensorMap m;
   CUresult r;
-  if (k.dtype == VT_BF16) {
+  if (k.dtype == VT_E4M3) {
+    // FP8 consumer: the same 4-D view as bf16 over bytes, column blocks of
+    // 128 codes (one 128-byte swizzle row), head_dim 128 or 256.
+    constexpr cuuint64_t kCols = 128;
+    const cuuint64_t dims[4] = {kCols, tokens, static_cast<cuuint64_t>(k.head_dim) / kCols,
+                                static_cast<cuuint64_t>(k.num_kv_heads)};
+    const cuuint64_t strides[3] = {row, kCols, static_cast<cuuint64_t>(k.head_dim)};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kCols), static_cast<cuuint32_t>(vt::kPageTokens),
+                               static_cast<cuuint32_t>(k.head_dim / kCols), 1u};
+    r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(k.ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else if (k.dtype == VT_BF16) {
     // Tensor-core consumer: a 4-D view (64 columns, token, column block, kv
     // head) so one box brings a whole [32 tokens][head_dim] tile of one head,
     // stored as head_dim/64 sub-tiles of [token][64 columns] with the 128-byte
@@ -318,7 +332,9 @@ struct Call {
   int window;
   cudaStream_t stream;
   int max_blocks_per_seq, num_blocks;
-  vt_dtype dtype;
+  vt_dtype dtype;                  // K/V storage (VT_E4M3: bf16 q and out)
+  const float* k_scale = nullptr;  // VT_E4M3 only: [num_kv_heads] dequantisation scales
+  const float* v_scale = nullptr;
 };
 
 struct Plan {
@@ -334,7 +350,11 @@ struct Plan {
 vt_status validate(const Call& c) {
   if (c.num_seqs < 0) return VT_ERR_INVALID_ARG;
   if (!c.out || !c.q || !c.k_cache || !c.v_cache || !c.block_tables || !c.context_lens) return VT_ERR_INVALID_ARG;
-  if (c.dtype != VT_BF16 && c.dtype != VT_F32) return VT_ERR_INVALID_ARG;
+  if (c.dtype != VT_BF16 && c.dtype != VT_F32 && c.dtype != VT_E4M3) return VT_ERR_INVALID_ARG;
+  // an FP8 cache comes with its scales, and only through vt_paged_attn_decode_fp8
+  if ((c.dtype == VT_E4M3) != (c.k_scale != nullptr) || (c.k_scale == nullptr) != (c.v_scale == nullptr))
+    return VT_ERR_INVALID_ARG;
+  if (c.k_scale && (!aligned(c.k_scale, 4) || !aligned(c.v_scale, 4))) return VT_ERR_INVALID_ARG;
   if (c.num_q_heads <= 0 || c.num_kv_heads <= 0 || c.num_q_heads % c.num_kv_heads != 0) return VT_ERR_INVALID_ARG;
   if (c.max_blocks_per_seq <= 0 || c.num_blocks <= 0 || c.block_size <= 0 || c.head_dim <= 0)
     return VT_ERR_INVALID_ARG;
@@ -343,6 +363,7 @@ vt_status validate(const Call& c) {
       !aligned(c.block_tables, 4) || !aligned(c.context_lens, 4))
     return VT_ERR_INVALID_ARG;
   if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256) return VT_ERR_UNSUPPORTED;
+  if (c.dtype == VT_E4M3 && c.head_dim == 64) return VT_ERR_UNSUPPORTED;
   if (c.block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(c.num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(c.max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
@@ -406,6 +427,8 @@ vt_status launch(const Call& c, const Plan& p, char* base, size_t counters_regio
   args.wait_limit = g_test_wait_limit > 0 ? g_test_wait_limit : vt::kWaitLimitCycles;
   args.withhold_cta = g_test_withhold_tile >= 0 ? g_test_withhold_cta : -1;
   args.withhold_tile = g_test_withhold_tile;
+  args.k_scale = c.k_scale;
+  args.v_scale = c.v_scale;
 
   cudaError_t e = p.v->launch(tk, tv, args, p.grid, c.stream, g_overlap);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -437,7 +460,7 @@ Call make_call(void* out, const void* q, const void* k_cache, const void* v_cach
                int num_blocks, vt_dtype dtype) {
   return Call{out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
               head_dim, block_size, scale, window, reinterpret_cast<cudaStream_t>(stream), max_blocks_per_seq,
-              num_blocks, dtype};
+              num_blocks, dtype, nullptr, nullptr};
 }
 
 // ---------------------------------------------------------------------------
@@ -562,15 +585,14 @@ vt_status vt_paged_attn_set_workspace(void* dev_ptr, size_t bytes, vt_stream_t s
   return VT_OK;
 }
 
-vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                               const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
-                               int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
-                               int window, vt_stream_t stream, int max_blocks_per_seq, int num_blocks,
-                               vt_dtype dtype) {
-  const Call c = make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
-                           num_kv_heads, head_dim, block_size, scale, window, stream, max_blocks_per_seq,
-                           num_blocks, dtype);
-  if (num_seqs == 0) return VT_OK;
+}  // extern "C"
+
+namespace {
+
+// A call on the device's workspace: the caller's (vt_paged_attn_set_workspace)
+// when one is set, else the library's own.
+vt_status decode_on_workspace(const Call& c) {
+  if (c.num_seqs == 0) return VT_OK;
   vt_status st = validate(c);
   if (st != VT_OK) return st;
   Plan p;
@@ -593,6 +615,33 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   }
   const size_t used = kStatusBytes + w.counters_cap + p.need.part_bytes;
   return launch(c, p, w.base, w.counters_cap, used, source);
+}
+
+}  // namespace
+
+extern "C" {
+
+vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                               int window, vt_stream_t stream, int max_blocks_per_seq, int num_blocks,
+                               vt_dtype dtype) {
+  return decode_on_workspace(make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                       num_q_heads, num_kv_heads, head_dim, block_size, scale, window, stream,
+                                       max_blocks_per_seq, num_blocks, dtype));
+}
+
+vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                   const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, float scale, int window, vt_stream_t stream,
+                                   int max_blocks_per_seq, int num_blocks) {
+  Call c = make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, window, stream, max_blocks_per_seq, num_blocks, VT_E4M3);
+  if (!k_scale || !v_scale) return VT_ERR_INVALID_ARG;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  return decode_on_workspace(c);
 }
 
 vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,

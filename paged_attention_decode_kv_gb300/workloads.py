@@ -13,7 +13,10 @@ batch for that arm of the library.  Recipe, per case:
   context lengths, a random permutation of the page pool, Q, K (all used
   pages), V (all used pages), then any per-case extra (the peaked head);
 * Q/K/V are drawn as float32 N(0, sigma); bf16 storage is their
-  round-to-nearest-even image, fp32 storage keeps them as drawn;
+  round-to-nearest-even image, fp32 storage keeps them as drawn; FP8 (E4M3)
+  K/V storage divides each kv head's draws by one scale per head (the
+  head's largest magnitude over 448, the largest E4M3 value) and keeps the
+  nearest E4M3 codes, with bf16 queries;
 * sequence b takes the next ceil(L_b / 32) pages of the permutation; its
   block-table slots past those point at pool pages no sequence uses;
 * every pool page no sequence uses, and every in-page slot at or past L_b
@@ -43,7 +46,7 @@ class Workload:
     #                 "loguniform:a,b", "skewed"
     max_blocks_per_seq: int
     sigma: float = 1.0
-    dtype: str = "bf16"  # "bf16" | "f32"
+    dtype: str = "bf16"  # K/V storage: "bf16" | "f32" | "e4m3" (bf16 q and out)
     window: int = 0
     peaked_head: bool = False
     table_is_permutation: bool = False
@@ -59,7 +62,13 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 2 if self.dtype == "bf16" else 4
+        """Bytes of one stored K/V element."""
+        return {"bf16": 2, "f32": 4, "e4m3": 1}[self.dtype]
+
+    @property
+    def qo_elem_bytes(self) -> int:
+        """Bytes of one query or output element."""
+        return 4 if self.dtype == "f32" else 2
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -142,6 +151,23 @@ BATCH1_LONG = _register(Workload(
     num_seqs=1, num_q_heads=32, num_kv_heads=8, head_dim=128, pool_blocks=65536,
     contexts="fixed:32768", max_blocks_per_seq=1024))
 
+# FP8 (E4M3) K/V storage with per-kv-head scales: the same batches with one
+# byte per cached element (not configurations of the pages, whose caches are
+# bf16; the storage extension's own test and sweep cases).
+_FP8 = "; FP8 E4M3 K/V codes with per-kv-head scales, bf16 queries"
+QWEN3_1P7B_FP8 = _register(QWEN3_1P7B.with_(name="qwen3_1p7b_b8_gqa2_d128_fp8", dtype="e4m3",
+                                           description=QWEN3_1P7B.description + _FP8))
+D256_GQA4_FP8 = _register(D256_GQA4.with_(name="d256_gqa4_b16_fp8", dtype="e4m3",
+                                         description=D256_GQA4.description + _FP8))
+D256_GQA4_W1024_FP8 = _register(D256_GQA4.with_(name="d256_gqa4_b16_w1024_fp8", dtype="e4m3", window=1024,
+                                               description=D256_GQA4.description + "; sliding window 1024" + _FP8))
+LARGE_GQA_FP8 = _register(LARGE_GQA.with_(name="large_gqa8_b64_d128_fp8", dtype="e4m3",
+                                         description=LARGE_GQA.description + _FP8))
+SKEWED_FP8 = _register(SKEWED.with_(name="skewed_b128_gqa4_d128_fp8", dtype="e4m3",
+                                   description=SKEWED.description + _FP8))
+BATCH1_LONG_FP8 = _register(BATCH1_LONG.with_(name="batch1_ctx32768_gqa4_d128_fp8", dtype="e4m3",
+                                             description=BATCH1_LONG.description + _FP8))
+
 
 def custom(name: str, contexts, num_q_heads: int, num_kv_heads: int, head_dim: int,
            dtype: str = "bf16", window: int = 0, sigma: float = 1.0, spare_pages: int = 3) -> Workload:
@@ -212,7 +238,22 @@ class PagedCase:
 
     @property
     def dtype(self) -> torch.dtype:
+        """Storage type of q and out."""
         return self.q.dtype
+
+    @property
+    def kv_dtype(self) -> torch.dtype:
+        """Storage type of the K/V pages (uint8 E4M3 codes for FP8)."""
+        return self.k_pages.dtype
+
+    @property
+    def fp8(self) -> bool:
+        return self.workload.dtype == "e4m3"
+
+    def _nan_fill(self, shape, device):
+        if self.fp8:
+            return torch.full(shape, E4M3_NAN, dtype=torch.uint8, device=device)
+        return torch.full(shape, float("nan"), dtype=self.kv_dtype, device=device)
 
     def pool(self, device="cpu"):
         """Full (k_cache, v_cache) pools [num_blocks][P][Hkv][D] on ``device``."""
@@ -221,10 +262,14 @@ class PagedCase:
         idx = self.used_pages.to(device)
         out = []
         for pages in (self.k_pages, self.v_pages):
-            cache = torch.full(shape, float("nan"), dtype=self.dtype, device=device)
+            cache = self._nan_fill(shape, device)
             cache.index_copy_(0, idx, pages.to(device))
             out.append(cache)
         return tuple(out)
+
+    def scales(self, device="cpu"):
+        """FP8 storage: the per-kv-head (k_scale, v_scale), float32 [Hkv]."""
+        return self.extra["k_scale"].to(device), self.extra["v_scale"].to(device)
 
     def compact(self):
         """(k, v, block_tables) with only the used pages, renumbered 0..n_used-1,
@@ -234,8 +279,7 @@ class PagedCase:
         n = self.used_pages.numel()
         remap = torch.full((self.num_blocks,), n, dtype=torch.int64)
         remap[self.used_pages] = torch.arange(n)
-        nan_page = torch.full((1, w.block_size, w.num_kv_heads, w.head_dim), float("nan"),
-                              dtype=self.dtype)
+        nan_page = self._nan_fill((1, w.block_size, w.num_kv_heads, w.head_dim), "cpu")
         k = torch.cat([self.k_pages, nan_page])
         v = torch.cat([self.v_pages, nan_page])
         bt = remap[self.block_tables.long()].to(torch.int32)
@@ -251,7 +295,7 @@ class PagedCase:
 
     def qo_bytes(self) -> int:
         w = self.workload
-        return 2 * w.num_seqs * w.num_q_heads * w.head_dim * w.elem_bytes
+        return 2 * w.num_seqs * w.num_q_heads * w.head_dim * w.qo_elem_bytes
 
 
 def make_case(w: Workload, seed: int = 0) -> PagedCase:
@@ -276,24 +320,47 @@ def make_case(w: Workload, seed: int = 0) -> PagedCase:
             bt[b, s] = spare[spare_pos % spare.numel()]
             spare_pos += 1
 
-    store = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    fp8 = w.dtype == "e4m3"
+    store = torch.float32 if w.dtype == "f32" else torch.bfloat16
     q = (torch.randn((B, Hq, D), generator=g) * w.sigma).to(store)
-    k = (torch.randn((n_used, P, Hkv, D), generator=g) * w.sigma).to(store)
-    v = (torch.randn((n_used, P, Hkv, D), generator=g) * w.sigma).to(store)
+    k = torch.randn((n_used, P, Hkv, D), generator=g) * w.sigma
+    v = torch.randn((n_used, P, Hkv, D), generator=g) * w.sigma
+    if not fp8:
+        k, v = k.to(store), v.to(store)
     peaked = -1
     if w.peaked_head:
         peaked = int(torch.randint(0, Hkv, (1,), generator=g))
         k[:, :, peaked, :] *= 4  # power of two: exact in bf16 and fp32
+    extra = {}
+    if fp8:
+        k, ks = _e4m3_per_head(k)
+        v, vs = _e4m3_per_head(v)
+        extra = {"k_scale": ks, "v_scale": vs}
     # Poison the in-page tail of every sequence's last page.
+    poison = E4M3_NAN if fp8 else float("nan")
     pos = 0
     for b, n in enumerate(pages_per_seq):
         L = int(ctx[b])
         if n and L % P:
-            k[pos + n - 1, L % P:] = float("nan")
-            v[pos + n - 1, L % P:] = float("nan")
+            k[pos + n - 1, L % P:] = poison
+            v[pos + n - 1, L % P:] = poison
         pos += n
     return PagedCase(workload=w, seed=int(seed), q=q, k_pages=k, v_pages=v, used_pages=used,
-                     block_tables=bt.to(torch.int32), context_lens=ctx, peaked_kv_head=peaked)
+                     block_tables=bt.to(torch.int32), context_lens=ctx, peaked_kv_head=peaked, extra=extra)
+
+
+E4M3_MAX = 448.0
+E4M3_NAN = 0x7F  # the positive NaN code of E4M3
+
+
+def _e4m3_per_head(x: torch.Tensor):
+    """float32 [..][Hkv][D] draws -> (uint8 E4M3 codes, float32 scale per kv
+    head): each head is divided by its largest magnitude over 448 and rounded
+    to the nearest code by torch's float8_e4m3fn conversion."""
+    amax = x.abs().amax(dim=tuple(i for i in range(x.dim()) if i != x.dim() - 2))
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    codes = (x / scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
 
 
 def bf16_bits(t: torch.Tensor):
@@ -303,9 +370,10 @@ def bf16_bits(t: torch.Tensor):
 
 
 def to_oracle_array(t: torch.Tensor):
-    """Storage-exact numpy array for the oracle: bf16 -> uint16 bits, fp32 -> float32."""
+    """Storage-exact numpy array for the oracle: bf16 -> uint16 bits, fp32 ->
+    float32, E4M3 codes (uint8) -> uint8."""
     if t.dtype == torch.bfloat16:
         return bf16_bits(t)
-    if t.dtype in (torch.float32, torch.float64):
+    if t.dtype in (torch.float32, torch.float64, torch.uint8):
         return t.contiguous().numpy()
     raise TypeError(t.dtype)

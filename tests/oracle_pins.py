@@ -423,6 +423,24 @@ def pin_decode_rows_matches_decode(oracle):
                     assert np.array_equal(got[r], full[b, i]), (kind, window, threads, r, b, i)
 
 
+def pin_e4m3_rows_over_threads(oracle):
+    """The FP8 row-sampling entry gives each (sequence, query head) the same
+    bits whether the rows run on one host thread, are split over seven, or
+    are asked for one at a time (pairs shuffled and repeated)."""
+    rng = np.random.default_rng(31)
+    lens, hq, hkv, d = [1, 33, 70, 5, 40], 6, 2, 32
+    q, ck, cv, ks, vs, _, _ = _e4m3_case(rng, lens, hq, hkv, d)
+    kc, vc, bt, cl = paginate(ck, cv, 32, rng)
+    pairs = [(b, i) for b in range(len(lens)) for i in range(hq)]
+    rows = [pairs[j] for j in rng.permutation(len(pairs))] + [(2, 5), (0, 0), (2, 5)]
+    one = oracle.decode_rows_e4m3(rows, q, kc, vc, ks, vs, bt, cl, 0.3, 20)
+    seven = oracle.decode_rows_e4m3(rows, q, kc, vc, ks, vs, bt, cl, 0.3, 20, threads=7)
+    assert np.array_equal(one, seven)
+    for r, pair in enumerate(rows):
+        single = oracle.decode_rows_e4m3([pair], q, kc, vc, ks, vs, bt, cl, 0.3, 20)[0]
+        assert np.array_equal(one[r], single), (r, pair)
+
+
 def pin_query_heads_independent(oracle):
     """Each query head alone (Hq = Hkv = 1, its kv head's pages) gives the same
     bits as inside the full GQA problem."""
@@ -498,11 +516,13 @@ def pin_rejects_bad_inputs(oracle):
                            (bt, np.asarray([bt.shape[1] * 32 + 1], np.int32)),
                            (np.where(bt >= 0, kc.shape[0], bt).astype(np.int32), cl),
                            (np.full_like(bt, -1), cl)):
-        try:
-            oracle.decode(q, kc, vc, bad_bt, bad_cl, 0.3, 0)
-        except OracleError:
-            continue
-        raise AssertionError("oracle accepted an invalid input")
+        for call in (lambda: oracle.decode(q, kc, vc, bad_bt, bad_cl, 0.3, 0),
+                     lambda: oracle.decode_rows([(0, 0), (0, 1)], q, kc, vc, bad_bt, bad_cl, 0.3, 0, threads=2)):
+            try:
+                call()
+            except OracleError:
+                continue
+            raise AssertionError("oracle accepted an invalid input")
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -124,12 +124,14 @@ def test_unmutated_copy_passes_all_pins(tmp_path):
 
 
 # Mistakes planted in a copy of the oracle's Python front end (the host-thread
-# split of the row-sampling entry), run through the pin that covers it.
+# split of the row-sampling entries), run through every pin.
 PY_MUTANTS = {
     "thread_split_results_dropped": ("sub_out = out[lo:hi]", "sub_out = out[lo:hi].copy()"),
     "thread_split_rows_shifted": ("sub_rows = np.ascontiguousarray(rows[lo:hi])",
                                   "sub_rows = np.ascontiguousarray(rows[max(lo - 1, 0):hi - (lo > 0)])"),
     "thread_split_last_part_dropped": ("range(threads)))", "range(threads - 1)))"),
+    "thread_split_rc_ignored": ("    for rc in rcs:\n        if rc != 0:\n            raise OracleError(ERRORS.get(rc, str(rc)))",
+                                "    for rc in rcs:\n        pass"),
 }
 
 PY_RUNNER = textwrap.dedent("""
@@ -138,13 +140,15 @@ PY_RUNNER = textwrap.dedent("""
     spec = importlib.util.spec_from_file_location("oracle_mut", {init!r})
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
-    from oracle_pins import pin_decode_rows_matches_decode
+    from oracle_pins import ALL_PINS
     o = mod.Oracle({lib!r})
-    try:
-        pin_decode_rows_matches_decode(o)
-        print(json.dumps([]))
-    except Exception:
-        print(json.dumps(["pin_decode_rows_matches_decode"]))
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except Exception:
+            failed.append(pin.__name__)
+    print(json.dumps(failed))
 """)
 
 

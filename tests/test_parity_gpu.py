@@ -1,8 +1,10 @@
 """CUDA path vs the fp64 oracle, element by element, through the C-ABI.
 
 Tolerances (fixed by the decode PR's CPU-oracle gate and the workload spec):
-bf16 storage: NMSE <= 5e-4 over the call's outputs and max |err| <= 2e-2;
-fp32 storage: max |err| <= 1e-5.  NMSE = sum (gpu - ref)^2 / sum ref^2.
+bf16 output (bf16 storage, and the FP8 E4M3 K/V cache against the oracle
+on the dequantised cache): NMSE <= 5e-4 over the call's outputs and
+max |err| <= 2e-2; fp32 storage: max |err| <= 1e-5.
+NMSE = sum (gpu - ref)^2 / sum ref^2.
 
 These tests fail (never skip) when no GPU or no library is present: a GPU
 job that cannot run them must not look green.
@@ -45,14 +47,24 @@ def _reset_override():
         vt.vt_paged_attn_set_workspace(0, 0)
 
 
-def gpu_run(case, dev, grid=0, min_units=0, window=None, tables=None, lens=None, stream=None):
+def run_decode(case, q, k, v, bt, cl, window=None, out=None, stream=None, scale=None):
+    """One decode through the entry point for the case's storage type."""
     w = case.workload
+    scale = w.scale if scale is None else scale
+    window = w.window if window is None else window
+    if case.fp8:
+        ks, vs = case.scales(q.device)
+        return vt.decode_fp8(q, k, v, ks, vs, bt, cl, scale, window, out=out, stream=stream)
+    return vt.decode(q, k, v, bt, cl, scale, window, out=out, stream=stream)
+
+
+def gpu_run(case, dev, grid=0, min_units=0, window=None, tables=None, lens=None, stream=None):
     k, v = case.pool(dev)
     q = case.q.to(dev)
     bt = (case.block_tables if tables is None else tables).to(dev)
     cl = (case.context_lens if lens is None else lens).to(dev)
     vt.vt_paged_attn_set_override(grid, min_units)
-    out = vt.decode(q, k, v, bt, cl, w.scale, w.window if window is None else window, stream=stream)
+    out = run_decode(case, q, k, v, bt, cl, window=window, stream=stream)
     plan = vt.vt_paged_attn_last_plan()
     vt.vt_paged_attn_set_override(0, 0)
     torch.cuda.synchronize()
@@ -70,6 +82,10 @@ def oracle_rows(case, rows=None, window=None, lens=None):
             w.scale, w.window if window is None else window)
     if rows is None:
         rows = [(b, i) for b in range(w.num_seqs) for i in range(w.num_q_heads)]
+    if case.fp8:
+        ks, vs = case.scales()
+        return np.asarray(rows), o.decode_rows_e4m3(rows, args[0], args[1], args[2], ks.numpy(), vs.numpy(),
+                                                    *args[3:], threads=THREADS)
     return np.asarray(rows), o.decode_rows(rows, *args, threads=THREADS)
 
 
@@ -90,9 +106,9 @@ def check_case(case, dev, rows=None, **kw):
     out, plan = gpu_run(case, dev, **kw)
     # the intended variant ran: head_dim, storage type and consumer kind
     w = case.workload
-    bf16 = case.q.dtype == torch.bfloat16
-    assert plan["head_dim"] == w.head_dim and plan["dtype"] == (vt.VT_BF16 if bf16 else vt.VT_F32)
-    assert plan["tensor_cores"] == (1 if bf16 else 0)
+    code = {"bf16": vt.VT_BF16, "f32": vt.VT_F32, "e4m3": vt.VT_E4M3}[w.dtype]
+    assert plan["head_dim"] == w.head_dim and plan["dtype"] == code
+    assert plan["tensor_cores"] == (0 if w.dtype == "f32" else 1)
     assert plan["group_tile"] * plan["subgroups"] >= w.num_q_heads // w.num_kv_heads
     idx, ref = oracle_rows(case, rows, window=kw.get("window"))
     got = out[idx[:, 0], idx[:, 1]].to(torch.float64).numpy()
@@ -101,7 +117,7 @@ def check_case(case, dev, rows=None, **kw):
 
 # ---------------------------------------------------------------------------
 SMALL = [W.TINY, W.QWEN3_1P7B, W.D256_GQA4, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D256_GQA4_F32_W1024,
-         W.D64_GQA4, W.D64_GQA4_F32]
+         W.D64_GQA4, W.D64_GQA4_F32, W.QWEN3_1P7B_FP8, W.D256_GQA4_FP8, W.D256_GQA4_W1024_FP8]
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -121,7 +137,8 @@ def _sample_rows(case, n_seqs=6):
     return [(b, i) for b in sorted(pick) for i in range(case.workload.num_q_heads)]
 
 
-@pytest.mark.parametrize("w", [W.LARGE_GQA, W.SKEWED, W.BATCH1_LONG], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.LARGE_GQA, W.SKEWED, W.BATCH1_LONG, W.LARGE_GQA_FP8, W.SKEWED_FP8,
+                               W.BATCH1_LONG_FP8], ids=lambda w: w.name)
 def test_workload_full_size_sampled(dev, w):
     """Full-size workloads in the benchmark's launch plan; the oracle checks all
     heads of sampled sequences (always the longest and the shortest)."""
@@ -130,7 +147,8 @@ def test_workload_full_size_sampled(dev, w):
 
 
 @pytest.mark.parametrize("grid", [1, 2, 3, 7, 64, 152, 500, 1500])
-@pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D64_GQA4], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D64_GQA4, W.QWEN3_1P7B_FP8,
+                               W.D256_GQA4_W1024_FP8], ids=lambda w: w.name)
 def test_forced_partitions(dev, w, grid):
     """The split/no-split paths and the combine: any CTA count (with at least
     one tile per CTA) gives the oracle's result."""
@@ -151,7 +169,8 @@ def test_page_boundary_contexts(dev, ctx):
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4), (16, 4), (20, 4), (32, 4), (48, 4), (64, 4), (6, 2)])
-@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (128, "f32"), (64, "bf16"), (64, "f32")])
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (128, "f32"), (64, "bf16"), (64, "f32"),
+                                     (128, "e4m3"), (256, "e4m3")])
 def test_group_sizes(dev, hq, hkv, d, dtype):
     """GQA groups 1..16 including ones that pad the group tile (3, 5) or need
     several query subgroups per kv head (12, 16)."""
@@ -160,11 +179,61 @@ def test_group_sizes(dev, hq, hkv, d, dtype):
     check_case(case, dev, grid=5, min_units=1)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("window", [1, 2, 31, 32, 33, 64, 299, 300, 301, 5000])
-def test_windows(dev, window):
-    case = W.make_case(W.custom("win", [1, 33, 300, 1000], 16, 4, 128), 9)
+def test_windows(dev, window, dtype):
+    case = W.make_case(W.custom("win", [1, 33, 300, 1000], 16, 4, 128, dtype=dtype), 9)
     check_case(case, dev, window=window)
     check_case(case, dev, window=window, grid=11, min_units=1)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_fp8_page_boundary_contexts(dev, d):
+    """The FP8 arm on the contexts straddling the 32-token page, with and
+    without a window, split and unsplit."""
+    case = W.make_case(W.custom(f"fp8_straddle_d{d}", list(STRADDLE), 16, 4, d, dtype="e4m3"), 26)
+    for window in (0, 33, 300):
+        check_case(case, dev, window=window)
+        check_case(case, dev, window=window, grid=13, min_units=1)
+
+
+def test_fp8_scales_per_head(dev):
+    """Scaling one kv head's key or value scale acts on exactly that head's
+    query rows: the value scale multiplies them, the key scale sharpens their
+    softmax (checked against the oracle with the same scales)."""
+    case = W.make_case(W.custom("fp8_scales", [40, 300, 77], 16, 4, 128, dtype="e4m3"), 27)
+    base, _ = gpu_run(case, dev)
+    ks, vs = case.extra["k_scale"].clone(), case.extra["v_scale"].clone()
+    case.extra["v_scale"][2] *= 4
+    case.extra["k_scale"][1] *= 3
+    try:
+        check_case(case, dev)
+        got, _ = gpu_run(case, dev)
+    finally:
+        case.extra["k_scale"], case.extra["v_scale"] = ks, vs
+    g = case.workload.group
+    for i in range(16):
+        h = i // g
+        if h == 2:
+            assert torch.equal(got[:, i].float(), (base[:, i].float() * 4).bfloat16().float())
+        elif h == 1:
+            assert not torch.equal(got[:, i], base[:, i])
+        else:
+            assert torch.equal(got[:, i], base[:, i])
+
+
+def test_fp8_invalid_device_data_and_empty(dev):
+    """FP8 arm: an empty context gives a zero row, a page id outside the pool
+    NaN rows for that sequence only."""
+    case = W.make_case(W.custom("fp8_bad", [0, 40, 70, 33], 8, 2, 128, dtype="e4m3"), 28)
+    bt = case.block_tables.clone()
+    bt[2, 1] = case.num_blocks + 1
+    for grid in (0, 3):
+        out, _ = gpu_run(case, dev, tables=bt, grid=grid, min_units=1)
+        assert torch.count_nonzero(out[0]) == 0
+        assert torch.isnan(out[2].float()).all()
+        idx, ref = oracle_rows(case, [(b, i) for b in (1, 3) for i in range(8)])
+        compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -291,7 +360,8 @@ def test_segment_cost_ragged(dev):
 
 def _overlap_cases():
     return [W.make_case(W.QWEN3_1P7B, 18), W.make_case(W.custom("ovl_empty", [0, 70, 0, 1000, 33], 16, 4, 128), 18),
-            W.make_case(W.D256_GQA4_W1024, 18), W.make_case(W.custom("ovl_f32", [5, 300, 2000], 8, 2, 128, dtype="f32"), 18)]
+            W.make_case(W.D256_GQA4_W1024, 18), W.make_case(W.custom("ovl_f32", [5, 300, 2000], 8, 2, 128, dtype="f32"), 18),
+            W.make_case(W.custom("ovl_fp8", [7, 500, 1200], 32, 8, 128, dtype="e4m3"), 18)]
 
 
 def test_overlap_back_to_back(dev):
@@ -314,7 +384,7 @@ def test_overlap_back_to_back(dev):
     torch.cuda.synchronize()
     for r in range(3):
         for j, (case, q, k, v, bt, cl) in enumerate(dev_in):
-            vt.decode(q, k, v, bt, cl, case.workload.scale, case.workload.window, out=outs[(r, j)])
+            run_decode(case, q, k, v, bt, cl, out=outs[(r, j)])
             assert vt.vt_paged_attn_last_plan()["launch_overlap"] == 1
     case0, q0, k0, v0, bt0, cl0 = dev_in[0]
     vt.decode(q0, k0, v0, bt0, cl0, case0.workload.scale, out=shared)
