@@ -150,6 +150,15 @@ def pin_sdpa_head_dim_64(oracle):
     _check_against_sdpa(oracle, rng, [1, 31, 33, 100], 8, 2, 64, 32, "f32", 45, 1e-12)
 
 
+def pin_sdpa_head_dim_512(oracle):
+    """head_dim 512 (the widest arm the pages' kernels cover): bf16 storage,
+    GQA 4, contexts across page boundaries, with and without a window,
+    against brute force."""
+    rng = np.random.default_rng(32)
+    _check_against_sdpa(oracle, rng, [1, 31, 33, 70], 8, 2, 512, 32, "bf16", 0, 1e-12)
+    _check_against_sdpa(oracle, rng, [1, 31, 33, 70], 8, 2, 512, 32, "bf16", 40, 1e-12)
+
+
 def _e4m3_value(codes):
     """Values of E4M3 codes by torch's float8_e4m3fn (independent of the oracle)."""
     t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
