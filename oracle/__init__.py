@@ -84,6 +84,10 @@ class Oracle:
         self._lib.oracle_decode_rows_kv.argtypes = [c_void, c_void, c_int, c_void, c_int, c_void, c_void, c_int,
                                                     c_void, c_void] + common[4:]
         self._lib.oracle_decode_rows_kv.restype = c_int
+        self._lib.oracle_decode_multi_rows.argtypes = [c_void, c_void, c_int, c_void, c_void, c_void, c_int, c_void,
+                                                       c_void, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                                       c_int, c_double, c_int]
+        self._lib.oracle_decode_multi_rows.restype = c_int
 
     @staticmethod
     def _prepare(q, k_cache, v_cache, block_tables, context_lens):
@@ -171,6 +175,36 @@ class Oracle:
                 _ptr(sub_out), _ptr(sub_rows), hi - lo, _ptr(q), q_elem, _ptr(k_codes), _ptr(v_codes), ELEM_E4M3,
                 _ptr(ks), _ptr(vs), _ptr(bt), _ptr(cl), B, Hq, Hkv, D, P, bt.shape[1], nb, float(scale),
                 int(window))
+
+        _over_threads(run, rows.shape[0], threads)
+        return out
+
+    def decode_multi_rows(self, rows, q, k_cache, v_cache, block_tables, context_lens, scale, window=0,
+                          threads: int = 1):
+        """Selected rows [(b, j, i), ...] of a multi-token decode -> float64
+        [len(rows)][D].  q is [B][q_len][Hq][D] (bf16 bits, float32 or
+        float64); the caches, block table and context lengths as for decode;
+        new token j of sequence b attends to the first
+        context_lens[b] - q_len + 1 + j tokens."""
+        q = np.ascontiguousarray(q)
+        if q.ndim != 4:
+            raise ValueError("q is [B][q_len][Hq][D]")
+        B, q_len, Hq, D = q.shape
+        qq, k_cache, v_cache, bt, cl, elem = self._prepare(q.reshape(B * q_len, Hq, D), k_cache, v_cache,
+                                                           block_tables, context_lens)
+        nb, P, Hkv, D2 = k_cache.shape
+        assert D2 == D and bt.shape[0] == B and cl.shape == (B,)
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+        out = np.zeros((rows.shape[0], D), dtype=np.float64)
+
+        def run(lo, hi):
+            if hi <= lo:
+                return 0
+            sub_rows = np.ascontiguousarray(rows[lo:hi])
+            sub_out = out[lo:hi]
+            return self._lib.oracle_decode_multi_rows(
+                _ptr(sub_out), _ptr(sub_rows), hi - lo, _ptr(q), _ptr(k_cache), _ptr(v_cache), elem, _ptr(bt),
+                _ptr(cl), B, q_len, Hq, Hkv, D, P, bt.shape[1], nb, float(scale), int(window))
 
         _over_threads(run, rows.shape[0], threads)
         return out

@@ -40,7 +40,10 @@
  *     contiguous ("NHD");
  *   - block table [num_seqs][max_blocks_per_seq] int32, row-major;
  *   - window W > 0 keeps the keys t with L - W <= t < L; W <= 0 keeps all;
- *   - a sequence with L == 0 yields a zero row.
+ *   - a sequence with L == 0 yields a zero row;
+ *   - multi-token decode: new token j of q_len sits at position L - q_len + j
+ *     and attends causally to the tokens up to and including itself
+ *     (oracle_decode_multi_row).
  *
  * Error behaviour: returns ORACLE_OK (0) or a negative code, and writes
  * nothing for the offending row, when a context length is negative or longer
@@ -248,6 +251,60 @@ int oracle_decode_rows(double* out, const int32_t* rows, int num_rows,
         context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
         block_size, max_blocks_per_seq, num_blocks, scale, window, rows[2 * r],
         rows[2 * r + 1]);
+    if (rc != ORACLE_OK) return rc;
+  }
+  return ORACLE_OK;
+}
+
+/* Multi-token decode (several new tokens per sequence, e.g. a chunk of a
+ * prefill or draft tokens to verify) over the same paged cache.  The PR
+ * "perf(rocm): head_dim=128 decode arm", section "Not claimed", lists a
+ * d=128 prefill as owed; the reading taken here: every sequence b carries
+ * q_len new tokens whose keys and values already sit in its pages as the last
+ * q_len of its context_lens[b] tokens; new token j (0 <= j < q_len), at
+ * position L - q_len + j, attends causally to the tokens before it and to
+ * itself, i.e. it is the single-token decode over a context of
+ * L - q_len + 1 + j tokens (the window, if any, counts back from there).
+ * q and out are [num_seqs][q_len][num_q_heads][head_dim].  A context shorter
+ * than q_len is rejected (ORACLE_BAD_CONTEXT). */
+int oracle_decode_multi_row(double* out_row, const void* q, int elem,
+                            const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                            int head_dim, int block_size, int max_blocks_per_seq,
+                            int num_blocks, double scale, int window, int b, int j, int i) {
+  if (!q || !context_lens || !block_tables || q_len < 1 || j < 0 || j >= q_len ||
+      b < 0 || b >= num_seqs || num_q_heads <= 0 || head_dim <= 0 ||
+      elem < ORACLE_ELEM_BF16 || elem > ORACLE_ELEM_F64)
+    return ORACLE_BAD_ARG;
+  const int L = context_lens[b];
+  if (L < q_len) return ORACLE_BAD_CONTEXT;
+  const int32_t Lj = L - q_len + 1 + j;
+  static const size_t elem_size[3] = {2, 4, 8};
+  const char* q_tok = (const char*)q +
+                      ((size_t)b * q_len + j) * num_q_heads * head_dim * elem_size[elem];
+  return oracle_decode_row_kv(out_row, q_tok, elem, k_cache, v_cache, elem, NULL, NULL,
+                              block_tables + (size_t)b * max_blocks_per_seq, &Lj, 1,
+                              num_q_heads, num_kv_heads, head_dim, block_size,
+                              max_blocks_per_seq, num_blocks, scale, window, 0, i);
+}
+
+/* Chosen rows of a multi-token decode: rows[3*r .. 3*r+2] = (b, j, i); out is
+ * [num_rows][head_dim]. */
+int oracle_decode_multi_rows(double* out, const int32_t* rows, int num_rows,
+                             const void* q, const void* k_cache, const void* v_cache,
+                             int elem, const int32_t* block_tables,
+                             const int32_t* context_lens, int num_seqs, int q_len,
+                             int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks_per_seq, int num_blocks,
+                             double scale, int window) {
+  if (!out || !rows || num_rows < 0 || head_dim <= 0) return ORACLE_BAD_ARG;
+  for (int r = 0; r < num_rows; ++r) {
+    const int rc = oracle_decode_multi_row(
+        out + (size_t)r * head_dim, q, elem, k_cache, v_cache, block_tables,
+        context_lens, num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
+        block_size, max_blocks_per_seq, num_blocks, scale, window, rows[3 * r],
+        rows[3 * r + 1], rows[3 * r + 2]);
     if (rc != ORACLE_OK) return rc;
   }
   return ORACLE_OK;

@@ -450,6 +450,79 @@ def pin_e4m3_rows_over_threads(oracle):
         assert np.array_equal(one[r], single), (r, pair)
 
 
+def _multi_case(rng, lens, q_len, hq, hkv, d, kind, block_size):
+    q = _rand(rng, (len(lens), q_len, hq, d), kind)
+    dk = [_rand(rng, (L, hkv, d), kind) for L in lens]
+    dv = [_rand(rng, (L, hkv, d), kind) for L in lens]
+    kc, vc, bt, cl = paginate(dk, dv, block_size, rng)
+    return q, dk, dv, kc, vc, bt, cl
+
+
+def _all_multi_rows(B, q_len, hq):
+    return [(b, j, i) for b in range(B) for j in range(q_len) for i in range(hq)]
+
+
+def pin_multi_token_against_sdpa(oracle):
+    """Multi-token decode (q_len new tokens per sequence, the last q_len of its
+    context) against brute force: torch fp64 SDPA on dense K/V with an
+    explicit causal mask, new token j seeing keys t <= L - q_len + j (and,
+    with a window W, t > L - q_len + j - W); several q_len, windows, GQA
+    groups and page sizes."""
+    rng = np.random.default_rng(33)
+    for q_len, hq, hkv, d, bs, kind in ((3, 4, 2, 16, 32, "bf16"), (5, 6, 3, 8, 4, "f64"), (1, 4, 4, 8, 32, "f32"),
+                                        (8, 8, 2, 128, 32, "bf16")):
+        lens = [q_len, q_len + 1, 33, 70]
+        q, dk, dv, kc, vc, bt, cl = _multi_case(rng, lens, q_len, hq, hkv, d, kind, bs)
+        scale = 1.0 / math.sqrt(d)
+        for window in (0, 2, 40):
+            rows = _all_multi_rows(len(lens), q_len, hq)
+            got = oracle.decode_multi_rows(rows, q, kc, vc, bt, cl, scale, window)
+            want = np.zeros((len(lens), q_len, hq, d))
+            for b, L in enumerate(lens):
+                qq = torch.from_numpy(widen(q[b])).permute(1, 0, 2)[None]          # [1][Hq][q_len][D]
+                kk = torch.from_numpy(widen(dk[b])).permute(1, 0, 2)[None]
+                vv = torch.from_numpy(widen(dv[b])).permute(1, 0, 2)[None]
+                pos = L - q_len + torch.arange(q_len)[:, None]                   # position of new token j
+                t = torch.arange(L)[None, :]
+                mask = t <= pos
+                if window > 0:
+                    mask &= t > pos - window
+                o = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask[None, None], scale=scale,
+                                                   enable_gqa=True)
+                want[b] = o[0].permute(1, 0, 2).numpy()
+            err = np.abs(got - want.reshape(-1, d)).max()
+            assert err <= 1e-12, f"multi-token oracle vs SDPA max |err| {err:.3e} (q_len {q_len}, W {window})"
+
+
+def pin_multi_token_reduces_to_decode(oracle):
+    """q_len = 1 is the single-token decode, and the last new token of any
+    q_len attends to the whole context exactly as the single-token decode of
+    that token does (same bits)."""
+    rng = np.random.default_rng(34)
+    lens, hq, hkv, d = [4, 33, 70, 9], 4, 2, 16
+    for q_len in (1, 4):
+        q, dk, dv, kc, vc, bt, cl = _multi_case(rng, lens, q_len, hq, hkv, d, "bf16", 32)
+        for window in (0, 5):
+            rows = _all_multi_rows(len(lens), q_len, hq)
+            got = oracle.decode_multi_rows(rows, q, kc, vc, bt, cl, 0.3, window).reshape(len(lens), q_len, hq, d)
+            last = oracle.decode(np.ascontiguousarray(q[:, -1]), kc, vc, bt, cl, 0.3, window)
+            assert np.array_equal(got[:, -1], last), (q_len, window)
+
+
+def pin_multi_token_rejects_short_context(oracle):
+    """A context shorter than the new tokens it must hold is refused."""
+    from oracle import OracleError
+    rng = np.random.default_rng(35)
+    q, dk, dv, kc, vc, bt, cl = _multi_case(rng, [2, 5], 3, 2, 1, 8, "f64", 32)
+    try:
+        oracle.decode_multi_rows([(0, 0, 0)], q, kc, vc, bt, cl, 0.3, 0)
+    except OracleError:
+        pass
+    else:
+        raise AssertionError("oracle accepted a context shorter than q_len")
+    oracle.decode_multi_rows([(1, 2, 1)], q, kc, vc, bt, cl, 0.3, 0)
+
+
 def pin_query_heads_independent(oracle):
     """Each query head alone (Hq = Hkv = 1, its kv head's pages) gives the same
     bits as inside the full GQA problem."""

@@ -57,6 +57,10 @@ MUTANTS = {
     "rows_pair_swapped": ("window, rows[2 * r],\n        rows[2 * r + 1]);", "window, rows[2 * r + 1],\n        rows[2 * r]);", 0),
     "rows_kv_pair_swapped": ("rows[2 * r], rows[2 * r + 1]);", "rows[2 * r + 1], rows[2 * r]);", 0),
     "rows_output_not_advanced": ("out + (size_t)r * head_dim, q, k_cache", "out, q, k_cache", 0),
+    "multi_causal_off_by_one": ("const int32_t Lj = L - q_len + 1 + j;", "const int32_t Lj = L - q_len + j;", 0),
+    "multi_causal_ignored": ("const int32_t Lj = L - q_len + 1 + j;", "const int32_t Lj = L;", 0),
+    "multi_token_offset_dropped": ("((size_t)b * q_len + j) * num_q_heads", "((size_t)b * q_len) * num_q_heads", 0),
+    "multi_rows_j_i_swapped": ("rows[3 * r + 1], rows[3 * r + 2]);", "rows[3 * r + 2], rows[3 * r + 1]);", 0),
     "scale_of_kv_head_zero": ("const double ks = k_scale ? k_scale[h] : 1.0;", "const double ks = k_scale ? k_scale[0] : 1.0;", 0),
 }
 
