@@ -43,7 +43,7 @@ DEFAULT_WORKLOAD = "skewed_b128_gqa4_d128"
 SWEEP = ["batch1_ctx32768_gqa4_d128", "large_gqa8_b64_d128", "d256_gqa4_b16", "d256_gqa4_b16_w1024",
          "d256_gqa4_b16_f32", "d256_gqa4_b16_f32_w1024", "qwen3_1p7b_b8_gqa2_d128", "d64_gqa4_b32",
          "d64_gqa4_b32_f32", "skewed_b128_gqa4_d128_fp8", "batch1_ctx32768_gqa4_d128_fp8",
-         "large_gqa8_b64_d128_fp8", "d256_gqa4_b16_fp8"]
+         "large_gqa8_b64_d128_fp8", "d256_gqa4_b16_fp8", "d512_gqa4_b16", "d512_gqa4_b16_w1024", "multi_q4_b64_gqa4_d128"]
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "vt_paged_attn_api.cu"]  # shared by every variant
 
@@ -197,6 +197,8 @@ def decode_step(vt, case, t, q, k, v, bt, cl, out):
     w = case.workload
     if case.fp8:
         return vt.decode_fp8(q, k, v, t["ks"], t["vs"], bt, cl, w.scale, w.window, out=out)
+    if w.q_len > 1:
+        return vt.decode_multi(q, k, v, bt, cl, w.scale, w.window, out=out)
     return vt.decode(q, k, v, bt, cl, w.scale, w.window, out=out)
 
 
@@ -363,22 +365,27 @@ def oracle_baseline(case, budget_s: float, threads: int = 1):
     tail = (bt.numpy(), case.context_lens.numpy(), w.scale, w.window)
 
     def decode_rows(rows, threads=1):
+        if w.q_len > 1:
+            return o.decode_multi_rows(rows, qa, ka, va, *tail, threads=threads)
         if case.fp8:
             ks, vs = case.scales()
             return o.decode_rows_e4m3(rows, qa, ka, va, ks.numpy(), vs.numpy(), *tail, threads=threads)
         return o.decode_rows(rows, qa, ka, va, *tail, threads=threads)
 
-    rows_all = [(b, i) for b in range(w.num_seqs) for i in range(w.num_q_heads)]
+    if w.q_len > 1:
+        rows_all = [(b, j, i) for b in range(w.num_seqs) for j in range(w.q_len) for i in range(w.num_q_heads)]
+    else:
+        rows_all = [(b, i) for b in range(w.num_seqs) for i in range(w.num_q_heads)]
     # cost of a whole call from a probe of 8 rows: oracle time grows with the
     # tokens a row attends to, so the probe's time is scaled by tokens
     L = case.context_lens.numpy().astype(np.int64)
     L_eff = np.minimum(L, w.window) if w.window > 0 else L
-    tokens_all = float(L_eff.sum()) * w.num_q_heads
+    tokens_all = float(L_eff.sum()) * w.num_q_heads * w.q_len
     probe = [rows_all[j] for j in np.linspace(0, len(rows_all) - 1, 8).astype(int)]
     t0 = time.perf_counter()
     decode_rows(probe)
     probe_s = time.perf_counter() - t0
-    tokens_probe = float(sum(L_eff[b] for b, _ in probe))
+    tokens_probe = float(sum(L_eff[r[0]] for r in probe))
     whole_est = max(probe_s, 1e-7) * tokens_all / max(tokens_probe, 1.0)
     who = "single thread" if threads == 1 else f"{threads} threads"
     if whole_est / threads <= budget_s:

@@ -73,7 +73,8 @@ typedef enum { VT_BF16 = 0, VT_F32 = 1, VT_E4M3 = 2 } vt_dtype;
  *   context_lens [num_seqs] int32, 0 <= L_b <= max_blocks_per_seq * block_size.
  * Sizes:
  *   num_seqs >= 0 (0 is a no-op), num_q_heads % num_kv_heads == 0,
- *   head_dim in {64, 128, 256}, block_size == 32, scale finite (1/sqrt(head_dim)
+ *   head_dim in {64, 128, 256} (and 512 for bf16 storage; the pages' widest
+ *   arm), block_size == 32, scale finite (1/sqrt(head_dim)
  *   is usual), window <= 0 for full context else the number of most recent
  *   tokens attended (query token included).
  * Forced additions to the classic signature:
@@ -177,6 +178,36 @@ VT_API vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* 
                                           vt_stream_t stream, int max_blocks_per_seq,
                                           int num_blocks);
 
+/*
+ * vt_paged_attn_decode_multi -- several new tokens per sequence over the same
+ * paged cache: a chunk of a prefill, or draft tokens to verify.
+ *
+ * The pages list a head_dim-128 prefill as owed (PR "perf(rocm): head_dim=128
+ * decode arm", section "Not claimed"); the reading taken: every sequence b
+ * carries q_len new tokens whose keys and values are already in its pages as
+ * the last q_len of its L = context_lens[b] tokens.  New token j
+ * (0 <= j < q_len), at position L - q_len + j, attends with the decode's
+ * arithmetic to the tokens t with
+ *   t0_j <= t <= L - q_len + j,   t0_j = window > 0 ? max(0, L - q_len + 1 + j - window) : 0
+ * (causal within the chunk), i.e. it is the single-token decode over a
+ * context of L - q_len + 1 + j tokens.
+ *
+ * Arguments as for vt_paged_attn_decode, except:
+ *   q, out   [num_seqs][q_len][num_q_heads][head_dim] (bf16 or fp32).
+ *   q_len    >= 1 (1 is vt_paged_attn_decode); q_len * group <= 4096.
+ * The query rows of one kv head (q_len tokens x its group of query heads)
+ * share every page the head's kv tile is read for, so the cache is read once
+ * per kv head for the whole chunk.  A sequence with L < q_len gets NaN rows
+ * for all its new tokens.  dtype VT_E4M3 is VT_ERR_INVALID_ARG.
+ */
+VT_API vt_status vt_paged_attn_decode_multi(void* out, const void* q, const void* k_cache,
+                                            const void* v_cache, const int32_t* block_tables,
+                                            const int32_t* context_lens, int num_seqs, int q_len,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, float scale, int window,
+                                            vt_stream_t stream, int max_blocks_per_seq,
+                                            int num_blocks, vt_dtype dtype);
+
 /* What the last successful decode call on this host thread launched. */
 typedef struct {
   int grid_ctas;          /* CTAs launched (persistent, balanced split of the work) */
@@ -196,6 +227,7 @@ typedef struct {
   int segment_cost;       /* partition weight of a segment boundary, in tiles (vt_paged_attn_set_segment_cost) */
   int scratch_source;     /* split scratch used: 0 library-owned, 1 the caller's (vt_paged_attn_set_workspace),
                              2 the static array (vt_paged_attn_decode_noalloc) */
+  int q_len;              /* new tokens per sequence (1 except for vt_paged_attn_decode_multi) */
 } vt_plan;
 
 VT_API vt_status vt_paged_attn_last_plan(vt_plan* plan);

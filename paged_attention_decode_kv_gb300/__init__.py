@@ -21,6 +21,7 @@ VT_BF16, VT_F32, VT_E4M3 = 0, 1, 2
 BLOCK_SIZE = 32
 
 EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_decode_fp8",
+            "vt_paged_attn_decode_multi",
             "vt_paged_attn_last_plan",
             "vt_paged_attn_set_override", "vt_paged_attn_set_overlap", "vt_paged_attn_set_segment_cost",
             "vt_paged_attn_set_workspace", "vt_paged_attn_set_test_wait",
@@ -45,7 +46,7 @@ class vt_plan(ctypes.Structure):
                 ("subgroups", ctypes.c_int), ("min_units_per_cta", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
                 ("workspace_bytes", ctypes.c_size_t), ("launch_overlap", ctypes.c_int),
-                ("segment_cost", ctypes.c_int), ("scratch_source", ctypes.c_int)]
+                ("segment_cost", ctypes.c_int), ("scratch_source", ctypes.c_int), ("q_len", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -76,6 +77,9 @@ def library() -> ctypes.CDLL:
             lib.vt_paged_attn_decode_fp8.argtypes = [c_void] * 8 + [c_int] * 5 + [c_float, c_int, c_void, c_int,
                                                                                    c_int]
             lib.vt_paged_attn_decode_fp8.restype = c_int
+            lib.vt_paged_attn_decode_multi.argtypes = [c_void] * 6 + [c_int] * 6 + [c_float, c_int, c_void, c_int,
+                                                                                    c_int, c_int]
+            lib.vt_paged_attn_decode_multi.restype = c_int
             lib.vt_paged_attn_last_plan.argtypes = [ctypes.POINTER(vt_plan)]
             lib.vt_paged_attn_last_plan.restype = c_int
             lib.vt_paged_attn_set_override.argtypes = [c_int, c_int]
@@ -135,6 +139,16 @@ def vt_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, context
                                                   num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                                   float(scale), int(window), stream, max_blocks_per_seq,
                                                   num_blocks, dtype)
+
+
+def vt_paged_attn_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, q_len, num_q_heads,
+                               num_kv_heads, head_dim, block_size, scale, window, stream, max_blocks_per_seq,
+                               num_blocks, dtype) -> int:
+    """Raw call of the multi-token decode (q_len new tokens per sequence,
+    causal within them); returns the status code."""
+    return library().vt_paged_attn_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                                q_len, num_q_heads, num_kv_heads, head_dim, block_size, float(scale),
+                                                int(window), stream, max_blocks_per_seq, num_blocks, dtype)
 
 
 def vt_paged_attn_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
@@ -312,4 +326,38 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
                                   context_lens.data_ptr(), B, Hq, Hkv, D, P, scale, window, _stream_handle(stream),
                                   block_tables.shape[1], nb)
     _check(st, "vt_paged_attn_decode_fp8")
+    return out
+
+
+def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale=None, window: int = 0, out=None,
+                 stream=None):
+    """Multi-token decode for torch CUDA tensors: q [B][q_len][Hq][D]; the new
+    tokens are the last q_len of each sequence's context_lens[b] cached tokens
+    and attend causally.  Returns out [B][q_len][Hq][D]."""
+    import torch
+    B, q_len, Hq, D = q.shape
+    nb, P, Hkv, D2 = k_cache.shape
+    if D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks][32][Hkv][head_dim] matching q")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("block_tables", block_tables),
+                    ("context_lens", context_lens)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
+    if scale is None:
+        scale = D ** -0.5
+    st = vt_paged_attn_decode_multi(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                    block_tables.data_ptr(), context_lens.data_ptr(), B, q_len, Hq, Hkv, D, P,
+                                    scale, window, _stream_handle(stream), block_tables.shape[1], nb,
+                                    dtype_code(q))
+    _check(st, "vt_paged_attn_decode_multi")
     return out

@@ -24,6 +24,7 @@ SOURCES = [
     "decode_d64.cu",
     "decode_d128_bf16.cu",
     "decode_d256_bf16.cu",
+    "decode_d512_bf16.cu",
     "decode_d128_f32.cu",
     "decode_d256_f32.cu",
     "decode_e4m3.cu",

@@ -61,6 +61,8 @@ constexpr int kSwizzleCols = 64; // bf16 columns per 128-byte swizzled sub-tile 
 // GB300's 2.07 GHz maximum, 2^31 cycles is about 1 s and 2^28 about 0.13 s).
 constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr long long kDrainLimitCycles = 1ll << 28;
+// Page tiles of its slice a CTA prefetches into L2 before its dependency wait.
+constexpr int kPrefetchTiles = 8;
 
 // Stage flags written by the producer.
 enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8, kEnd = 16 };  // kEnd: no more tiles
@@ -82,9 +84,11 @@ struct DecodeArgs {
   const int* context_lens;
   int num_seqs;
   int num_q_heads;
+  int q_len;        // new tokens per sequence (1: single-token decode)
+  int rows;         // query rows per kv head: q_len * group
   int num_kv_heads;
   int group;        // num_q_heads / num_kv_heads
-  int subgroups;    // ceil(group / group tile)
+  int subgroups;    // ceil(rows / group tile)
   int max_blocks;   // block-table row stride
   int num_blocks;   // pool size in pages
   int window;       // <= 0: none
@@ -116,7 +120,8 @@ struct DecodeArgs {
 struct StageHeader {
   int b;        // sequence
   int vh;       // virtual kv head = h * subgroups + sub
-  int lo, hi;   // valid token slots [lo, hi) of this page
+  int lo, hi;   // token slots [lo, hi) of this page attended by some query row
+  int rel_end;  // context length minus the page's first token (may exceed 32)
   int flags;
   int gq;       // live query rows of this virtual head (<= G)
   int nsplit;   // CTAs sharing this (sequence, virtual head)
@@ -153,6 +158,12 @@ struct Smem {
   alignas(1024) KvElem<T, M> k[NSTAGE][kPageTokens * D];
   alignas(1024) KvElem<T, M> v[NSTAGE][kPageTokens * D];
   alignas(128) T q[NSTAGE][G * D];
+  // head_dim 512 (bf16 tensor cores): the Q^T fragments of 32 k-steps do not
+  // fit in registers, so the segment's query rows are copied into this
+  // buffer ([head_dim / 64][G][64 columns], 128-byte swizzle) and read with
+  // ldmatrix per k-step pair.
+  static constexpr bool QS = (M == Math::kMma) && D >= 512;
+  alignas(1024) T qs[QS ? G * D : 8];
   // Tensor-core epilogue: warps of token half 1 hand their O^T accumulator
   // fragments to the warps of token half 0 ([segment parity][dp][m-tile][lane]);
   // token half 0 then reuses its slice to stage rows for coalesced stores.
@@ -173,7 +184,7 @@ struct Smem {
   alignas(8) unsigned long long full[NSTAGE];
   unsigned long long empty[NSTAGE];
   unsigned long long csync;
-  unsigned long long comb;  // partials staged for a combine
+  unsigned long long comb[2];  // partials staged for a combine (two ring halves)
   long long scan[16];
   int b_start_s;
   long long cum_start_s;
@@ -237,6 +248,18 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
       : "memory");
+}
+
+// L2 prefetch of a tensor box (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
 }
 
 // Plain bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned).
@@ -458,6 +481,13 @@ struct Partition {
   }
 };
 
+// Row of q / out (in rows of head_dim elements) for query row r of kv head h
+// of sequence b: r = j * group + i is head h * group + i of new token j.
+__device__ __forceinline__ size_t q_row(const DecodeArgs& a, int b, int h, int r) {
+  const int j = r / a.group, i = r - j * a.group;
+  return (static_cast<size_t>(b) * a.q_len + j) * a.num_q_heads + h * a.group + i;
+}
+
 struct SeqSpan {
   int p_lo;   // first page touched
   int np;     // pages touched (0: nothing to do)
@@ -466,15 +496,21 @@ struct SeqSpan {
   bool bad;   // context length invalid
 };
 
-__device__ __forceinline__ SeqSpan seq_span(int L, int window, int max_blocks) {
+// Pages a sequence's query rows attend: with q_len new tokens (the last
+// q_len of the context), token j sees the first L - q_len + 1 + j tokens and
+// the window counts back from there, so the union starts at the first
+// token's window.  A context shorter than q_len > 1 is invalid.
+__device__ __forceinline__ SeqSpan seq_span(int L, int window, int max_blocks, int q_len) {
   SeqSpan s;
   s.L = L;
-  s.bad = (L < 0) || (static_cast<long long>(L) > static_cast<long long>(max_blocks) * kPageTokens);
+  s.bad = (L < 0) || (static_cast<long long>(L) > static_cast<long long>(max_blocks) * kPageTokens) ||
+          (q_len > 1 && L < q_len);
   if (s.bad || L == 0) {
     s.p_lo = 0; s.np = 0; s.t0 = 0;
     return s;
   }
-  s.t0 = (window > 0 && L > window) ? L - window : 0;
+  const int first_end = L - q_len + 1;  // context of the first new token
+  s.t0 = (window > 0 && first_end > window) ? first_end - window : 0;
   s.p_lo = s.t0 / kPageTokens;
   s.np = (L + kPageTokens - 1) / kPageTokens - s.p_lo;
   return s;
@@ -509,6 +545,162 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 }
 
 // ---------------------------------------------------------------------------
+// S8: the deferred LSE combines a CTA owes, run by its consumer warps after
+// their last tile.  A separate (not inlined) function, so its registers are
+// allocated apart from the tile loop's.
+// ---------------------------------------------------------------------------
+template <int D, typename T, int G, int NCW, int NSTAGE, Math MATH>
+__device__ __noinline__ void combine_pending(Smem<D, T, G, NCW, NSTAGE, MATH>& s, const DecodeArgs& a,
+                                            const Partition part, const int prec, uint32_t& sync_phase) {
+  using KV = KvElem<T, MATH>;
+  constexpr int NC = NCW * 32;
+  const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
+  const float kNegInf = -__int_as_float(0x7f800000);
+  auto cons_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.csync);
+    bool r = wait_phase(&s.csync, sync_phase, &s.abort_flag, a.status, kStatusSync, a.wait_limit);
+    r = __all_sync(0xffffffffu, r);
+    sync_phase ^= 1u;
+    return r;
+  };
+  const int n_pend = s.pend_n;
+  float* const ring = reinterpret_cast<float*>(&s.k[0][0]);
+  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(KV);
+  constexpr size_t kHalfFloats = kRingBytes / 8;  // floats in one half of the ring
+  constexpr int kRowChunks = D / 4;  // float4 chunks of a row
+  constexpr int kOwn = (G * kRowChunks + NC - 1) / NC;
+  static_assert(kHalfFloats >= static_cast<size_t>(G) * (4 + D), "half the ring must hold a partial record");
+  uint32_t comb_phases = 0u;  // bit b: phase parity of ring half b
+  for (int pi = 0; pi < n_pend; ++pi) {
+    const PendingCombine pc = s.pend[pi];
+    const int h = pc.vh / a.subgroups, sub = pc.vh - h * a.subgroups;
+    const int r0 = sub * G;  // first query row of this subgroup
+    const int gq = pc.gq;
+    const int c_first = pc.c_first;
+    // The k-th CTA sharing the item left its partial in first-segment slot
+    // c_first + k, except the first CTA when the item starts inside its slice
+    // (last-segment slot grid + c_first).
+    const bool first_last = part.start(c_first) < pc.item_u;
+    const int rec = prec;
+    const uint32_t rec_bytes = static_cast<uint32_t>(rec) * 4;
+    const int per_round = static_cast<int>(kHalfFloats * 4 / rec_bytes);
+    const int rounds = (pc.nsplit + per_round - 1) / per_round;
+    float Mrun[kOwn], Lrun[kOwn], acc[kOwn][4];
+#pragma unroll
+    for (int q = 0; q < kOwn; ++q) {
+      Mrun[q] = kNegInf;
+      Lrun[q] = 0.f;
+      acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+    }
+    if (pi > 0 && !cons_sync()) return;  // everyone is done with the previous item's rounds
+    // Iteration r merges round r (r >= 0), then issues round r + 2 into the
+    // half it frees (rounds 0 and 1 are issued by the first two iterations).
+    for (int r = -2; r < rounds; ++r) {
+      if (r >= 0) {
+      const int nk = min(per_round, pc.nsplit - r * per_round);
+      float* const buf = ring + (r & 1) * kHalfFloats;
+      bool ok = wait_phase(&s.comb[r & 1], (comb_phases >> (r & 1)) & 1u, &s.abort_flag, a.status, kStatusCombine,
+                           a.wait_limit);
+      comb_phases ^= 1u << (r & 1);
+      if (!__all_sync(0xffffffffu, ok)) return;
+#pragma unroll
+      for (int q = 0; q < kOwn; ++q) {
+        const int oc = ct + q * NC;
+        const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
+        if (i >= gq) continue;
+        const float* mlp = buf + i * 4;                  // (m, l) of row i, record stride rec
+        const float* src = buf + G * 4 + i * D + 4 * cc;  // this thread's chunk, record stride rec
+        // One pass in batches of kB partials, all loads of a batch in flight:
+        // the batch's largest m rescales what is accumulated so far.
+        constexpr int kB = 8;
+        float M = Mrun[q], l = Lrun[q], a0 = acc[q][0], a1 = acc[q][1], a2 = acc[q][2], a3 = acc[q][3];
+        for (int k = 0; k < nk; k += kB) {
+          float2 ml[kB];
+          float4 ov[kB];
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            if (k + u < nk) {
+              ml[u] = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k + u) * rec);
+              ov[u] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k + u) * rec);
+            } else {
+              ml[u] = make_float2(kNegInf, 0.f);
+              ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          float Mb = M;
+#pragma unroll
+          for (int u = 0; u < kB; ++u) Mb = fmaxf(Mb, ml[u].x);
+          const float sc = exp2f(M - Mb);  // 0 before the first partial (M = -inf)
+          M = Mb;
+          l *= sc;
+          a0 *= sc;
+          a1 *= sc;
+          a2 *= sc;
+          a3 *= sc;
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            const float w = ml[u].y * exp2f(ml[u].x - Mb);  // 0 for the padding entries
+            l += w;
+            a0 = fmaf(w, ov[u].x, a0);
+            a1 = fmaf(w, ov[u].y, a1);
+            a2 = fmaf(w, ov[u].z, a2);
+            a3 = fmaf(w, ov[u].w, a3);
+          }
+        }
+        Mrun[q] = M;
+        Lrun[q] = l;
+        acc[q][0] = a0;
+        acc[q][1] = a1;
+        acc[q][2] = a2;
+        acc[q][3] = a3;
+      }
+      }
+      // Round n: records n * per_round .. + nk - 1 into ring half n & 1.  They
+      // are one run of first-segment slots, but for record 0 when it sits in
+      // the last-segment half: two copies at most, issued by warp 0.
+      const int n = r + 2;
+      if (n < rounds) {
+        if (r >= 0 && !cons_sync()) return;  // everyone is done reading half n & 1
+        if (warp == 0) {
+          const int k0 = n * per_round, nk = min(per_round, pc.nsplit - k0);
+          float* dst = ring + (n & 1) * kHalfFloats;
+          unsigned long long* bar = &s.comb[n & 1];
+          const bool split0 = k0 == 0 && first_last;
+          if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nk) * rec_bytes);
+          __syncwarp();
+          if (lane < 2) {
+            fence_proxy_async_global();
+            const size_t g = gridDim.x;
+            if (lane == 0 && split0) bulk_load(dst, a.part + (g + c_first) * rec, rec_bytes, bar);
+            const int k_run = split0 ? 1 : 0;  // first record of the run in this round
+            if (lane == (split0 ? 1 : 0) && nk > k_run)
+              bulk_load(dst + static_cast<size_t>(k_run) * rec,
+                        a.part + static_cast<size_t>(c_first + k0 + k_run) * rec,
+                        static_cast<uint32_t>(nk - k_run) * rec_bytes, bar);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kOwn; ++q) {
+      const int oc = ct + q * NC;
+      const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
+      if (i >= gq) continue;
+      const float inv = 1.f / Lrun[q];
+      T* row = static_cast<T*>(a.out) + q_row(a, pc.b, h, r0 + i) * D + 4 * cc;
+      if constexpr (sizeof(T) == 2) {
+        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(acc[q][0] * inv, acc[q][1] * inv),
+                                                    pack_bf16(acc[q][2] * inv, acc[q][3] * inv));
+      } else {
+        *reinterpret_cast<float4*>(row) =
+            make_float4(acc[q][0] * inv, acc[q][1] * inv, acc[q][2] * inv, acc[q][3] * inv);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, typename T, int G, int NCW, int NSTAGE, int MINB, Math MATH>
@@ -520,9 +712,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int NC = NCW * 32;  // consumer threads
   using KV = KvElem<T, MATH>;
   constexpr uint32_t kTileBytes = kPageTokens * D * sizeof(KV);
-  const int prec = G * 4 + min(G, a.group) * D;  // floats of a partial record
+  const int prec = G * 4 + min(G, a.rows) * D;  // floats of a partial record
   constexpr bool kMma = MATH != Math::kSimt;
   constexpr bool kFp8 = MATH == Math::kMma8;
+  constexpr bool kQSmem = S::QS;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
                 "mma consumer shape");
   static_assert(!kFp8 || (D % 128 == 0 && (D / (NCW / 2)) % 32 == 0), "fp8 consumer shape");
@@ -545,14 +738,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   // previous kernel on the stream may still read or write `out`.
   auto fill_empty_rows = [&](int nthreads, int t) {
     for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
-      const SeqSpan sp = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks);
+      const SeqSpan sp = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks, a.q_len);
       if (sp.np != 0) continue;
       const float fill = sp.bad ? __int_as_float(0x7fc00000) : 0.f;
       float vals[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) vals[e] = fill;
-      T* row0 = static_cast<T*>(a.out) + static_cast<size_t>(b) * a.num_q_heads * D;
-      for (int e = t * 8; e < a.num_q_heads * D; e += nthreads * 8) LaneMap<T, D>::store(row0, e, vals);
+      T* row0 = static_cast<T*>(a.out) + static_cast<size_t>(b) * a.q_len * a.num_q_heads * D;
+      for (int e = t * 8; e < a.q_len * a.num_q_heads * D; e += nthreads * 8) LaneMap<T, D>::store(row0, e, vals);
     }
   };
 
@@ -562,7 +755,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       mbar_init(&s.empty[st], NCW);
     }
     mbar_init(&s.csync, NCW);  // one arrival per consumer warp
-    mbar_init(&s.comb, 1);
+    mbar_init(&s.comb[0], 1);
+    mbar_init(&s.comb[1], 1);
     s.abort_flag = 0;
     s.b_start_s = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -580,7 +774,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int kWeightMinTiles = 4;
   const bool weighable = static_cast<long long>(a.num_seqs) * nvh <= kItemMask;
   auto packed_units = [&](int b) -> long long {
-    const int np = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks).np;
+    const int np = seq_span(__ldg(a.context_lens + b), a.window, a.max_blocks, a.q_len).np;
     if (np <= 0) return 0;
     return (static_cast<long long>(np) * nvh << kItemBits) + (weighable ? nvh : 0);
   };
@@ -660,7 +854,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     bool withheld = false;
     long long covered = 0;  // units walked, for the self-check
     while (ok && u < u1) {
-      const SeqSpan sp = seq_span(length_of(b), a.window, a.max_blocks);
+      const SeqSpan sp = seq_span(length_of(b), a.window, a.max_blocks, a.q_len);
       const int w = sp.np + X;  // units of one (sequence, virtual head) item
       const long long ub = static_cast<long long>(w) * nvh;
       long long off = u - cum;
@@ -681,8 +875,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         // first-segment slots, then last-segment slots (the item starts inside our slice)
         const int slot = static_cast<int>(blockIdx.x) + (u0 < item_u ? static_cast<int>(gridDim.x) : 0);
         const int h = vh / a.subgroups, sub = vh - h * a.subgroups;
-        const int q_row0 = h * a.group + sub * G;
-        const int gq = min(G, a.group - sub * G);
+        const int qr0 = sub * G;  // first query row of this subgroup
+        const int gq = min(G, a.rows - qr0);
         const int* bt_row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + sp.p_lo;
         for (int p0 = pa; ok && p0 < pb; p0 += 32) {
           const int my_p = p0 + lane;
@@ -690,7 +884,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           // q, K and V may be written by the previous kernel on the stream;
           // the first copies wait for it (context lengths and block tables
           // were read before: the caller keeps them unchanged across it).
-          if (issued == 0) grid_dependency_wait();
+          // Before waiting, the first pages of the slice are prefetched into
+          // L2, so their HBM latency overlaps that kernel's tail.  L2 is the
+          // point of coherence: the copies after the wait still see every
+          // write the previous kernel made.
+          if (issued == 0) {
+            const int n_pf = min(min(pb - p0, kPrefetchTiles), 32);
+            if (lane < n_pf && my_id >= 0 && my_id < a.num_blocks) {
+              if constexpr (kMma) {
+                tma_prefetch_4d(&tmap_k, 0, my_id * kPageTokens, 0, h);
+                tma_prefetch_4d(&tmap_v, 0, my_id * kPageTokens, 0, h);
+              } else {
+                tma_prefetch_3d(&tmap_k, 0, h, my_id * kPageTokens);
+                tma_prefetch_3d(&tmap_v, 0, h, my_id * kPageTokens);
+              }
+            }
+            grid_dependency_wait();
+          }
           const int n = min(32, pb - p0);
           for (int jj = 0; jj < n; ++jj) {
             const int pid = __shfl_sync(0xffffffffu, my_id, jj);
@@ -711,6 +921,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               hd.vh = vh;
               hd.lo = max(sp.t0 - first_tok, 0);
               hd.hi = min(sp.L - first_tok, kPageTokens);
+              hd.rel_end = sp.L - first_tok;
               hd.flags = (p == pa ? kFirst : 0) | (p == pb - 1 ? kLast : 0) | (nsplit > 1 ? kSplit : 0) |
                          (bad ? kBadPage : 0);
               hd.gq = gq;
@@ -735,9 +946,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               else
                 tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, 0, h, pid * kPageTokens, &s.full[stage]);
             }
-            if (p == pa && lane == 31) {
-              const T* qsrc = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.num_q_heads + q_row0) * D;
-              bulk_load(s.q[stage], qsrc, static_cast<uint32_t>(gq) * D * sizeof(T), &s.full[stage]);
+            if (p == pa && lane >= 16) {
+              // The subgroup's rows, one bulk copy per new token they cover
+              // (one copy in all for single-token decode).
+              const int j = qr0 / a.group + (lane - 16);
+              const int lo = max(j * a.group, qr0), hi = min(j * a.group + a.group, qr0 + gq);
+              if (hi > lo) {
+                const T* qsrc = static_cast<const T*>(a.q) + q_row(a, b, h, lo) * D;
+                bulk_load(s.q[stage] + (lo - qr0) * D, qsrc, static_cast<uint32_t>(hi - lo) * D * sizeof(T),
+                          &s.full[stage]);
+              }
             }
             __syncwarp();
             ++issued;
@@ -753,7 +971,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       // next sequence with work
       do {
         ++b;
-      } while (ok && u < u1 && b < a.num_seqs && seq_span(length_of(b), a.window, a.max_blocks).np == 0);
+      } while (ok && u < u1 && b < a.num_seqs && seq_span(length_of(b), a.window, a.max_blocks, a.q_len).np == 0);
       if (b >= a.num_seqs) break;
     }
     // Self-check: the walk must have covered exactly this CTA's slice.
@@ -842,11 +1060,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   while (alive && more) {
   float qf[kMma ? 1 : G][8];
   float acc[kMma ? 1 : G][8];
-  uint32_t qb[kMma ? kKSteps : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
+  uint32_t qb[kMma && !kQSmem ? kKSteps : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
   float oacc[kMma ? kMt : 1][NQT][4];       // O^T accumulators
   float m_run = kNegInf, l_run = 0.f;       // simt: the lane's query
   float sl2 = a.scale_log2;                 // score factor into the log2 domain (fp8: times k_scale[h])
   float vsc = 1.f;                          // value factor (fp8: v_scale[h])
+  // Causal offset of a query row's new token: q_len - 1 - j (0 for
+  // single-token decode); its keys end that many tokens before the context's.
+  int qoff[kMma ? NQT : 1][2];              // mma: queries 8n + 2tig + {0,1}; simt: [0][0] is the lane's
   float mq[NQT][2], lq[NQT][2];             // mma: queries 8n + 2tig + {0,1}
   bool poison = false;
   int hold_stage = 0;
@@ -887,10 +1108,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         m_run = kNegInf;
         l_run = 0.f;
         poison = false;
+        qoff[0][0] = a.q_len - 1 - ((hd.vh % a.subgroups) * G + iq) / a.group;
       }
       if (hd.flags & kBadPage) {
         poison = true;
       } else {
+        const int end_q = hd.rel_end - qoff[0][0];                      // keys t < end_q
+        const int beg_q = a.window > 0 ? end_q - a.window : -(1 << 30);  // and t >= beg_q
         const T* ks = s.k[stage];
         const T* vs = s.v[stage];
         float sc[TPG];
@@ -908,7 +1132,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             part_s[i] = sum;
           }
           const float r = group_reduce_scatter<G, GS>(part_s, c);
-          sc[tt] = (t >= hd.lo && t < hd.hi) ? r : kNegInf;
+          sc[tt] = (t >= hd.lo && t < hd.hi && t >= beg_q && t < end_q) ? r : kNegInf;
         }
         float mloc = sc[0];
 #pragma unroll
@@ -983,6 +1207,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               qb[ks][n][1] = bf16x2_to_f16x2(w.y);
             }
           }
+        } else if constexpr (kQSmem) {
+          // Every consumer warp is past the previous segment's epilogue
+          // rendezvous, so nobody reads the buffer any more: copy the rows in
+          // 16-byte chunks (rows past the live group are zero), then meet.
+          char* qs = reinterpret_cast<char*>(s.qs);
+          const T* src = s.q[stage];
+          for (int e = ct; e < G * (D / 8); e += NC) {
+            const int row = e / (D / 8), c8 = e - row * (D / 8);
+            const uint4 val = row < hd.gq ? *reinterpret_cast<const uint4*>(src + row * D + c8 * 8)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(qs + (c8 >> 3) * (G * 128) + row * 128 + (((c8 & 7) ^ (row & 7)) << 4)) = val;
+          }
+          if (!cons_sync()) {
+            alive = false;
+            break;
+          }
         } else {
 #pragma unroll
           for (int n = 0; n < NQT; ++n) {
@@ -1006,6 +1246,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         for (int n = 0; n < NQT; ++n) {
           mq[n][0] = mq[n][1] = kNegInf;
           lq[n][0] = lq[n][1] = 0.f;
+#pragma unroll
+          for (int jq = 0; jq < 2; ++jq)
+            qoff[n][jq] = a.q_len - 1 - ((hd.vh % a.subgroups) * G + 8 * n + 2 * tig + jq) / a.group;
         }
         poison = false;
       }
@@ -1047,6 +1290,33 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               for (int n = 0; n < NQT; ++n) mma_f16(sacc[n][half], ak, qb[ks][n][0], qb[ks][n][1]);
             }
           }
+        } else if constexpr (kQSmem) {
+          // Q^T B fragments by ldmatrix from the swizzled copy: matrices
+          // (queries 8n..+7) x (columns 16ks, 16ks + 8, 16ks + 16, 16ks + 24)
+          // give b0b1 / b2b3 of k-steps ks and ks + 1.
+          const int mi = lane >> 3, r = lane & 7;
+          const int t = 16 * tg + ((mi & 1) << 3) + r;
+          const uint32_t qbase = smem_addr(s.qs);
+#pragma unroll 4
+          for (int ks = 0; ks < kKSteps; ks += 2) {
+            uint32_t qf[NQT][4];
+#pragma unroll
+            for (int n = 0; n < NQT; ++n) {
+              const int row = 8 * n + r;
+              const int d = ks * 16 + ((mi & 1) << 3) + ((mi >> 1) << 4);
+              ldmatrix_x4(qbase + (d / kSwizzleCols) * (G * 128) + row * 128 + ((((d % kSwizzleCols) >> 3) ^ (row & 7)) << 4),
+                          qf[n]);
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int d = (ks + h2) * 16 + ((mi >> 1) << 3);
+              const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
+              uint32_t ak[4];
+              ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
+#pragma unroll
+              for (int n = 0; n < NQT; ++n) mma_bf16(sacc[n][h2], ak, qf[n][2 * h2], qf[n][2 * h2 + 1]);
+            }
+          }
         } else {
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;  // token row this lane addresses
@@ -1063,8 +1333,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         // S4 + S5: mask and scale; online softmax per query column.  Lane
         // holds tokens 16tg + gid (values 0, 1) and + 8 (values 2, 3) of
         // queries 8n + 2tig (values 0, 2) and + 1 (values 1, 3).
+        // Query row q of new token j sees the page's tokens t with
+        // beg <= t < end, end = rel_end - (q_len - 1 - j), beg = end - window
+        // (for single-token decode exactly [lo, hi)).
         const int t_lo = 16 * tg + gid, t_hi = t_lo + 8;
-        const bool tok_lo = t_lo >= hd.lo && t_lo < hd.hi, tok_hi = t_hi >= hd.lo && t_hi < hd.hi;
+        const int wlim = a.window > 0 ? a.window : (1 << 30);
         float pr[NQT][4];
         float al[NQT][2];
         bool moved = false;
@@ -1074,6 +1347,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           for (int jq = 0; jq < 2; ++jq) {
             const int q = 8 * n + 2 * tig + jq;
             const bool qok = q < hd.gq;
+            const int end = hd.rel_end - qoff[n][jq], beg = end - wlim;
+            const bool tok_lo = t_lo >= beg && t_lo < end, tok_hi = t_hi >= beg && t_hi < end;
             const float s_lo = (qok && tok_lo) ? (sacc[n][0][jq] + sacc[n][1][jq]) * sl2 : kNegInf;
             const float s_hi = (qok && tok_hi) ? (sacc[n][0][jq + 2] + sacc[n][1][jq + 2]) * sl2 : kNegInf;
             float mx = fmaxf(s_lo, s_hi);
@@ -1110,6 +1385,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
                              ((tl + 1 >= hd.lo && tl + 1 < hd.hi) ? 0xffff0000u : 0u);
         const uint32_t mhi = ((tl + 8 >= hd.lo && tl + 8 < hd.hi) ? 0x0000ffffu : 0u) |
                              ((tl + 9 >= hd.lo && tl + 9 < hd.hi) ? 0xffff0000u : 0u);
+        const bool full_page = hd.lo == 0 && hd.hi == kPageTokens;  // no token to clear
         if constexpr (kFp8) {
           // P^T as an f16 B operand (11 significant bits of each weight),
           // transposed from the S^T accumulator layout with movmatrix.
@@ -1141,8 +1417,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               const uint32_t sel = half ? 0x7362u : 0x5140u;
               const uint32_t lo_pair = __byte_perm(w[0], w[1], sel);  // tokens 2tig, 2tig + 1
               const uint32_t hi_pair = __byte_perm(w[2], w[3], sel);  // tokens 2tig + 8, + 9
-              const uint32_t av[4] = {e4m3x2_to_f16x2(lo_pair) & mlo, e4m3x2_to_f16x2(lo_pair >> 16) & mlo,
-                                      e4m3x2_to_f16x2(hi_pair) & mhi, e4m3x2_to_f16x2(hi_pair >> 16) & mhi};
+              uint32_t av[4] = {e4m3x2_to_f16x2(lo_pair), e4m3x2_to_f16x2(lo_pair >> 16), e4m3x2_to_f16x2(hi_pair),
+                                e4m3x2_to_f16x2(hi_pair >> 16)};
+              if (!full_page) {
+                av[0] &= mlo;
+                av[1] &= mlo;
+                av[2] &= mhi;
+                av[3] &= mhi;
+              }
 #pragma unroll
               for (int n = 0; n < NQT; ++n) mma_f16(oacc[2 * cb + half][n], av, pb[n][0], pb[n][1]);
             }
@@ -1172,10 +1454,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
             uint32_t av[4];
             ldmatrix_x4_trans(vbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), av);
-            av[0] &= mlo;
-            av[1] &= mlo;
-            av[2] &= mhi;
-            av[3] &= mhi;
+            if (!full_page) {
+              av[0] &= mlo;
+              av[1] &= mlo;
+              av[2] &= mhi;
+              av[3] &= mhi;
+            }
 #pragma unroll
             for (int n = 0; n < NQT; ++n) {
               mma_bf16(oacc[mt][n], av, pbh[n][0], pbh[n][1]);
@@ -1203,7 +1487,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 
   // ---- end of a (sequence, virtual head) segment ----------------------------
   const int h = hd.vh / a.subgroups, sub = hd.vh - h * a.subgroups;
-  const int q_row0 = h * a.group + sub * G;
+  const int r0 = sub * G;  // first query row of this subgroup
   const bool split = (hd.flags & kSplit) != 0;
   // red_m / red_l / xbuf are double-buffered: a thread can only reach the next
   // segment but one after every thread finished reading this segment's copy.
@@ -1277,7 +1561,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       for (int e = 0; e < 8; ++e) val[e] /= L;
       if (i >= hd.gq) continue;
       if (!split) {
-        T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + i) * D;
+        T* row = static_cast<T*>(a.out) + q_row(a, hd.b, h, r0 + i) * D;
         LaneMap<T, D>::store(row, d0, val);
       } else {
         float* po = a.part + static_cast<size_t>(hd.slot) * prec + G * 4 + i * D + d0;
@@ -1390,7 +1674,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           // bf16: two neighbouring float4 chunks make one 16-byte store
           if ((c4 & 1) == 0) {
             const float4 w4 = *reinterpret_cast<const float4*>(xb + q * kDPart + 4 * c4 + 4);
-            T* row = static_cast<T*>(a.out) + (static_cast<size_t>(hd.b) * a.num_q_heads + q_row0 + q) * D + d;
+            T* row = static_cast<T*>(a.out) + q_row(a, hd.b, h, r0 + q) * D + d;
             *reinterpret_cast<uint4*>(row) = make_uint4(pack_bf16(v4.x, v4.y), pack_bf16(v4.z, v4.w),
                                                         pack_bf16(w4.x, w4.y), pack_bf16(w4.z, w4.w));
           }
@@ -1420,131 +1704,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 
   // ===================== S8: deferred LSE combines ============================
   // Run after this CTA consumed all its tiles, so the stage ring is free.  An
-  // item's partials are one run of records (see DecodeArgs::part): one or two
-  // bulk copies stage a round of them.  Each thread then merges its 4-column
-  // chunks, weighting every partial by l * 2^(m - M).
+  // item's partials are one run of records (see DecodeArgs::part), staged by
+  // bulk copies in rounds that alternate between the two halves of the ring:
+  // the next round's copy is in flight while the current one is merged.  Each
+  // thread merges its 4-column chunks, weighting every partial by
+  // l * 2^(m - M).
   if (!alive) return;
   if (!cons_sync()) return;  // pend_n was written by thread 0
-  const int n_pend = s.pend_n;
-  float* const ring = reinterpret_cast<float*>(&s.k[0][0]);
-  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(KV);
-  constexpr int kRowChunks = D / 4;  // float4 chunks of a row
-  constexpr int kOwn = (G * kRowChunks + NC - 1) / NC;
-  uint32_t comb_phase = 0;
-  for (int pi = 0; pi < n_pend; ++pi) {
-    const PendingCombine pc = s.pend[pi];
-    const int h = pc.vh / a.subgroups, sub = pc.vh - h * a.subgroups;
-    const int q_row0 = h * a.group + sub * G;
-    const int gq = pc.gq;
-    const int c_first = pc.c_first;
-    // The k-th CTA sharing the item left its partial in first-segment slot
-    // c_first + k, except the first CTA when the item starts inside its slice
-    // (last-segment slot grid + c_first).
-    const bool first_last = part.start(c_first) < pc.item_u;
-    const int rec = prec;
-    const uint32_t rec_bytes = static_cast<uint32_t>(rec) * 4;
-    const int per_round = static_cast<int>(kRingBytes / rec_bytes);
-    float Mrun[kOwn], Lrun[kOwn], acc[kOwn][4];
-#pragma unroll
-    for (int q = 0; q < kOwn; ++q) {
-      Mrun[q] = kNegInf;
-      Lrun[q] = 0.f;
-      acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-    }
-    for (int k0 = 0; k0 < pc.nsplit; k0 += per_round) {
-      const int nk = min(per_round, pc.nsplit - k0);
-      if (k0 > 0 || pi > 0) {
-        if (!cons_sync()) return;  // everyone is done reading the ring
-      }
-      if (warp == 0) {
-        // records k0 .. k0 + nk - 1 are one run of first-segment slots, but
-        // for record 0 when it sits in the last-segment half: two copies at most
-        const bool split0 = k0 == 0 && first_last;
-        if (lane == 0) mbar_arrive_expect_tx(&s.comb, static_cast<uint32_t>(nk) * rec_bytes);
-        __syncwarp();
-        if (lane < 2) {
-          fence_proxy_async_global();
-          const size_t g = gridDim.x;
-          if (lane == 0 && split0)
-            bulk_load(ring, a.part + (g + c_first) * rec, rec_bytes, &s.comb);
-          const int k_run = split0 ? 1 : 0;  // first record of the run in this round
-          if (lane == (split0 ? 1 : 0) && nk > k_run)
-            bulk_load(ring + static_cast<size_t>(k_run) * rec,
-                      a.part + static_cast<size_t>(c_first + k0 + k_run) * rec,
-                      static_cast<uint32_t>(nk - k_run) * rec_bytes, &s.comb);
-        }
-      }
-      bool ok = wait_phase(&s.comb, comb_phase, &s.abort_flag, a.status, kStatusCombine, a.wait_limit);
-      comb_phase ^= 1u;
-      if (!__all_sync(0xffffffffu, ok)) return;
-#pragma unroll
-      for (int q = 0; q < kOwn; ++q) {
-        const int oc = ct + q * NC;
-        const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
-        if (i >= gq) continue;
-        const float* mlp = ring + i * 4;                  // (m, l) of row i, record stride rec
-        const float* src = ring + G * 4 + i * D + 4 * cc;  // this thread's chunk, record stride rec
-        // One pass in batches of kB partials, all loads of a batch in flight:
-        // the batch's largest m rescales what is accumulated so far.
-        constexpr int kB = 8;
-        float M = Mrun[q], l = Lrun[q], a0 = acc[q][0], a1 = acc[q][1], a2 = acc[q][2], a3 = acc[q][3];
-        for (int k = 0; k < nk; k += kB) {
-          float2 ml[kB];
-          float4 ov[kB];
-#pragma unroll
-          for (int u = 0; u < kB; ++u) {
-            if (k + u < nk) {
-              ml[u] = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k + u) * rec);
-              ov[u] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k + u) * rec);
-            } else {
-              ml[u] = make_float2(kNegInf, 0.f);
-              ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-          }
-          float Mb = M;
-#pragma unroll
-          for (int u = 0; u < kB; ++u) Mb = fmaxf(Mb, ml[u].x);
-          const float sc = exp2f(M - Mb);  // 0 before the first partial (M = -inf)
-          M = Mb;
-          l *= sc;
-          a0 *= sc;
-          a1 *= sc;
-          a2 *= sc;
-          a3 *= sc;
-#pragma unroll
-          for (int u = 0; u < kB; ++u) {
-            const float w = ml[u].y * exp2f(ml[u].x - Mb);  // 0 for the padding entries
-            l += w;
-            a0 = fmaf(w, ov[u].x, a0);
-            a1 = fmaf(w, ov[u].y, a1);
-            a2 = fmaf(w, ov[u].z, a2);
-            a3 = fmaf(w, ov[u].w, a3);
-          }
-        }
-        Mrun[q] = M;
-        Lrun[q] = l;
-        acc[q][0] = a0;
-        acc[q][1] = a1;
-        acc[q][2] = a2;
-        acc[q][3] = a3;
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kOwn; ++q) {
-      const int oc = ct + q * NC;
-      const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
-      if (i >= gq) continue;
-      const float inv = 1.f / Lrun[q];
-      T* row = static_cast<T*>(a.out) + (static_cast<size_t>(pc.b) * a.num_q_heads + q_row0 + i) * D + 4 * cc;
-      if constexpr (sizeof(T) == 2) {
-        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(acc[q][0] * inv, acc[q][1] * inv),
-                                                    pack_bf16(acc[q][2] * inv, acc[q][3] * inv));
-      } else {
-        *reinterpret_cast<float4*>(row) =
-            make_float4(acc[q][0] * inv, acc[q][1] * inv, acc[q][2] * inv, acc[q][3] * inv);
-      }
-    }
-  }
+  combine_pending<D, T, G, NCW, NSTAGE, MATH>(s, a, part, prec, sync_phase);
 }
 
 }  // namespace vt

@@ -82,6 +82,7 @@ const VariantInfo* variants_d64_bf16(int* count);
 const VariantInfo* variants_d64_f32(int* count);
 const VariantInfo* variants_d128_bf16(int* count);
 const VariantInfo* variants_d256_bf16(int* count);
+const VariantInfo* variants_d512_bf16(int* count);
 const VariantInfo* variants_d128_f32(int* count);
 const VariantInfo* variants_d256_f32(int* count);
 const VariantInfo* variants_d128_e4m3(int* count);

@@ -60,6 +60,7 @@ const VariantInfo* find_variant(int head_dim, vt_dtype dtype, int group_tile) {
   if (head_dim == 64 && dtype == VT_F32) table = vt::variants_d64_f32(&n);
   if (head_dim == 128 && dtype == VT_BF16) table = vt::variants_d128_bf16(&n);
   if (head_dim == 256 && dtype == VT_BF16) table = vt::variants_d256_bf16(&n);
+  if (head_dim == 512 && dtype == VT_BF16) table = vt::variants_d512_bf16(&n);
   if (head_dim == 128 && dtype == VT_F32) table = vt::variants_d128_f32(&n);
   if (head_dim == 256 && dtype == VT_F32) table = vt::variants_d256_f32(&n);
   if (head_dim == 128 && dtype == VT_E4M3) table = vt::variants_d128_e4m3(&n);
@@ -71,10 +72,11 @@ const VariantInfo* find_variant(int head_dim, vt_dtype dtype, int group_tile) {
 
 // Query rows computed per kv head and CTA.  bf16 runs on tensor cores with
 // the queries as the N dimension of m16n8k16: one tile of 8 (or 16) rows
-// covers any group up to that size.  fp32 runs on CUDA cores, where every
-// padded row costs FMAs: the next power of two, at most 8.
-int group_tile_for(int group, vt_dtype dtype) {
-  if (dtype != VT_F32) return group <= 8 ? 8 : 16;
+// covers any group up to that size (head_dim 512: 8, larger groups become
+// query subgroups).  fp32 runs on CUDA cores, where every padded row costs
+// FMAs: the next power of two, at most 8.
+int group_tile_for(int group, vt_dtype dtype, int head_dim) {
+  if (dtype != VT_F32) return (group <= 8 || head_dim >= 512) ? 8 : 16;
   int g = 1;
   while (g < group && g < kMaxGroupTile) g <<= 1;
   return g;
@@ -263,6 +265,11 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
   const cuuint64_t tokens = static_cast<cuuint64_t>(k.num_blocks) * vt::kPageTokens;
   const cuuint64_t row = static_cast<cuuint64_t>(k.head_dim) * k.num_kv_heads * es;  // bytes per token
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  // L2 promotion no wider than one head's token row: a 128-byte row (FP8 at
+  // head_dim 128, bf16 at 64) promoted to 256 bytes would also pull the next
+  // kv head's row, which another CTA reads at another time.
+  const CUtensorMapL2promotion promo =
+      static_cast<size_t>(k.head_dim) * es <= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   CUtensorMap m;
   CUresult r;
   if (k.dtype == VT_E4M3) {
@@ -275,7 +282,7 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
     const cuuint32_t box[4] = {static_cast<cuuint32_t>(kCols), static_cast<cuuint32_t>(vt::kPageTokens),
                                static_cast<cuuint32_t>(k.head_dim / kCols), 1u};
     r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(k.ptr), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else if (k.dtype == VT_BF16) {
     // Tensor-core consumer: a 4-D view (64 columns, token, column block, kv
@@ -290,7 +297,7 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
     const cuuint32_t box[4] = {static_cast<cuuint32_t>(vt::kSwizzleCols), static_cast<cuuint32_t>(vt::kPageTokens),
                                static_cast<cuuint32_t>(k.head_dim / vt::kSwizzleCols), 1u};
     r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k.ptr), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     // CUDA-core consumer: a 3-D view (column, kv head, token) and one
@@ -299,7 +306,7 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(k.head_dim) * es, row};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(k.head_dim), 1u, static_cast<cuuint32_t>(vt::kPageTokens)};
     r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(k.ptr), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, promo,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
   if (r != CUDA_SUCCESS) {
@@ -335,12 +342,13 @@ struct Call {
   vt_dtype dtype;                  // K/V storage (VT_E4M3: bf16 q and out)
   const float* k_scale = nullptr;  // VT_E4M3 only: [num_kv_heads] dequantisation scales
   const float* v_scale = nullptr;
+  int q_len = 1;                   // new tokens per sequence (vt_paged_attn_decode_multi)
 };
 
 struct Plan {
   const VariantInfo* v = nullptr;
   int dev = 0, grid = 0, per_sm = 0, min_units = 0, num_sms = 0;
-  int group = 0, gt = 0, subgroups = 0;
+  int group = 0, rows = 0, gt = 0, subgroups = 0;
   long long nvh = 0;
   WsNeed need{};
 };
@@ -348,7 +356,7 @@ struct Plan {
 // Argument checks that need no device: every error returns before any
 // launch.  (num_seqs == 0 is handled by the caller as a no-op.)
 vt_status validate(const Call& c) {
-  if (c.num_seqs < 0) return VT_ERR_INVALID_ARG;
+  if (c.num_seqs < 0 || c.q_len < 1) return VT_ERR_INVALID_ARG;
   if (!c.out || !c.q || !c.k_cache || !c.v_cache || !c.block_tables || !c.context_lens) return VT_ERR_INVALID_ARG;
   if (c.dtype != VT_BF16 && c.dtype != VT_F32 && c.dtype != VT_E4M3) return VT_ERR_INVALID_ARG;
   // an FP8 cache comes with its scales, and only through vt_paged_attn_decode_fp8
@@ -362,8 +370,9 @@ vt_status validate(const Call& c) {
   if (!aligned(c.out, 16) || !aligned(c.q, 16) || !aligned(c.k_cache, 16) || !aligned(c.v_cache, 16) ||
       !aligned(c.block_tables, 4) || !aligned(c.context_lens, 4))
     return VT_ERR_INVALID_ARG;
-  if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256) return VT_ERR_UNSUPPORTED;
-  if (c.dtype == VT_E4M3 && c.head_dim == 64) return VT_ERR_UNSUPPORTED;
+  if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256 && c.head_dim != 512) return VT_ERR_UNSUPPORTED;
+  if (c.dtype == VT_E4M3 && (c.head_dim == 64 || c.head_dim == 512)) return VT_ERR_UNSUPPORTED;
+  if (c.dtype == VT_F32 && c.head_dim == 512) return VT_ERR_UNSUPPORTED;
   if (c.block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(c.num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(c.max_blocks_per_seq) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
@@ -374,8 +383,11 @@ vt_status validate(const Call& c) {
 // Caller holds g_mutex.
 vt_status make_plan(const Call& c, Plan* p) {
   p->group = c.num_q_heads / c.num_kv_heads;
-  p->gt = group_tile_for(p->group, c.dtype);
-  p->subgroups = (p->group + p->gt - 1) / p->gt;
+  const long long rows = static_cast<long long>(p->group) * c.q_len;  // query rows per kv head
+  if (rows > 4096) return VT_ERR_UNSUPPORTED;
+  p->rows = static_cast<int>(rows);
+  p->gt = group_tile_for(p->rows, c.dtype, c.head_dim);
+  p->subgroups = (p->rows + p->gt - 1) / p->gt;
   p->nvh = static_cast<long long>(c.num_kv_heads) * p->subgroups;
   if (p->nvh * c.num_seqs > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;
   p->v = find_variant(c.head_dim, c.dtype, p->gt);
@@ -416,6 +428,8 @@ vt_status launch(const Call& c, const Plan& p, char* base, size_t counters_regio
   args.num_seqs = c.num_seqs;
   args.num_q_heads = c.num_q_heads;
   args.num_kv_heads = c.num_kv_heads;
+  args.q_len = c.q_len;
+  args.rows = p.rows;
   args.group = p.group;
   args.subgroups = p.subgroups;
   args.max_blocks = c.max_blocks_per_seq;
@@ -450,6 +464,7 @@ vt_status launch(const Call& c, const Plan& p, char* base, size_t counters_regio
   r.launch_overlap = g_overlap ? 1 : 0;
   r.segment_cost = args.seg_cost;
   r.scratch_source = scratch_source;
+  r.q_len = c.q_len;
   g_have_plan = true;
   return VT_OK;
 }
@@ -460,7 +475,7 @@ Call make_call(void* out, const void* q, const void* k_cache, const void* v_cach
                int num_blocks, vt_dtype dtype) {
   return Call{out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
               head_dim, block_size, scale, window, reinterpret_cast<cudaStream_t>(stream), max_blocks_per_seq,
-              num_blocks, dtype, nullptr, nullptr};
+              num_blocks, dtype, nullptr, nullptr, 1};
 }
 
 // ---------------------------------------------------------------------------
@@ -553,7 +568,7 @@ size_t vt_paged_attn_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_h
                                      vt_dtype dtype) {
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
   const int group = num_q_heads / num_kv_heads;
-  const int gt = group_tile_for(group, dtype);
+  const int gt = group_tile_for(group, dtype, head_dim);
   const VariantInfo* v = find_variant(head_dim, dtype, gt);
   if (!v) return 0;
   int dev = 0;
@@ -629,6 +644,18 @@ vt_status vt_paged_attn_decode(void* out, const void* q, const void* k_cache, co
   return decode_on_workspace(make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                                        num_q_heads, num_kv_heads, head_dim, block_size, scale, window, stream,
                                        max_blocks_per_seq, num_blocks, dtype));
+}
+
+vt_status vt_paged_attn_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                                     int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                     float scale, int window, vt_stream_t stream, int max_blocks_per_seq,
+                                     int num_blocks, vt_dtype dtype) {
+  Call c = make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, window, stream, max_blocks_per_seq, num_blocks, dtype);
+  if (dtype == VT_E4M3) return VT_ERR_INVALID_ARG;
+  c.q_len = q_len;
+  return decode_on_workspace(c);
 }
 
 vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -6,8 +6,8 @@ contents, context lengths and block tables, and lays them out.
 
 The shapes follow the decode workloads the pages measure (Qwen3-family decode
 with 32-token pages, GQA groups of 2 to 8, head_dim 128 and 256), as five
-named configurations plus a batch-1 long-context case, and a head_dim 64
-batch for that arm of the library.  Recipe, per case:
+named configurations plus a batch-1 long-context case, plus batches for the
+library's other arms: head_dim 512 and 64, and FP8 (E4M3) K/V storage.  Recipe, per case:
 
 * one ``torch.Generator`` seeded with ``seed`` draws, in this order: the
   context lengths, a random permutation of the page pool, Q, K (all used
@@ -51,6 +51,7 @@ class Workload:
     peaked_head: bool = False
     table_is_permutation: bool = False
     block_size: int = BLOCK_SIZE
+    q_len: int = 1  # new tokens per sequence (> 1: multi-token decode, q is [B][q_len][Hq][D])
 
     @property
     def group(self) -> int:
@@ -117,6 +118,19 @@ D256_GQA4_F32_W1024 = _register(D256_GQA4.with_(
     name="d256_gqa4_b16_f32_w1024", dtype="f32", window=1024,
     description=D256_GQA4.description + "; fp32 storage; sliding window 1024"))
 
+# head_dim 512 arm (the pages' kernels cover head_dim 512): the d256 batch's
+# sequences and GQA-4 grouping at the wider head; 4096-page pool.
+D512_GQA4 = _register(Workload(
+    name="d512_gqa4_b16",
+    description="head_dim 512 GQA-4 decode: 16 seqs, 8 q / 2 kv heads, contexts U[512,4096]; "
+                "4096-page pool",
+    num_seqs=16, num_q_heads=8, num_kv_heads=2, head_dim=512, pool_blocks=4096,
+    contexts="uniform:512,4096", max_blocks_per_seq=128))
+
+D512_GQA4_W1024 = _register(D512_GQA4.with_(
+    name="d512_gqa4_b16_w1024", window=1024,
+    description=D512_GQA4.description + "; sliding window 1024"))
+
 # head_dim 64 arm: not a configuration of the pages (their kernels cover
 # head_dim 128, 256 and 512); the d256 batch's lengths at a Qwen-like
 # 16 q / 4 kv heads, so every (sequence, kv head) page tile is 4 KB.
@@ -165,12 +179,25 @@ LARGE_GQA_FP8 = _register(LARGE_GQA.with_(name="large_gqa8_b64_d128_fp8", dtype=
                                          description=LARGE_GQA.description + _FP8))
 SKEWED_FP8 = _register(SKEWED.with_(name="skewed_b128_gqa4_d128_fp8", dtype="e4m3",
                                    description=SKEWED.description + _FP8))
+# Multi-token decode (several new tokens per sequence: draft tokens to verify,
+# or a chunk of a prefill), attending causally within the chunk: the large
+# batch's shape at GQA 4 with 4 new tokens, so one kv head's 16 query rows
+# fill one tensor-core tile.  Not a configuration of the pages (which list a
+# head_dim-128 prefill as owed); the multi-token arm's own case.
+MULTI_Q4 = _register(Workload(
+    name="multi_q4_b64_gqa4_d128",
+    description="multi-token decode: 64 seqs x 4 new tokens, 32 q / 8 kv heads, head_dim 128, contexts "
+                "U[512,8192] (the new tokens are the last 4); 20000-page pool",
+    num_seqs=64, num_q_heads=32, num_kv_heads=8, head_dim=128, pool_blocks=20000,
+    contexts="uniform:512,8192", max_blocks_per_seq=256, q_len=4))
+
 BATCH1_LONG_FP8 = _register(BATCH1_LONG.with_(name="batch1_ctx32768_gqa4_d128_fp8", dtype="e4m3",
                                              description=BATCH1_LONG.description + _FP8))
 
 
 def custom(name: str, contexts, num_q_heads: int, num_kv_heads: int, head_dim: int,
-           dtype: str = "bf16", window: int = 0, sigma: float = 1.0, spare_pages: int = 3) -> Workload:
+           dtype: str = "bf16", window: int = 0, sigma: float = 1.0, spare_pages: int = 3,
+           q_len: int = 1) -> Workload:
     """A workload with an explicit list of context lengths (edge-case tests)."""
     contexts = [int(x) for x in contexts]
     pages = sum((L + BLOCK_SIZE - 1) // BLOCK_SIZE for L in contexts)
@@ -178,7 +205,7 @@ def custom(name: str, contexts, num_q_heads: int, num_kv_heads: int, head_dim: i
     return Workload(name=name, description=f"explicit contexts {contexts}", num_seqs=len(contexts),
                     num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                     pool_blocks=pages + spare_pages, contexts="list:" + ",".join(map(str, contexts)),
-                    max_blocks_per_seq=maxb, sigma=sigma, dtype=dtype, window=window)
+                    max_blocks_per_seq=maxb, sigma=sigma, dtype=dtype, window=window, q_len=q_len)
 
 
 def _draw_contexts(w: Workload, g: torch.Generator) -> torch.Tensor:
@@ -295,7 +322,7 @@ class PagedCase:
 
     def qo_bytes(self) -> int:
         w = self.workload
-        return 2 * w.num_seqs * w.num_q_heads * w.head_dim * w.qo_elem_bytes
+        return 2 * w.num_seqs * w.q_len * w.num_q_heads * w.head_dim * w.qo_elem_bytes
 
 
 def make_case(w: Workload, seed: int = 0) -> PagedCase:
@@ -336,6 +363,10 @@ def make_case(w: Workload, seed: int = 0) -> PagedCase:
         k, ks = _e4m3_per_head(k)
         v, vs = _e4m3_per_head(v)
         extra = {"k_scale": ks, "v_scale": vs}
+    if w.q_len > 1:
+        # multi-token decode: the queries of the q_len new tokens, drawn last
+        # so every other draw matches the single-token case of the same seed
+        q = (torch.randn((B, w.q_len, Hq, D), generator=g) * w.sigma).to(store)
     # Poison the in-page tail of every sequence's last page.
     poison = E4M3_NAN if fp8 else float("nan")
     pos = 0

@@ -62,7 +62,8 @@ def _call(**over):
     (dict(num_q_heads=12, num_kv_heads=8), vt.VT_ERR_INVALID_ARG),
     (dict(num_kv_heads=0), vt.VT_ERR_INVALID_ARG),
     (dict(head_dim=96), vt.VT_ERR_UNSUPPORTED),
-    (dict(head_dim=512), vt.VT_ERR_UNSUPPORTED),
+    (dict(head_dim=512, dtype=vt.VT_F32), vt.VT_ERR_UNSUPPORTED),
+    (dict(head_dim=1024), vt.VT_ERR_UNSUPPORTED),
     (dict(block_size=16), vt.VT_ERR_UNSUPPORTED),
     (dict(max_blocks_per_seq=0), vt.VT_ERR_INVALID_ARG),
     (dict(num_blocks=0), vt.VT_ERR_INVALID_ARG),

@@ -55,6 +55,8 @@ def run_decode(case, q, k, v, bt, cl, window=None, out=None, stream=None, scale=
     if case.fp8:
         ks, vs = case.scales(q.device)
         return vt.decode_fp8(q, k, v, ks, vs, bt, cl, scale, window, out=out, stream=stream)
+    if w.q_len > 1:
+        return vt.decode_multi(q, k, v, bt, cl, scale, window, out=out, stream=stream)
     return vt.decode(q, k, v, bt, cl, scale, window, out=out, stream=stream)
 
 
@@ -117,7 +119,8 @@ def check_case(case, dev, rows=None, **kw):
 
 # ---------------------------------------------------------------------------
 SMALL = [W.TINY, W.QWEN3_1P7B, W.D256_GQA4, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D256_GQA4_F32_W1024,
-         W.D64_GQA4, W.D64_GQA4_F32, W.QWEN3_1P7B_FP8, W.D256_GQA4_FP8, W.D256_GQA4_W1024_FP8]
+         W.D64_GQA4, W.D64_GQA4_F32, W.QWEN3_1P7B_FP8, W.D256_GQA4_FP8, W.D256_GQA4_W1024_FP8,
+         W.D512_GQA4, W.D512_GQA4_W1024]
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -148,7 +151,7 @@ def test_workload_full_size_sampled(dev, w):
 
 @pytest.mark.parametrize("grid", [1, 2, 3, 7, 64, 152, 500, 1500])
 @pytest.mark.parametrize("w", [W.QWEN3_1P7B, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D64_GQA4, W.QWEN3_1P7B_FP8,
-                               W.D256_GQA4_W1024_FP8], ids=lambda w: w.name)
+                               W.D256_GQA4_W1024_FP8, W.D512_GQA4_W1024], ids=lambda w: w.name)
 def test_forced_partitions(dev, w, grid):
     """The split/no-split paths and the combine: any CTA count (with at least
     one tile per CTA) gives the oracle's result."""
@@ -170,7 +173,7 @@ def test_page_boundary_contexts(dev, ctx):
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4), (16, 4), (20, 4), (32, 4), (48, 4), (64, 4), (6, 2)])
 @pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (128, "f32"), (64, "bf16"), (64, "f32"),
-                                     (128, "e4m3"), (256, "e4m3")])
+                                     (128, "e4m3"), (256, "e4m3"), (512, "bf16")])
 def test_group_sizes(dev, hq, hkv, d, dtype):
     """GQA groups 1..16 including ones that pad the group tile (3, 5) or need
     several query subgroups per kv head (12, 16)."""
@@ -185,6 +188,16 @@ def test_windows(dev, window, dtype):
     case = W.make_case(W.custom("win", [1, 33, 300, 1000], 16, 4, 128, dtype=dtype), 9)
     check_case(case, dev, window=window)
     check_case(case, dev, window=window, grid=11, min_units=1)
+
+
+@pytest.mark.parametrize("d", [512])
+def test_head_dim_512_page_boundary_contexts(dev, d):
+    """The head_dim 512 arm on the contexts straddling the 32-token page, with
+    and without a window, split and unsplit."""
+    case = W.make_case(W.custom(f"d{d}_straddle", list(STRADDLE), 16, 4, d), 29)
+    for window in (0, 33, 300):
+        check_case(case, dev, window=window)
+        check_case(case, dev, window=window, grid=13, min_units=1)
 
 
 @pytest.mark.parametrize("d", [128, 256])
@@ -538,3 +551,87 @@ def test_bounded_wait_gives_up_and_reports(dev, path):
         vt.vt_paged_attn_set_override(0, 0)
         if buf is not None:
             vt.vt_paged_attn_set_workspace(0, 0)
+
+
+# ---------------------------------------------------------------------------
+# Multi-token decode (q_len new tokens per sequence, causal within them)
+# ---------------------------------------------------------------------------
+def oracle_multi_rows(case, rows=None, window=None, lens=None):
+    import oracle
+    o = oracle.default_oracle()
+    w = case.workload
+    k, v, bt = case.compact()
+    cl = case.context_lens if lens is None else lens
+    if rows is None:
+        rows = [(b, j, i) for b in range(w.num_seqs) for j in range(w.q_len) for i in range(w.num_q_heads)]
+    ref = o.decode_multi_rows(rows, W.to_oracle_array(case.q), W.to_oracle_array(k), W.to_oracle_array(v),
+                              bt.numpy(), cl.numpy(), w.scale, w.window if window is None else window,
+                              threads=THREADS)
+    return np.asarray(rows), ref
+
+
+def check_multi(case, dev, rows=None, **kw):
+    out, plan = gpu_run(case, dev, **kw)
+    w = case.workload
+    assert plan["q_len"] == w.q_len and plan["head_dim"] == w.head_dim
+    assert plan["group_tile"] * plan["subgroups"] >= w.q_len * (w.num_q_heads // w.num_kv_heads)
+    idx, ref = oracle_multi_rows(case, rows, window=kw.get("window"))
+    got = out[idx[:, 0], idx[:, 1], idx[:, 2]].to(torch.float64).numpy()
+    return compare(got, ref, case.q.dtype, w.name), plan
+
+
+@pytest.mark.parametrize("q_len", [2, 3, 4, 7])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (32, 8), (8, 8), (12, 4)])
+def test_multi_token(dev, q_len, hq, hkv):
+    """Every row of a multi-token decode (new tokens j attend causally to the
+    first L - q_len + 1 + j tokens) against the oracle: contexts from exactly
+    q_len up, straddling pages; windows; split and unsplit; query rows that
+    span several tensor-core tiles (subgroups)."""
+    lens = [q_len, q_len + 1, 31, 33, 100, 685]
+    case = W.make_case(W.custom(f"multi_q{q_len}", lens, hq, hkv, 128, q_len=q_len), 30 + q_len)
+    for window in (0, 5, 64):
+        check_multi(case, dev, window=window)
+        check_multi(case, dev, window=window, grid=9, min_units=1)
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "f32"), (256, "bf16"), (64, "bf16"), (512, "bf16"), (64, "f32")])
+def test_multi_token_head_dims(dev, d, dtype):
+    case = W.make_case(W.custom(f"multi_d{d}_{dtype}", [4, 40, 300, 97], 16, 4, d, dtype=dtype, q_len=4), 31)
+    for window in (0, 50):
+        check_multi(case, dev, window=window)
+        check_multi(case, dev, window=window, grid=7, min_units=1)
+
+
+def test_multi_token_q_len_one_is_decode(dev):
+    """q_len = 1 through the multi-token entry point gives the single-token
+    decode's bits."""
+    case = W.make_case(W.QWEN3_1P7B, 32)
+    single, _ = gpu_run(case, dev)
+    k, v = case.pool(dev)
+    q = case.q.to(dev)[:, None]
+    out = vt.decode_multi(q, k, v, case.block_tables.to(dev), case.context_lens.to(dev), case.workload.scale)
+    torch.cuda.synchronize()
+    assert vt.vt_paged_attn_last_plan()["q_len"] == 1
+    assert torch.equal(out[:, 0].cpu().view(torch.int16), single.view(torch.int16))
+
+
+def test_multi_token_short_context_is_nan(dev):
+    """A context shorter than its q_len new tokens turns only that sequence's
+    rows into NaN; the other sequences are exact."""
+    case = W.make_case(W.custom("multi_short", [10, 40, 70], 8, 2, 128, q_len=4), 33)
+    lens = case.context_lens.clone()
+    lens[1] = 3
+    out, _ = gpu_run(case, dev, lens=lens)
+    assert torch.isnan(out[1].float()).all()
+    idx, ref = oracle_multi_rows(case, [(b, j, i) for b in (0, 2) for j in range(4) for i in range(8)], lens=lens)
+    compare(out[idx[:, 0], idx[:, 1], idx[:, 2]].double().numpy(), ref, torch.bfloat16)
+
+
+def test_multi_token_full_size_sampled(dev):
+    """The multi-token benchmark batch in the benchmark's launch plan, all rows
+    of sampled sequences."""
+    case = W.make_case(W.MULTI_Q4, 0)
+    L = case.context_lens.numpy()
+    pick = sorted({int(np.argmin(L)), int(np.argmax(L)), 7, 30, 55})
+    rows = [(b, j, i) for b in pick for j in range(4) for i in range(32)]
+    check_multi(case, dev, rows=rows)
