@@ -631,7 +631,10 @@ __device__ __noinline__ void combine_pending(Smem<D, T, G, NCW, NSTAGE, MATH>& s
           float Mb = M;
 #pragma unroll
           for (int u = 0; u < kB; ++u) Mb = fmaxf(Mb, ml[u].x);
-          const float sc = exp2f(M - Mb);  // 0 before the first partial (M = -inf)
+          // Mu: the batch maximum, or 0 while every partial so far is empty
+          // (m = -inf, l = 0: a multi-token row with no key in that share)
+          const float Mu = (Mb == kNegInf) ? 0.f : Mb;
+          const float sc = exp2f(M - Mu);  // 0 before the first partial (M = -inf)
           M = Mb;
           l *= sc;
           a0 *= sc;
@@ -640,7 +643,7 @@ __device__ __noinline__ void combine_pending(Smem<D, T, G, NCW, NSTAGE, MATH>& s
           a3 *= sc;
 #pragma unroll
           for (int u = 0; u < kB; ++u) {
-            const float w = ml[u].y * exp2f(ml[u].x - Mb);  // 0 for the padding entries
+            const float w = ml[u].y * exp2f(ml[u].x - Mu);  // 0 for the padding and the empty entries
             l += w;
             a0 = fmaf(w, ov[u].x, a0);
             a1 = fmaf(w, ov[u].y, a1);
@@ -1534,7 +1537,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         float L = 0.f;
 #pragma unroll
         for (int g2 = 0; g2 < NG; ++g2) L += rl[g2][i] * exp2f(rm[g2][i] - Ms);
-        s.fin_m[i] = Ms;
+        s.fin_m[i] = Mx;  // -inf for a row with no key in this share
         s.fin_l[i] = L;
       }
     }
@@ -1558,7 +1561,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         val[4] += b4.x; val[5] += b4.y; val[6] += b4.z; val[7] += b4.w;
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) val[e] /= L;
+      for (int e = 0; e < 8; ++e) val[e] = (L == 0.f) ? 0.f : val[e] / L;  // l = 0: a row with no key here
       if (i >= hd.gq) continue;
       if (!split) {
         T* row = static_cast<T*>(a.out) + q_row(a, hd.b, h, r0 + i) * D;
@@ -1630,10 +1633,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             f0[n][jq] = exp2f(m0 - Ms);
             f1[n][jq] = exp2f(m1 - Ms);
             const float L = rl[0][q] * f0[n][jq] + rl[1][q] * f1[n][jq];
-            inv[n][jq] = vsc / L;
+            // With several new tokens a CTA's share of an item can hold no key
+            // of a row (l = 0): its partial is zero and weighs nothing.  A
+            // poisoned row (l NaN) stays NaN.
+            inv[n][jq] = (L == 0.f) ? 0.f : vsc / L;
             if (split && dp == 0 && gid == 0)
               *reinterpret_cast<float4*>(a.part + static_cast<size_t>(hd.slot) * prec + q * 4) =
-                  make_float4(Ms, L, 0.f, 0.f);
+                  make_float4(Mx, L, 0.f, 0.f);  // m = -inf for a row with no key here
           }
         }
       float o[kMt][NQT][4];
