@@ -162,12 +162,13 @@ VT_API vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const vo
  *   k_scale, v_scale  device float32 [num_kv_heads], 4-byte aligned; NULL is
  *                     VT_ERR_INVALID_ARG.
  *   head_dim          128 or 256 (64 is VT_ERR_UNSUPPORTED).
- * Arithmetic: codes widen exactly to f16 in registers; q is taken as f16
- * (exact for bf16 magnitudes in [2^-14, 65504]); QK^T and PV run on f16
- * tensor-core MMAs with fp32 accumulation, the softmax weights entering PV
- * as f16 (11 significant bits); k_scale folds into the score scale and
- * v_scale into the final normalisation.  Workspace, plan, status and errors
- * are those of vt_paged_attn_decode.
+ * Arithmetic: the K and V codes enter E4M3 tensor-core MMAs (fp32
+ * accumulation) as they are.  Each query row is scaled by a power of two and
+ * split into two E4M3 terms (about 8 significant bits, like bf16; rows below
+ * 2^-100 in magnitude count as zero), and so are the softmax weights, times
+ * 256 (weights below 2^-17 of their row's largest drop out).  k_scale folds
+ * into the score scale and v_scale into the final normalisation.
+ * Workspace, plan, status and errors are those of vt_paged_attn_decode.
  */
 VT_API vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache,
                                           const void* v_cache, const float* k_scale,

@@ -61,6 +61,10 @@ constexpr int kSwizzleCols = 64; // bf16 columns per 128-byte swizzled sub-tile 
 // GB300's 2.07 GHz maximum, 2^31 cycles is about 1 s and 2^28 about 0.13 s).
 constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr long long kDrainLimitCycles = 1ll << 28;
+// FP8 consumer: the softmax weights (at most 1) enter PV times this power of
+// two, so that weights down to 2^-17 of the row's largest stay E4M3 numbers.
+constexpr float kPScale = 256.f;
+
 // Page tiles of its slice a CTA prefetches into L2 before its dependency wait.
 constexpr int kPrefetchTiles = 8;
 
@@ -131,8 +135,8 @@ struct StageHeader {
 };
 
 // Consumer kinds: CUDA cores (fp32 storage); tensor cores on bf16 K/V
-// (mma.sync bf16); tensor cores on FP8 E4M3 K/V codes widened to f16 in
-// registers (mma.sync f16, bf16 queries and output).
+// (mma.sync bf16); tensor cores on FP8 E4M3 K/V codes (mma.sync e4m3, the
+// codes used as they are; bf16 queries and output).
 enum class Math { kSimt, kMma, kMma8 };
 
 // Element type of the K/V page tiles for a consumer kind.
@@ -184,7 +188,7 @@ struct Smem {
   alignas(8) unsigned long long full[NSTAGE];
   unsigned long long empty[NSTAGE];
   unsigned long long csync;
-  unsigned long long comb[2];  // partials staged for a combine (two ring halves)
+  unsigned long long comb;  // partials staged for a combine
   long long scan[16];
   int b_start_s;
   long long cum_start_s;
@@ -329,15 +333,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// D = A * B + D, f16 inputs, fp32 accumulators, m16n8k16.
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // Two E4M3 codes (low byte: element 0) widened to an f16 pair, exactly: every
 // E4M3 value (at most 448 in magnitude, at least 2^-9 apart from zero) is an
 // f16 normal number or zero; the NaN codes give NaN.
@@ -346,12 +341,37 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
-// A bf16 pair as an f16 pair (exact for magnitudes in [2^-14, 65504]; smaller
-// ones round to f16 subnormals, larger ones overflow).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-  return *reinterpret_cast<const uint32_t*>(&h);
+// An f16 pair (low half: element 0) rounded to two E4M3 codes (low byte:
+// element 0), saturating to +-448.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+  __half2_raw r;
+  r.x = static_cast<unsigned short>(h & 0xffffu);
+  r.y = static_cast<unsigned short>(h >> 16);
+  return __nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
 }
+
+// Two floats rounded to two E4M3 codes (low byte: lo), saturating to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  return __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// D = A * B + D, E4M3 inputs (four codes per register), fp32 accumulators,
+// m16n8k32.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^e as a float, e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -545,165 +565,6 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 }
 
 // ---------------------------------------------------------------------------
-// S8: the deferred LSE combines a CTA owes, run by its consumer warps after
-// their last tile.  A separate (not inlined) function, so its registers are
-// allocated apart from the tile loop's.
-// ---------------------------------------------------------------------------
-template <int D, typename T, int G, int NCW, int NSTAGE, Math MATH>
-__device__ __noinline__ void combine_pending(Smem<D, T, G, NCW, NSTAGE, MATH>& s, const DecodeArgs& a,
-                                            const Partition part, const int prec, uint32_t& sync_phase) {
-  using KV = KvElem<T, MATH>;
-  constexpr int NC = NCW * 32;
-  const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
-  const float kNegInf = -__int_as_float(0x7f800000);
-  auto cons_sync = [&]() -> bool {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s.csync);
-    bool r = wait_phase(&s.csync, sync_phase, &s.abort_flag, a.status, kStatusSync, a.wait_limit);
-    r = __all_sync(0xffffffffu, r);
-    sync_phase ^= 1u;
-    return r;
-  };
-  const int n_pend = s.pend_n;
-  float* const ring = reinterpret_cast<float*>(&s.k[0][0]);
-  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(KV);
-  constexpr size_t kHalfFloats = kRingBytes / 8;  // floats in one half of the ring
-  constexpr int kRowChunks = D / 4;  // float4 chunks of a row
-  constexpr int kOwn = (G * kRowChunks + NC - 1) / NC;
-  static_assert(kHalfFloats >= static_cast<size_t>(G) * (4 + D), "half the ring must hold a partial record");
-  uint32_t comb_phases = 0u;  // bit b: phase parity of ring half b
-  for (int pi = 0; pi < n_pend; ++pi) {
-    const PendingCombine pc = s.pend[pi];
-    const int h = pc.vh / a.subgroups, sub = pc.vh - h * a.subgroups;
-    const int r0 = sub * G;  // first query row of this subgroup
-    const int gq = pc.gq;
-    const int c_first = pc.c_first;
-    // The k-th CTA sharing the item left its partial in first-segment slot
-    // c_first + k, except the first CTA when the item starts inside its slice
-    // (last-segment slot grid + c_first).
-    const bool first_last = part.start(c_first) < pc.item_u;
-    const int rec = prec;
-    const uint32_t rec_bytes = static_cast<uint32_t>(rec) * 4;
-    const int per_round = static_cast<int>(kHalfFloats * 4 / rec_bytes);
-    const int rounds = (pc.nsplit + per_round - 1) / per_round;
-    float Mrun[kOwn], Lrun[kOwn], acc[kOwn][4];
-#pragma unroll
-    for (int q = 0; q < kOwn; ++q) {
-      Mrun[q] = kNegInf;
-      Lrun[q] = 0.f;
-      acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-    }
-    if (pi > 0 && !cons_sync()) return;  // everyone is done with the previous item's rounds
-    // Iteration r merges round r (r >= 0), then issues round r + 2 into the
-    // half it frees (rounds 0 and 1 are issued by the first two iterations).
-    for (int r = -2; r < rounds; ++r) {
-      if (r >= 0) {
-      const int nk = min(per_round, pc.nsplit - r * per_round);
-      float* const buf = ring + (r & 1) * kHalfFloats;
-      bool ok = wait_phase(&s.comb[r & 1], (comb_phases >> (r & 1)) & 1u, &s.abort_flag, a.status, kStatusCombine,
-                           a.wait_limit);
-      comb_phases ^= 1u << (r & 1);
-      if (!__all_sync(0xffffffffu, ok)) return;
-#pragma unroll
-      for (int q = 0; q < kOwn; ++q) {
-        const int oc = ct + q * NC;
-        const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
-        if (i >= gq) continue;
-        const float* mlp = buf + i * 4;                  // (m, l) of row i, record stride rec
-        const float* src = buf + G * 4 + i * D + 4 * cc;  // this thread's chunk, record stride rec
-        // One pass in batches of kB partials, all loads of a batch in flight:
-        // the batch's largest m rescales what is accumulated so far.
-        constexpr int kB = 8;
-        float M = Mrun[q], l = Lrun[q], a0 = acc[q][0], a1 = acc[q][1], a2 = acc[q][2], a3 = acc[q][3];
-        for (int k = 0; k < nk; k += kB) {
-          float2 ml[kB];
-          float4 ov[kB];
-#pragma unroll
-          for (int u = 0; u < kB; ++u) {
-            if (k + u < nk) {
-              ml[u] = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k + u) * rec);
-              ov[u] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k + u) * rec);
-            } else {
-              ml[u] = make_float2(kNegInf, 0.f);
-              ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-          }
-          float Mb = M;
-#pragma unroll
-          for (int u = 0; u < kB; ++u) Mb = fmaxf(Mb, ml[u].x);
-          // Mu: the batch maximum, or 0 while every partial so far is empty
-          // (m = -inf, l = 0: a multi-token row with no key in that share)
-          const float Mu = (Mb == kNegInf) ? 0.f : Mb;
-          const float sc = exp2f(M - Mu);  // 0 before the first partial (M = -inf)
-          M = Mb;
-          l *= sc;
-          a0 *= sc;
-          a1 *= sc;
-          a2 *= sc;
-          a3 *= sc;
-#pragma unroll
-          for (int u = 0; u < kB; ++u) {
-            const float w = ml[u].y * exp2f(ml[u].x - Mu);  // 0 for the padding and the empty entries
-            l += w;
-            a0 = fmaf(w, ov[u].x, a0);
-            a1 = fmaf(w, ov[u].y, a1);
-            a2 = fmaf(w, ov[u].z, a2);
-            a3 = fmaf(w, ov[u].w, a3);
-          }
-        }
-        Mrun[q] = M;
-        Lrun[q] = l;
-        acc[q][0] = a0;
-        acc[q][1] = a1;
-        acc[q][2] = a2;
-        acc[q][3] = a3;
-      }
-      }
-      // Round n: records n * per_round .. + nk - 1 into ring half n & 1.  They
-      // are one run of first-segment slots, but for record 0 when it sits in
-      // the last-segment half: two copies at most, issued by warp 0.
-      const int n = r + 2;
-      if (n < rounds) {
-        if (r >= 0 && !cons_sync()) return;  // everyone is done reading half n & 1
-        if (warp == 0) {
-          const int k0 = n * per_round, nk = min(per_round, pc.nsplit - k0);
-          float* dst = ring + (n & 1) * kHalfFloats;
-          unsigned long long* bar = &s.comb[n & 1];
-          const bool split0 = k0 == 0 && first_last;
-          if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nk) * rec_bytes);
-          __syncwarp();
-          if (lane < 2) {
-            fence_proxy_async_global();
-            const size_t g = gridDim.x;
-            if (lane == 0 && split0) bulk_load(dst, a.part + (g + c_first) * rec, rec_bytes, bar);
-            const int k_run = split0 ? 1 : 0;  // first record of the run in this round
-            if (lane == (split0 ? 1 : 0) && nk > k_run)
-              bulk_load(dst + static_cast<size_t>(k_run) * rec,
-                        a.part + static_cast<size_t>(c_first + k0 + k_run) * rec,
-                        static_cast<uint32_t>(nk - k_run) * rec_bytes, bar);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kOwn; ++q) {
-      const int oc = ct + q * NC;
-      const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
-      if (i >= gq) continue;
-      const float inv = 1.f / Lrun[q];
-      T* row = static_cast<T*>(a.out) + q_row(a, pc.b, h, r0 + i) * D + 4 * cc;
-      if constexpr (sizeof(T) == 2) {
-        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(acc[q][0] * inv, acc[q][1] * inv),
-                                                    pack_bf16(acc[q][2] * inv, acc[q][3] * inv));
-      } else {
-        *reinterpret_cast<float4*>(row) =
-            make_float4(acc[q][0] * inv, acc[q][1] * inv, acc[q][2] * inv, acc[q][3] * inv);
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, typename T, int G, int NCW, int NSTAGE, int MINB, Math MATH>
@@ -719,6 +580,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr bool kMma = MATH != Math::kSimt;
   constexpr bool kFp8 = MATH == Math::kMma8;
   constexpr bool kQSmem = S::QS;
+  // Two pages per consumer iteration: measured slower on GB300 (it holds two
+  // stages of shallow rings at once), so off; kept to try on deeper rings.
+  constexpr bool kPair = false;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
                 "mma consumer shape");
   static_assert(!kFp8 || (D % 128 == 0 && (D / (NCW / 2)) % 32 == 0), "fp8 consumer shape");
@@ -758,8 +622,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       mbar_init(&s.empty[st], NCW);
     }
     mbar_init(&s.csync, NCW);  // one arrival per consumer warp
-    mbar_init(&s.comb[0], 1);
-    mbar_init(&s.comb[1], 1);
+    mbar_init(&s.comb, 1);
     s.abort_flag = 0;
     s.b_start_s = -1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1066,7 +929,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   uint32_t qb[kMma && !kQSmem ? kKSteps : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
   float oacc[kMma ? kMt : 1][NQT][4];       // O^T accumulators
   float m_run = kNegInf, l_run = 0.f;       // simt: the lane's query
-  float sl2 = a.scale_log2;                 // score factor into the log2 domain (fp8: times k_scale[h])
+  float sl2 = a.scale_log2;                 // score factor into the log2 domain
+  float sq[kFp8 ? NQT : 1][2];              // fp8: the factor of the lane's query columns
   float vsc = 1.f;                          // value factor (fp8: v_scale[h])
   // Causal offset of a query row's new token: q_len - 1 - j (0 for
   // single-token decode); its keys end that many tokens before the context's.
@@ -1083,6 +947,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       break;
     }
     hd = s.hdr[stage];
+    bool paired = false;      // this iteration also takes the next stage (tensor-core consumer)
+    StageHeader hd_next = hd;
     if (hd.flags & kEnd) {
       more = false;
       break;
@@ -1190,24 +1056,61 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         // group are zero.
         const uint32_t* q32 = reinterpret_cast<const uint32_t*>(s.q[stage]);
         if constexpr (kFp8) {
-          // f16 operands.  The K fragments of a k-step carry head_dim columns
-          // 16ks + 4tig .. +3 (four consecutive codes per lane, see S3), so
-          // the contraction index is permuted the same way here: k = 2tig,
-          // 2tig + 1 are columns 16ks + 4tig, +1 and k = 2tig + 8, +9 are
-          // columns 16ks + 4tig + 2, +3.
+          // E4M3 operands of mma.sync m16n8k32: the lane holds query 8n + gid,
+          // columns 32kp + 4tig .. +3 (b0) and 32kp + 16 + 4tig .. +3 (b1) of
+          // k-step kp.  Each query row is scaled by a power of two 2^e that
+          // puts its largest magnitude in [128, 256) and split into two E4M3
+          // terms, hi = e4m3(q 2^e) and lo = e4m3(q 2^e - hi): about 8
+          // significant bits of q, like its bf16 storage (rows below 2^-100
+          // count as zero).  qb[2kp] holds hi, qb[2kp + 1] lo; the score of
+          // a query column is scaled back by 2^-e with the softmax factor.
           const int h = hd.vh / a.subgroups;
-          sl2 = a.scale_log2 * __ldg(a.k_scale + h);
-          vsc = __ldg(a.v_scale + h);
+          const float sk = a.scale_log2 * __ldg(a.k_scale + h);
+          vsc = __ldg(a.v_scale + h) * (1.f / kPScale);
 #pragma unroll
           for (int n = 0; n < NQT; ++n) {
             const int qr = 8 * n + gid;
             const bool ok = qr < hd.gq;
+            float mx = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < kKSteps; ++ks) {
-              const uint2 w = ok ? *reinterpret_cast<const uint2*>(q32 + ((qr * D + ks * 16 + 4 * tig) >> 1))
-                                 : make_uint2(0u, 0u);
-              qb[ks][n][0] = bf16x2_to_f16x2(w.x);
-              qb[ks][n][1] = bf16x2_to_f16x2(w.y);
+            for (int kp = 0; kp < kKSteps / 2; ++kp)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const uint2 w = ok ? *reinterpret_cast<const uint2*>(q32 + ((qr * D + kp * 32 + hf * 16 + 4 * tig) >> 1))
+                                   : make_uint2(0u, 0u);
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_lo_f(w.x)), fabsf(bf16_hi_f(w.x))),
+                                     fmaxf(fabsf(bf16_lo_f(w.y)), fabsf(bf16_hi_f(w.y)))));
+              }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;  // floor(log2 mx)
+            const int e = (mx >= 0x1p-100f && mx <= 0x1p+100f) ? 7 - ex : 0;
+            const float sc = pow2f(e);
+#pragma unroll
+            for (int kp = 0; kp < kKSteps / 2; ++kp)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const uint2 w = ok ? *reinterpret_cast<const uint2*>(q32 + ((qr * D + kp * 32 + hf * 16 + 4 * tig) >> 1))
+                                   : make_uint2(0u, 0u);
+                const float x0 = bf16_lo_f(w.x) * sc, x1 = bf16_hi_f(w.x) * sc;
+                const float x2 = bf16_lo_f(w.y) * sc, x3 = bf16_hi_f(w.y) * sc;
+                const uint32_t hi = f32x2_to_e4m3x2(x0, x1) | (f32x2_to_e4m3x2(x2, x3) << 16);
+                const uint32_t b01 = e4m3x2_to_f16x2(hi), b23 = e4m3x2_to_f16x2(hi >> 16);
+                const uint32_t lo =
+                    f32x2_to_e4m3x2(x0 - __half2float(__ushort_as_half(static_cast<unsigned short>(b01 & 0xffffu))),
+                                    x1 - __half2float(__ushort_as_half(static_cast<unsigned short>(b01 >> 16)))) |
+                    (f32x2_to_e4m3x2(x2 - __half2float(__ushort_as_half(static_cast<unsigned short>(b23 & 0xffffu))),
+                                     x3 - __half2float(__ushort_as_half(static_cast<unsigned short>(b23 >> 16))))
+                     << 16);
+                qb[2 * kp][n][hf] = hi;
+                qb[2 * kp + 1][n][hf] = lo;
+              }
+            // the factor of this lane's score columns, queries 8n + 2tig (+1),
+            // whose exponents sit with the lanes of gid 2tig (+1)
+#pragma unroll
+            for (int jq = 0; jq < 2; ++jq) {
+              const int eq = __shfl_sync(0xffffffffu, e, (2 * tig + jq) * 4);
+              sq[n][jq] = sk * pow2f(-eq);
             }
           }
         } else if constexpr (kQSmem) {
@@ -1255,42 +1158,60 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         }
         poison = false;
       }
-      if (hd.flags & kBadPage) {
+      // Two page tiles of the segment per iteration when this one is not its
+      // last (the next stage then holds the segment's next page): two
+      // independent QK^T chains, one softmax reduction over both pages' scores
+      // and two PV streams, which hides more of each tile's latency chain.
+      const bool pair = kPair && !(hd.flags & kLast);
+      int stage_b = stage + 1;
+      uint32_t phase_b = phase;
+      if (stage_b == NSTAGE) {
+        stage_b = 0;
+        phase_b ^= 1u;
+      }
+      StageHeader hd_b = hd;
+      if (pair) {
+        bool okb = wait_phase(&s.full[stage_b], phase_b, &s.abort_flag, a.status, kStatusFull, a.wait_limit);
+        okb = __all_sync(0xffffffffu, okb);
+        if (!okb) {
+          alive = false;
+          break;
+        }
+        hd_b = s.hdr[stage_b];
+        paired = true;
+        hd_next = hd_b;
+      }
+      if ((hd.flags & kBadPage) || (hd_b.flags & kBadPage)) {
         poison = true;
       } else {
-        const uint32_t kbase = smem_addr(s.k[stage]);
-        const uint32_t vbase = smem_addr(s.v[stage]);
-        // S3: S^T = K Q^T for this warp's 16 tokens; even and odd k-steps
-        // accumulate separately (two short MMA chains instead of one long).
-        float sacc[NQT][2][4];
+        // S3: S^T = K Q^T for this warp's 16 tokens of a page; even and odd
+        // k-steps accumulate separately (two short MMA chains instead of one).
+        auto qk = [&](const uint32_t kbase, float (&sc)[NQT][2][4]) {
 #pragma unroll
-        for (int n = 0; n < NQT; ++n)
+          for (int n = 0; n < NQT; ++n)
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
+            for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[n][hh][e] = 0.f;
+              for (int e = 0; e < 4; ++e) sc[n][hh][e] = 0.f;
         if constexpr (kFp8) {
-          // K codes, [token][head_dim] bytes in 128-byte swizzled rows: one
-          // ldmatrix.x4 brings 8 x 16-byte blocks for tokens 0-7 and 8-15 of
-          // the warp and two k-steps (32 columns); lane (gid, tig) gets the
-          // four codes of columns 4tig .. +3 of each block, for token gid
-          // (+ 8).  Widened to f16 pairs they are the A fragment directly.
+          // K codes, [token][head_dim] bytes in 128-byte swizzled rows, feed
+          // the e4m3 MMA as they are: one ldmatrix.x4 gives the A fragment of
+          // a 32-column k-step for the warp's 16 tokens (lane (gid, tig):
+          // codes of columns 4tig .. +3 and 16 + 4tig .. +3 for tokens gid and
+          // gid + 8).  Two MMAs per k-step, Q hi and Q lo, into separate
+          // accumulators.
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;
 #pragma unroll
           for (int kp = 0; kp < kKSteps / 2; ++kp) {
             const int byte = kp * 32 + ((mi >> 1) << 4);
             const int sb = byte >> 7, chunk = (byte & 127) >> 4;
-            uint32_t c4[4];
-            ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), c4);
+            uint32_t ak[4];
+            ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {  // k-step 2kp + half: blocks c4[2 half], c4[2 half + 1]
-              const uint32_t lo_tok = c4[2 * half], hi_tok = c4[2 * half + 1];
-              const uint32_t ak[4] = {e4m3x2_to_f16x2(lo_tok), e4m3x2_to_f16x2(hi_tok), e4m3x2_to_f16x2(lo_tok >> 16),
-                                      e4m3x2_to_f16x2(hi_tok >> 16)};
-              const int ks = 2 * kp + half;
-#pragma unroll
-              for (int n = 0; n < NQT; ++n) mma_f16(sacc[n][half], ak, qb[ks][n][0], qb[ks][n][1]);
+            for (int n = 0; n < NQT; ++n) {
+              mma_e4m3(sc[n][0], ak, qb[2 * kp][n][0], qb[2 * kp][n][1]);
+              mma_e4m3(sc[n][1], ak, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
             }
           }
         } else if constexpr (kQSmem) {
@@ -1317,7 +1238,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               uint32_t ak[4];
               ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
-              for (int n = 0; n < NQT; ++n) mma_bf16(sacc[n][h2], ak, qf[n][2 * h2], qf[n][2 * h2 + 1]);
+              for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][h2], ak, qf[n][2 * h2], qf[n][2 * h2 + 1]);
             }
           }
         } else {
@@ -1330,18 +1251,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             uint32_t ak[4];
             ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
-            for (int n = 0; n < NQT; ++n) mma_bf16(sacc[n][ks & 1], ak, qb[ks][n][0], qb[ks][n][1]);
+            for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][ks & 1], ak, qb[ks][n][0], qb[ks][n][1]);
           }
         }
-        // S4 + S5: mask and scale; online softmax per query column.  Lane
-        // holds tokens 16tg + gid (values 0, 1) and + 8 (values 2, 3) of
-        // queries 8n + 2tig (values 0, 2) and + 1 (values 1, 3).
-        // Query row q of new token j sees the page's tokens t with
+        };
+        float sacc[2][NQT][2][4];
+        qk(smem_addr(s.k[stage]), sacc[0]);
+        if (pair) qk(smem_addr(s.k[stage_b]), sacc[1]);
+        // S4 + S5: mask and scale; online softmax per query column over the
+        // iteration's pages.  Lane holds tokens 16tg + gid (values 0, 1) and
+        // + 8 (values 2, 3) of queries 8n + 2tig (values 0, 2) and + 1 (values
+        // 1, 3).  Query row q of new token j sees the page's tokens t with
         // beg <= t < end, end = rel_end - (q_len - 1 - j), beg = end - window
         // (for single-token decode exactly [lo, hi)).
         const int t_lo = 16 * tg + gid, t_hi = t_lo + 8;
         const int wlim = a.window > 0 ? a.window : (1 << 30);
-        float pr[NQT][4];
+        float pr[2][NQT][4];
         float al[NQT][2];
         bool moved = false;
 #pragma unroll
@@ -1350,11 +1275,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           for (int jq = 0; jq < 2; ++jq) {
             const int q = 8 * n + 2 * tig + jq;
             const bool qok = q < hd.gq;
-            const int end = hd.rel_end - qoff[n][jq], beg = end - wlim;
-            const bool tok_lo = t_lo >= beg && t_lo < end, tok_hi = t_hi >= beg && t_hi < end;
-            const float s_lo = (qok && tok_lo) ? (sacc[n][0][jq] + sacc[n][1][jq]) * sl2 : kNegInf;
-            const float s_hi = (qok && tok_hi) ? (sacc[n][0][jq + 2] + sacc[n][1][jq + 2]) * sl2 : kNegInf;
-            float mx = fmaxf(s_lo, s_hi);
+            const float f = kFp8 ? sq[kFp8 ? n : 0][jq] : sl2;
+            float sv[2][2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const StageHeader& h = u ? hd_b : hd;
+              const int end = h.rel_end - qoff[n][jq], beg = end - wlim;
+              const bool ok_u = qok && (u == 0 || pair);
+              sv[u][0] = (ok_u && t_lo >= beg && t_lo < end) ? (sacc[u][n][0][jq] + sacc[u][n][1][jq]) * f : kNegInf;
+              sv[u][1] = (ok_u && t_hi >= beg && t_hi < end) ? (sacc[u][n][0][jq + 2] + sacc[u][n][1][jq + 2]) * f
+                                                             : kNegInf;
+            }
+            float mx = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -1362,9 +1294,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const float mu = (mn == kNegInf) ? 0.f : mn;
             al[n][jq] = exp2f(mq[n][jq] - mu);
             moved |= al[n][jq] != 1.f;
-            pr[n][jq] = exp2f(s_lo - mu);
-            pr[n][jq + 2] = exp2f(s_hi - mu);
-            lq[n][jq] = lq[n][jq] * al[n][jq] + pr[n][jq] + pr[n][jq + 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              pr[u][n][jq] = exp2f(sv[u][0] - mu);
+              pr[u][n][jq + 2] = exp2f(sv[u][1] - mu);
+              lsum += pr[u][n][jq] + pr[u][n][jq + 2];
+            }
+            lq[n][jq] = lq[n][jq] * al[n][jq] + lsum;
             mq[n][jq] = mn;
           }
         }
@@ -1379,31 +1316,47 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               oacc[mt][n][3] *= al[n][1];
             }
         }
-        // V rows of masked tokens may hold anything (NaN in unused slots) and
-        // 0 * NaN is NaN inside the MMA: clear those tokens in the V^T
-        // fragments.  This lane's fragments carry tokens 16tg + 2tig (+1) and
-        // (+8, +9).
+        // S6: O^T[this warp's rows] += V^T P^T over a page's 16 tokens of
+        // this warp.  V rows of masked tokens may hold anything (NaN in unused
+        // slots) and 0 * NaN is NaN inside the MMA: clear those tokens in the
+        // V^T fragments.  This lane's fragments carry tokens 16tg + 2tig (+1)
+        // and (+8, +9).
         const int tl = 16 * tg + 2 * tig;
-        const uint32_t mlo = ((tl >= hd.lo && tl < hd.hi) ? 0x0000ffffu : 0u) |
-                             ((tl + 1 >= hd.lo && tl + 1 < hd.hi) ? 0xffff0000u : 0u);
-        const uint32_t mhi = ((tl + 8 >= hd.lo && tl + 8 < hd.hi) ? 0x0000ffffu : 0u) |
-                             ((tl + 9 >= hd.lo && tl + 9 < hd.hi) ? 0xffff0000u : 0u);
-        const bool full_page = hd.lo == 0 && hd.hi == kPageTokens;  // no token to clear
+        auto pv = [&](const int st, const StageHeader& h, const float (&p)[NQT][4]) {
+          const uint32_t mlo = ((tl >= h.lo && tl < h.hi) ? 0x0000ffffu : 0u) |
+                               ((tl + 1 >= h.lo && tl + 1 < h.hi) ? 0xffff0000u : 0u);
+          const uint32_t mhi = ((tl + 8 >= h.lo && tl + 8 < h.hi) ? 0x0000ffffu : 0u) |
+                               ((tl + 9 >= h.lo && tl + 9 < h.hi) ? 0xffff0000u : 0u);
+          const bool full_page = h.lo == 0 && h.hi == kPageTokens;  // no token to clear
         if constexpr (kFp8) {
-          // P^T as an f16 B operand (11 significant bits of each weight),
-          // transposed from the S^T accumulator layout with movmatrix.
+          // P^T for the e4m3 MMA: the weights times kPScale, split into two
+          // E4M3 terms hi + lo (about 8 significant bits).  After movmatrix a
+          // lane holds, for query gid, the weights of tokens 2tig, 2tig + 1
+          // (from the first 8x8 block) and 2tig + 8, 2tig + 9 (the second):
+          // the four codes of one B register, in that token order.  k = 0..15
+          // carries hi and k = 16..31 lo over the same tokens, and the V^T
+          // fragment repeats for both halves, so one MMA adds V (P_hi + P_lo).
           uint32_t pb[NQT][2];
 #pragma unroll
-          for (int n = 0; n < NQT; ++n)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) pb[n][hh] = movmatrix_trans(pack_f16(pr[n][2 * hh], pr[n][2 * hh + 1]));
-          // S6: O^T += V^T P^T.  V^T A fragments pair two tokens of one
-          // column, which sit 128 bytes apart: each lane reads the 4-byte
-          // codes of columns c0 + 4gid .. +3 for tokens 2tig, 2tig + 1,
-          // 2tig + 8, 2tig + 9 (bank-conflict free under the swizzle) and
-          // interleaves them per column with byte permutes.  A 32-column
-          // block makes two m-tiles whose rows are columns c0 + 4gid + {0, 1}
-          // and c0 + 4gid + {2, 3} (gid, gid + 8).
+          for (int n = 0; n < NQT; ++n) {
+            const uint32_t h0 = movmatrix_trans(pack_f16(p[n][0] * kPScale, p[n][1] * kPScale));
+            const uint32_t h1 = movmatrix_trans(pack_f16(p[n][2] * kPScale, p[n][3] * kPScale));
+            const uint32_t hi = f16x2_to_e4m3x2(h0) | (f16x2_to_e4m3x2(h1) << 16);
+            const uint32_t r0 = hsub2_u32(h0, e4m3x2_to_f16x2(hi)), r1 = hsub2_u32(h1, e4m3x2_to_f16x2(hi >> 16));
+            pb[n][0] = hi;
+            pb[n][1] = f16x2_to_e4m3x2(r0) | (f16x2_to_e4m3x2(r1) << 16);
+          }
+          // V^T A fragments: each lane reads the 4-byte codes of columns
+          // c0 + 4gid .. +3 for tokens 2tig, 2tig + 1, 2tig + 8, 2tig + 9
+          // (bank-conflict free under the swizzle) and transposes the 4x4
+          // bytes with byte permutes: one register per column, four tokens
+          // each.  A 32-column block makes two m-tiles whose rows are columns
+          // c0 + 4gid + {0, 1} and c0 + 4gid + {2, 3} (gid, gid + 8).  Codes
+          // of tokens outside the page's range are cleared (they may be NaN).
+          const uint32_t m8 = ((tl >= h.lo && tl < h.hi) ? 0x000000ffu : 0u) |
+                              ((tl + 1 >= h.lo && tl + 1 < h.hi) ? 0x0000ff00u : 0u) |
+                              ((tl + 8 >= h.lo && tl + 8 < h.hi) ? 0x00ff0000u : 0u) |
+                              ((tl + 9 >= h.lo && tl + 9 < h.hi) ? 0xff000000u : 0u);
 #pragma unroll
           for (int cb = 0; cb < kDPart / 32; ++cb) {
             const int byte = dp * kDPart + cb * 32 + 4 * gid;
@@ -1412,24 +1365,22 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int t = tl + (u & 1) + ((u >> 1) << 3);  // 2tig, +1, +8, +9
-              w[u] = *reinterpret_cast<const uint32_t*>(&s.v[stage][0] + sb * (kPageTokens * 128) + t * 128 +
+              w[u] = *reinterpret_cast<const uint32_t*>(&s.v[st][0] + sb * (kPageTokens * 128) + t * 128 +
                                                         ((chunk ^ (t & 7)) << 4) + within);
+            }
+            const uint32_t x01 = __byte_perm(w[0], w[1], 0x5140u), x23 = __byte_perm(w[2], w[3], 0x5140u);
+            const uint32_t y01 = __byte_perm(w[0], w[1], 0x7362u), y23 = __byte_perm(w[2], w[3], 0x7362u);
+            uint32_t col[4] = {__byte_perm(x01, x23, 0x5410u), __byte_perm(x01, x23, 0x7632u),
+                               __byte_perm(y01, y23, 0x5410u), __byte_perm(y01, y23, 0x7632u)};
+            if (!full_page) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) col[e] &= m8;
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {  // columns {0, 1} then {2, 3} of the lane's four
-              const uint32_t sel = half ? 0x7362u : 0x5140u;
-              const uint32_t lo_pair = __byte_perm(w[0], w[1], sel);  // tokens 2tig, 2tig + 1
-              const uint32_t hi_pair = __byte_perm(w[2], w[3], sel);  // tokens 2tig + 8, + 9
-              uint32_t av[4] = {e4m3x2_to_f16x2(lo_pair), e4m3x2_to_f16x2(lo_pair >> 16), e4m3x2_to_f16x2(hi_pair),
-                                e4m3x2_to_f16x2(hi_pair >> 16)};
-              if (!full_page) {
-                av[0] &= mlo;
-                av[1] &= mlo;
-                av[2] &= mhi;
-                av[3] &= mhi;
-              }
+              const uint32_t av[4] = {col[2 * half], col[2 * half + 1], col[2 * half], col[2 * half + 1]};
 #pragma unroll
-              for (int n = 0; n < NQT; ++n) mma_f16(oacc[2 * cb + half][n], av, pb[n][0], pb[n][1]);
+              for (int n = 0; n < NQT; ++n) mma_e4m3(oacc[2 * cb + half][n], av, pb[n][0], pb[n][1]);
             }
           }
         } else {
@@ -1441,7 +1392,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           for (int n = 0; n < NQT; ++n) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {  // tokens 0-7 then 8-15 of the warp
-              const float p0 = pr[n][2 * hh], p1 = pr[n][2 * hh + 1];
+              const float p0 = p[n][2 * hh], p1 = p[n][2 * hh + 1];
               const uint32_t h = pack_bf16(p0, p1);
               const uint32_t l = pack_bf16(p0 - bf16_lo_f(h), p1 - bf16_hi_f(h));
               pbh[n][hh] = movmatrix_trans(h);
@@ -1456,7 +1407,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const int d = dp * kDPart + mt * 16 + ((mi & 1) << 3);
             const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
             uint32_t av[4];
-            ldmatrix_x4_trans(vbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), av);
+            ldmatrix_x4_trans(smem_addr(s.v[st]) + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), av);
             if (!full_page) {
               av[0] &= mlo;
               av[1] &= mlo;
@@ -1470,6 +1421,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             }
           }
         }
+        };
+        pv(stage, hd, pr[0]);
+        if (pair) pv(stage_b, hd_b, pr[1]);
       }
     }
 
@@ -1484,6 +1438,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     if (++stage == NSTAGE) {
       stage = 0;
       phase ^= 1u;
+    }
+    if (paired) {  // the iteration also consumed the next stage
+      if (lane == 0) mbar_arrive(&s.empty[stage]);
+      if (++stage == NSTAGE) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      hd = hd_next;
     }
   } while (!(hd.flags & kLast));
   if (!alive || !more) break;
@@ -1710,14 +1672,134 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 
   // ===================== S8: deferred LSE combines ============================
   // Run after this CTA consumed all its tiles, so the stage ring is free.  An
-  // item's partials are one run of records (see DecodeArgs::part), staged by
-  // bulk copies in rounds that alternate between the two halves of the ring:
-  // the next round's copy is in flight while the current one is merged.  Each
-  // thread merges its 4-column chunks, weighting every partial by
-  // l * 2^(m - M).
+  // item's partials are one run of records (see DecodeArgs::part): one or two
+  // bulk copies stage a round of them.  Each thread then merges its 4-column
+  // chunks, weighting every partial by l * 2^(m - M).
   if (!alive) return;
   if (!cons_sync()) return;  // pend_n was written by thread 0
-  combine_pending<D, T, G, NCW, NSTAGE, MATH>(s, a, part, prec, sync_phase);
+  const int n_pend = s.pend_n;
+  float* const ring = reinterpret_cast<float*>(&s.k[0][0]);
+  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(KV);
+  constexpr int kRowChunks = D / 4;  // float4 chunks of a row
+  constexpr int kOwn = (G * kRowChunks + NC - 1) / NC;
+  static_assert(kRingBytes >= static_cast<size_t>(G) * (4 + D) * 4, "the ring must hold a partial record");
+  uint32_t comb_phase = 0;
+  for (int pi = 0; pi < n_pend; ++pi) {
+    const PendingCombine pc = s.pend[pi];
+    const int h = pc.vh / a.subgroups, sub = pc.vh - h * a.subgroups;
+    const int r0 = sub * G;  // first query row of this subgroup
+    const int gq = pc.gq;
+    const int c_first = pc.c_first;
+    // The k-th CTA sharing the item left its partial in first-segment slot
+    // c_first + k, except the first CTA when the item starts inside its slice
+    // (last-segment slot grid + c_first).
+    const bool first_last = part.start(c_first) < pc.item_u;
+    const int rec = prec;
+    const uint32_t rec_bytes = static_cast<uint32_t>(rec) * 4;
+    const int per_round = static_cast<int>(kRingBytes / rec_bytes);
+    float Mrun[kOwn], Lrun[kOwn], acc[kOwn][4];
+#pragma unroll
+    for (int q = 0; q < kOwn; ++q) {
+      Mrun[q] = kNegInf;
+      Lrun[q] = 0.f;
+      acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+    }
+    for (int k0 = 0; k0 < pc.nsplit; k0 += per_round) {
+      const int nk = min(per_round, pc.nsplit - k0);
+      if (k0 > 0 || pi > 0) {
+        if (!cons_sync()) return;  // everyone is done reading the ring
+      }
+      if (warp == 0) {
+        // records k0 .. k0 + nk - 1 are one run of first-segment slots, but
+        // for record 0 when it sits in the last-segment half: two copies at most
+        const bool split0 = k0 == 0 && first_last;
+        if (lane == 0) mbar_arrive_expect_tx(&s.comb, static_cast<uint32_t>(nk) * rec_bytes);
+        __syncwarp();
+        if (lane < 2) {
+          fence_proxy_async_global();
+          const size_t g = gridDim.x;
+          if (lane == 0 && split0) bulk_load(ring, a.part + (g + c_first) * rec, rec_bytes, &s.comb);
+          const int k_run = split0 ? 1 : 0;  // first record of the run in this round
+          if (lane == (split0 ? 1 : 0) && nk > k_run)
+            bulk_load(ring + static_cast<size_t>(k_run) * rec,
+                      a.part + static_cast<size_t>(c_first + k0 + k_run) * rec,
+                      static_cast<uint32_t>(nk - k_run) * rec_bytes, &s.comb);
+        }
+      }
+      bool ok = wait_phase(&s.comb, comb_phase, &s.abort_flag, a.status, kStatusCombine, a.wait_limit);
+      comb_phase ^= 1u;
+      if (!__all_sync(0xffffffffu, ok)) return;
+#pragma unroll
+      for (int q = 0; q < kOwn; ++q) {
+        const int oc = ct + q * NC;
+        const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
+        if (i >= gq) continue;
+        const float* mlp = ring + i * 4;                  // (m, l) of row i, record stride rec
+        const float* src = ring + G * 4 + i * D + 4 * cc;  // this thread's chunk, record stride rec
+        // One pass in batches of kB partials, all loads of a batch in flight:
+        // the batch's largest m rescales what is accumulated so far.
+        constexpr int kB = 8;
+        float M = Mrun[q], l = Lrun[q], a0 = acc[q][0], a1 = acc[q][1], a2 = acc[q][2], a3 = acc[q][3];
+        for (int k = 0; k < nk; k += kB) {
+          float2 ml[kB];
+          float4 ov[kB];
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            if (k + u < nk) {
+              ml[u] = *reinterpret_cast<const float2*>(mlp + static_cast<size_t>(k + u) * rec);
+              ov[u] = *reinterpret_cast<const float4*>(src + static_cast<size_t>(k + u) * rec);
+            } else {
+              ml[u] = make_float2(kNegInf, 0.f);
+              ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
+          float Mb = M;
+#pragma unroll
+          for (int u = 0; u < kB; ++u) Mb = fmaxf(Mb, ml[u].x);
+          // Mu: the batch maximum, or 0 while every partial so far is empty
+          // (m = -inf, l = 0: a multi-token row with no key in that share)
+          const float Mu = (Mb == kNegInf) ? 0.f : Mb;
+          const float sc = exp2f(M - Mu);  // 0 before the first partial (M = -inf)
+          M = Mb;
+          l *= sc;
+          a0 *= sc;
+          a1 *= sc;
+          a2 *= sc;
+          a3 *= sc;
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            const float w = ml[u].y * exp2f(ml[u].x - Mu);  // 0 for the padding and the empty entries
+            l += w;
+            a0 = fmaf(w, ov[u].x, a0);
+            a1 = fmaf(w, ov[u].y, a1);
+            a2 = fmaf(w, ov[u].z, a2);
+            a3 = fmaf(w, ov[u].w, a3);
+          }
+        }
+        Mrun[q] = M;
+        Lrun[q] = l;
+        acc[q][0] = a0;
+        acc[q][1] = a1;
+        acc[q][2] = a2;
+        acc[q][3] = a3;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kOwn; ++q) {
+      const int oc = ct + q * NC;
+      const int i = oc / kRowChunks, cc = oc - i * kRowChunks;
+      if (i >= gq) continue;
+      const float inv = 1.f / Lrun[q];
+      T* row = static_cast<T*>(a.out) + q_row(a, pc.b, h, r0 + i) * D + 4 * cc;
+      if constexpr (sizeof(T) == 2) {
+        *reinterpret_cast<uint2*>(row) = make_uint2(pack_bf16(acc[q][0] * inv, acc[q][1] * inv),
+                                                    pack_bf16(acc[q][2] * inv, acc[q][3] * inv));
+      } else {
+        *reinterpret_cast<float4*>(row) =
+            make_float4(acc[q][0] * inv, acc[q][1] * inv, acc[q][2] * inv, acc[q][3] * inv);
+      }
+    }
+  }
 }
 
 }  // namespace vt
