@@ -580,9 +580,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr bool kMma = MATH != Math::kSimt;
   constexpr bool kFp8 = MATH == Math::kMma8;
   constexpr bool kQSmem = S::QS;
-  // Two pages per consumer iteration: measured slower on GB300 (it holds two
-  // stages of shallow rings at once), so off; kept to try on deeper rings.
-  constexpr bool kPair = false;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
                 "mma consumer shape");
   static_assert(!kFp8 || (D % 128 == 0 && (D / (NCW / 2)) % 32 == 0), "fp8 consumer shape");
@@ -947,8 +944,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       break;
     }
     hd = s.hdr[stage];
-    bool paired = false;      // this iteration also takes the next stage (tensor-core consumer)
-    StageHeader hd_next = hd;
     if (hd.flags & kEnd) {
       more = false;
       break;
@@ -1158,33 +1153,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         }
         poison = false;
       }
-      // Two page tiles of the segment per iteration when this one is not its
-      // last (the next stage then holds the segment's next page): two
-      // independent QK^T chains, one softmax reduction over both pages' scores
-      // and two PV streams, which hides more of each tile's latency chain.
-      const bool pair = kPair && !(hd.flags & kLast);
-      int stage_b = stage + 1;
-      uint32_t phase_b = phase;
-      if (stage_b == NSTAGE) {
-        stage_b = 0;
-        phase_b ^= 1u;
-      }
-      StageHeader hd_b = hd;
-      if (pair) {
-        bool okb = wait_phase(&s.full[stage_b], phase_b, &s.abort_flag, a.status, kStatusFull, a.wait_limit);
-        okb = __all_sync(0xffffffffu, okb);
-        if (!okb) {
-          alive = false;
-          break;
-        }
-        hd_b = s.hdr[stage_b];
-        paired = true;
-        hd_next = hd_b;
-      }
-      if ((hd.flags & kBadPage) || (hd_b.flags & kBadPage)) {
+      if (hd.flags & kBadPage) {
         poison = true;
       } else {
-        // S3: S^T = K Q^T for this warp's 16 tokens of a page; even and odd
+        // S3: S^T = K Q^T for this warp's 16 tokens of the page; even and odd
         // k-steps accumulate separately (two short MMA chains instead of one).
         auto qk = [&](const uint32_t kbase, float (&sc)[NQT][2][4]) {
 #pragma unroll
@@ -1255,57 +1227,53 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           }
         }
         };
-        float sacc[2][NQT][2][4];
-        qk(smem_addr(s.k[stage]), sacc[0]);
-        if (pair) qk(smem_addr(s.k[stage_b]), sacc[1]);
-        // S4 + S5: mask and scale; online softmax per query column over the
-        // iteration's pages.  Lane holds tokens 16tg + gid (values 0, 1) and
-        // + 8 (values 2, 3) of queries 8n + 2tig (values 0, 2) and + 1 (values
-        // 1, 3).  Query row q of new token j sees the page's tokens t with
-        // beg <= t < end, end = rel_end - (q_len - 1 - j), beg = end - window
-        // (for single-token decode exactly [lo, hi)).
+        float sacc[NQT][2][4];
+        qk(smem_addr(s.k[stage]), sacc);
+        // S4 + S5: mask and scale; online softmax per query column.  Lane
+        // holds tokens 16tg + gid (values 0, 1) and + 8 (values 2, 3) of
+        // queries 8n + 2tig (values 0, 2) and + 1 (values 1, 3).  Query row q
+        // of new token j sees the page's tokens t with beg <= t < end,
+        // end = rel_end - (q_len - 1 - j), beg = end - window (for
+        // single-token decode exactly [lo, hi)).
         const int t_lo = 16 * tg + gid, t_hi = t_lo + 8;
         const int wlim = a.window > 0 ? a.window : (1 << 30);
-        float pr[2][NQT][4];
-        float al[NQT][2];
-        bool moved = false;
+        float sv[NQT][2][2];
+        bool up = false;  // some score above its column's running maximum
 #pragma unroll
         for (int n = 0; n < NQT; ++n) {
 #pragma unroll
           for (int jq = 0; jq < 2; ++jq) {
             const int q = 8 * n + 2 * tig + jq;
             const bool qok = q < hd.gq;
+            const int end = hd.rel_end - qoff[n][jq], beg = end - wlim;
             const float f = kFp8 ? sq[kFp8 ? n : 0][jq] : sl2;
-            float sv[2][2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const StageHeader& h = u ? hd_b : hd;
-              const int end = h.rel_end - qoff[n][jq], beg = end - wlim;
-              const bool ok_u = qok && (u == 0 || pair);
-              sv[u][0] = (ok_u && t_lo >= beg && t_lo < end) ? (sacc[u][n][0][jq] + sacc[u][n][1][jq]) * f : kNegInf;
-              sv[u][1] = (ok_u && t_hi >= beg && t_hi < end) ? (sacc[u][n][0][jq + 2] + sacc[u][n][1][jq + 2]) * f
-                                                             : kNegInf;
-            }
-            float mx = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float mn = fmaxf(mq[n][jq], mx);
-            const float mu = (mn == kNegInf) ? 0.f : mn;
-            al[n][jq] = exp2f(mq[n][jq] - mu);
-            moved |= al[n][jq] != 1.f;
-            float lsum = 0.f;
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              pr[u][n][jq] = exp2f(sv[u][0] - mu);
-              pr[u][n][jq + 2] = exp2f(sv[u][1] - mu);
-              lsum += pr[u][n][jq] + pr[u][n][jq + 2];
-            }
-            lq[n][jq] = lq[n][jq] * al[n][jq] + lsum;
-            mq[n][jq] = mn;
+            sv[n][jq][0] = (qok && t_lo >= beg && t_lo < end) ? (sacc[n][0][jq] + sacc[n][1][jq]) * f : kNegInf;
+            sv[n][jq][1] = (qok && t_hi >= beg && t_hi < end) ? (sacc[n][0][jq + 2] + sacc[n][1][jq + 2]) * f : kNegInf;
+            up |= fmaxf(sv[n][jq][0], sv[n][jq][1]) > mq[n][jq];
           }
         }
-        if (__any_sync(0xffffffffu, moved)) {
+        float pr[NQT][4];
+        if (__any_sync(0xffffffffu, up)) {
+          // A column maximum moves: reduce it over the 16 tokens (three
+          // shuffles), rescale l and O by 2^(m_old - m_new).
+          float al[NQT][2];
+#pragma unroll
+          for (int n = 0; n < NQT; ++n) {
+#pragma unroll
+            for (int jq = 0; jq < 2; ++jq) {
+              float mx = fmaxf(sv[n][jq][0], sv[n][jq][1]);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float mn = fmaxf(mq[n][jq], mx);
+              const float mu = (mn == kNegInf) ? 0.f : mn;
+              al[n][jq] = exp2f(mq[n][jq] - mu);
+              pr[n][jq] = exp2f(sv[n][jq][0] - mu);
+              pr[n][jq + 2] = exp2f(sv[n][jq][1] - mu);
+              lq[n][jq] = lq[n][jq] * al[n][jq] + pr[n][jq] + pr[n][jq + 2];
+              mq[n][jq] = mn;
+            }
+          }
 #pragma unroll
           for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
@@ -1315,8 +1283,21 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               oacc[mt][n][2] *= al[n][0];
               oacc[mt][n][3] *= al[n][1];
             }
+        } else {
+          // No maximum moves (the usual case once a segment is under way):
+          // the weights are taken against the running maxima as they stand.
+#pragma unroll
+          for (int n = 0; n < NQT; ++n) {
+#pragma unroll
+            for (int jq = 0; jq < 2; ++jq) {
+              const float mu = (mq[n][jq] == kNegInf) ? 0.f : mq[n][jq];
+              pr[n][jq] = exp2f(sv[n][jq][0] - mu);
+              pr[n][jq + 2] = exp2f(sv[n][jq][1] - mu);
+              lq[n][jq] += pr[n][jq] + pr[n][jq + 2];
+            }
+          }
         }
-        // S6: O^T[this warp's rows] += V^T P^T over a page's 16 tokens of
+        // S6: O^T[this warp's rows] += V^T P^T over the page's 16 tokens of
         // this warp.  V rows of masked tokens may hold anything (NaN in unused
         // slots) and 0 * NaN is NaN inside the MMA: clear those tokens in the
         // V^T fragments.  This lane's fragments carry tokens 16tg + 2tig (+1)
@@ -1422,8 +1403,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           }
         }
         };
-        pv(stage, hd, pr[0]);
-        if (pair) pv(stage_b, hd_b, pr[1]);
+        pv(stage, hd, pr);
       }
     }
 
@@ -1438,14 +1418,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     if (++stage == NSTAGE) {
       stage = 0;
       phase ^= 1u;
-    }
-    if (paired) {  // the iteration also consumed the next stage
-      if (lane == 0) mbar_arrive(&s.empty[stage]);
-      if (++stage == NSTAGE) {
-        stage = 0;
-        phase ^= 1u;
-      }
-      hd = hd_next;
     }
   } while (!(hd.flags & kLast));
   if (!alive || !more) break;
