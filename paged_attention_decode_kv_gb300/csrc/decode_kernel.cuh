@@ -149,7 +149,10 @@ struct PendingCombine {
   long long item_u;
 };
 
-template <int D, typename T, int G, int NCW, int NSTAGE, Math M>
+// Shared memory of a CTA.  The stage ring (k, v) sits last, followed by EXT
+// spare bytes: once the tiles are done, k, v and ext form one contiguous
+// buffer the split-KV combine stages partial records into.
+template <int D, typename T, int G, int NCW, int NSTAGE, Math M, int EXT = 0>
 struct Smem {
   // CUDA-core layout: lane c of a row group owns 8 elements of every row.
   static constexpr int GS = D / 8;
@@ -159,8 +162,6 @@ struct Smem {
   // NCW / 2 head_dim parts.
   static constexpr int NDP = (M != Math::kSimt) ? NCW / 2 : 1;
   static constexpr int kRedRows = (M == Math::kSimt) ? NG : 2;
-  alignas(1024) KvElem<T, M> k[NSTAGE][kPageTokens * D];
-  alignas(1024) KvElem<T, M> v[NSTAGE][kPageTokens * D];
   alignas(128) T q[NSTAGE][G * D];
   // head_dim 512 (bf16 tensor cores): the Q^T fragments of 32 k-steps do not
   // fit in registers, so the segment's query rows are copied into this
@@ -195,6 +196,9 @@ struct Smem {
   PendingCombine pend[2];
   int pend_n;
   volatile int abort_flag;
+  alignas(1024) KvElem<T, M> k[NSTAGE][kPageTokens * D];
+  alignas(1024) KvElem<T, M> v[NSTAGE][kPageTokens * D];
+  alignas(16) unsigned char ext[EXT > 0 ? EXT : 16];
 };
 
 // ---------------------------------------------------------------------------
@@ -567,11 +571,11 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, typename T, int G, int NCW, int NSTAGE, int MINB, Math MATH>
+template <int D, typename T, int G, int NCW, int NSTAGE, int MINB, Math MATH, int EXT>
 __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const DecodeArgs a) {
-  using S = Smem<D, T, G, NCW, NSTAGE, MATH>;
+  using S = Smem<D, T, G, NCW, NSTAGE, MATH, EXT>;
   constexpr int NT = (NCW + 1) * 32;
   constexpr int NC = NCW * 32;  // consumer threads
   using KV = KvElem<T, MATH>;
@@ -580,6 +584,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr bool kMma = MATH != Math::kSimt;
   constexpr bool kFp8 = MATH == Math::kMma8;
   constexpr bool kQSmem = S::QS;
+  // Independent QK^T accumulator chains per query n-tile: k-step i feeds
+  // chain i mod kQAcc (each MMA waits on the one before it in its chain).
+  constexpr int kQAcc = (kMma && G <= 8) ? 4 : 2;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
                 "mma consumer shape");
   static_assert(!kFp8 || (D % 128 == 0 && (D / (NCW / 2)) % 32 == 0), "fp8 consumer shape");
@@ -1158,11 +1165,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       } else {
         // S3: S^T = K Q^T for this warp's 16 tokens of the page; even and odd
         // k-steps accumulate separately (two short MMA chains instead of one).
-        auto qk = [&](const uint32_t kbase, float (&sc)[NQT][2][4]) {
+        auto qk = [&](const uint32_t kbase, float (&sc)[NQT][kQAcc][4]) {
 #pragma unroll
           for (int n = 0; n < NQT; ++n)
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int hh = 0; hh < kQAcc; ++hh)
 #pragma unroll
               for (int e = 0; e < 4; ++e) sc[n][hh][e] = 0.f;
         if constexpr (kFp8) {
@@ -1182,8 +1189,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
             for (int n = 0; n < NQT; ++n) {
-              mma_e4m3(sc[n][0], ak, qb[2 * kp][n][0], qb[2 * kp][n][1]);
-              mma_e4m3(sc[n][1], ak, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
+              mma_e4m3(sc[n][(2 * kp) % kQAcc], ak, qb[2 * kp][n][0], qb[2 * kp][n][1]);
+              mma_e4m3(sc[n][(2 * kp + 1) % kQAcc], ak, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
             }
           }
         } else if constexpr (kQSmem) {
@@ -1210,7 +1217,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               uint32_t ak[4];
               ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
-              for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][h2], ak, qf[n][2 * h2], qf[n][2 * h2 + 1]);
+              for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][(ks + h2) % kQAcc], ak, qf[n][2 * h2], qf[n][2 * h2 + 1]);
             }
           }
         } else {
@@ -1223,11 +1230,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             uint32_t ak[4];
             ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
-            for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][ks & 1], ak, qb[ks][n][0], qb[ks][n][1]);
+            for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][ks % kQAcc], ak, qb[ks][n][0], qb[ks][n][1]);
           }
         }
         };
-        float sacc[NQT][2][4];
+        float sacc[NQT][kQAcc][4];
         qk(smem_addr(s.k[stage]), sacc);
         // S4 + S5: mask and scale; online softmax per query column.  Lane
         // holds tokens 16tg + gid (values 0, 1) and + 8 (values 2, 3) of
@@ -1247,8 +1254,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const bool qok = q < hd.gq;
             const int end = hd.rel_end - qoff[n][jq], beg = end - wlim;
             const float f = kFp8 ? sq[kFp8 ? n : 0][jq] : sl2;
-            sv[n][jq][0] = (qok && t_lo >= beg && t_lo < end) ? (sacc[n][0][jq] + sacc[n][1][jq]) * f : kNegInf;
-            sv[n][jq][1] = (qok && t_hi >= beg && t_hi < end) ? (sacc[n][0][jq + 2] + sacc[n][1][jq + 2]) * f : kNegInf;
+            float s0 = sacc[n][0][jq], s1 = sacc[n][0][jq + 2];
+#pragma unroll
+            for (int c = 1; c < kQAcc; ++c) {
+              s0 += sacc[n][c][jq];
+              s1 += sacc[n][c][jq + 2];
+            }
+            sv[n][jq][0] = (qok && t_lo >= beg && t_lo < end) ? s0 * f : kNegInf;
+            sv[n][jq][1] = (qok && t_hi >= beg && t_hi < end) ? s1 * f : kNegInf;
             up |= fmaxf(sv[n][jq][0], sv[n][jq][1]) > mq[n][jq];
           }
         }
@@ -1651,7 +1664,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   if (!cons_sync()) return;  // pend_n was written by thread 0
   const int n_pend = s.pend_n;
   float* const ring = reinterpret_cast<float*>(&s.k[0][0]);
-  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(KV);
+  constexpr size_t kRingBytes = 2ull * NSTAGE * kPageTokens * D * sizeof(KV) + EXT;  // k, v and ext
   constexpr int kRowChunks = D / 4;  // float4 chunks of a row
   constexpr int kOwn = (G * kRowChunks + NC - 1) / NC;
   static_assert(kRingBytes >= static_cast<size_t>(G) * (4 + D) * 4, "the ring must hold a partial record");

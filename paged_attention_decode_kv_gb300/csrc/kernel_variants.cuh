@@ -36,12 +36,25 @@ struct StagePick<D, T, G, NCW, MINB, M, 0> {
   static constexpr int value = 0;
 };
 
+// Spare shared memory (bytes, multiple of 1024, at most 64 KB) a CTA with
+// this ring still has within its share of the SM: the split-KV combine
+// stages partial records into the ring plus these bytes.
+template <int D, typename T, int G, int NCW, int MINB, Math M, int NSTAGE>
+struct ExtPick {
+  static constexpr size_t budget = kSmemPerSm / MINB - kSmemReservedPerCta - 1024;
+  static constexpr size_t used = sizeof(Smem<D, T, G, NCW, NSTAGE, M, 0>) - 1024;  // without ext's own KB
+  static constexpr size_t spare = budget > used ? (budget - used) / 1024 * 1024 : 0;
+  static constexpr int value = static_cast<int>(spare < 65536 ? spare : 65536);
+};
+
 template <int D, typename T, int G, int NCW, int MINB, int MAXST, Math M>
 struct Variant {
   static constexpr int NSTAGE = StagePick<D, T, G, NCW, MINB, M, MAXST>::value;
   static_assert(NSTAGE >= 2, "variant does not fit two stages in shared memory");
-  using S = Smem<D, T, G, NCW, NSTAGE, M>;
+  static constexpr int EXT = ExtPick<D, T, G, NCW, MINB, M, NSTAGE>::value;
+  using S = Smem<D, T, G, NCW, NSTAGE, M, EXT>;
   static constexpr size_t smem = sizeof(S) + 1024;
+  static_assert((smem + kSmemReservedPerCta) * MINB <= kSmemPerSm, "variant does not fit its CTAs per SM");
 
   // overlap: launch as a programmatic dependent of the previous kernel on the
   // stream, so this grid's CTAs may start (and read context lengths and block
@@ -58,7 +71,7 @@ struct Variant {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M>, tk, tv, args);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M, EXT>, tk, tv, args);
   }
 
   static VariantInfo info() {
@@ -71,7 +84,7 @@ struct Variant {
                        (NCW + 1) * 32,
                        MINB,
                        smem,
-                       reinterpret_cast<const void*>(&paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M>),
+                       reinterpret_cast<const void*>(&paged_decode_kernel<D, T, G, NCW, NSTAGE, MINB, M, EXT>),
                        &launch};
   }
 };
