@@ -171,18 +171,20 @@ class ClockSampler:
 ROTATE_BYTES = 256 << 20  # distinct KV bytes read between two uses of the same pool copy (2x L2)
 
 
-def make_device_case(name: str, seed: int, device, pool_blocks: int = 0):
+def make_device_case(name: str, seed: int, device, pool_blocks: int = 0, copies: int = 0):
     """The workload on the device, with enough copies of its KV pool that
     consecutive calls never find their pages in L2: copy c serves calls
     c, c + n, ..., and n copies hold >= 2x L2 of referenced KV bytes.
-    pool_blocks > 0 shrinks the page pool (same contexts and pages used)."""
+    pool_blocks > 0 shrinks the page pool (same contexts and pages used);
+    copies > 0 fixes the number of pool copies (profiler runs, where the
+    profiler cleans the caches before each captured launch, use one)."""
     from paged_attention_decode_kv_gb300 import workloads as W
     w = W.WORKLOADS[name]
     if pool_blocks > 0:
         w = w.with_(pool_blocks=pool_blocks)
     case = W.make_case(w, seed)
     k, v = case.pool(device)
-    n_copies = max(2, -(-ROTATE_BYTES // max(case.kv_bytes(), 1)) + 1)
+    n_copies = copies if copies > 0 else max(2, -(-ROTATE_BYTES // max(case.kv_bytes(), 1)) + 1)
     pools = [(k, v)] + [(k.clone(), v.clone()) for _ in range(n_copies - 1)]
     t = {"q": case.q.to(device), "pools": pools, "k": k, "v": v,
          "bt": case.block_tables.to(device), "cl": case.context_lens.to(device)}
@@ -459,7 +461,7 @@ def run_profile_only(args):
     from paged_attention_decode_kv_gb300 import build_lib
     build_lib.build()
     dev = torch.device("cuda", 0)
-    case, t = make_device_case(args.workload, args.seed, dev, args.pool_blocks)
+    case, t = make_device_case(args.workload, args.seed, dev, args.pool_blocks, copies=1)
     w = case.workload
     out = torch.empty_like(t["q"])
     for i in range(args.warmup + args.steps):
