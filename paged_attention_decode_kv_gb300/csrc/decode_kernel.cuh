@@ -69,7 +69,9 @@ constexpr float kPScale = 256.f;
 constexpr int kPrefetchTiles = 8;
 
 // Stage flags written by the producer.
-enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8, kEnd = 16 };  // kEnd: no more tiles
+// kEnd: no more tiles; kPad: a stage without tiles that only closes a segment
+// for a warp pair (see Smem::NPAR).
+enum : int { kFirst = 1, kLast = 2, kSplit = 4, kBadPage = 8, kEnd = 16, kPad = 32 };
 
 // Status bits (global status word).
 enum : unsigned {
@@ -158,10 +160,17 @@ struct Smem {
   static constexpr int GS = D / 8;
   static constexpr int NG = (M == Math::kSimt) ? NCW * 32 / GS : 1;
   static constexpr int TPG = kPageTokens / NG;
-  // mma layout: warps split the page into (token half tg) x (head_dim part dp),
-  // NCW / 2 head_dim parts.
-  static constexpr int NDP = (M != Math::kSimt) ? NCW / 2 : 1;
-  static constexpr int kRedRows = (M == Math::kSimt) ? NG : 2;
+  // mma layout: warps split the page into (token half tg) x (head_dim part
+  // dp).  With NPAR = 2 the warps also form two pairs of alternate pages:
+  // pair par takes the ring stages s with s mod 2 = par, so two pages are in
+  // flight per CTA and no head_dim part repeats another's QK^T and softmax
+  // (FP8 K/V with four consumer warps: its per-tile instruction count, not
+  // the bytes, bounds it).  The producer gives every segment an even number
+  // of stages (closing odd ones with a kPad stage), so segments start on even
+  // stages.
+  static constexpr int NPAR = (M == Math::kMma8 && G <= 8 && NCW == 4) ? 2 : 1;
+  static constexpr int NDP = (M != Math::kSimt) ? NCW / (2 * NPAR) : 1;
+  static constexpr int kRedRows = (M == Math::kSimt) ? NG : 2 * NPAR;
   alignas(128) T q[NSTAGE][G * D];
   // head_dim 512 (bf16 tensor cores): the Q^T fragments of 32 k-steps do not
   // fit in registers, so the segment's query rows are copied into this
@@ -170,12 +179,14 @@ struct Smem {
   static constexpr bool QS = (M == Math::kMma) && D >= 512;
   alignas(1024) T qs[QS ? G * D : 8];
   // Tensor-core epilogue: warps of token half 1 hand their O^T accumulator
-  // fragments to the warps of token half 0 ([segment parity][dp][m-tile][lane]);
-  // token half 0 then reuses its slice to stage rows for coalesced stores.
+  // fragments to the warps of token half 0 ([segment parity][dp][slot][m-tile]
+  // [lane]); token half 0 then reuses the slice to stage rows for coalesced
+  // stores.  With NPAR = 2 the second pair first hands its fragments to the
+  // first (slot tg), then token half 1 of the first pair uses slot 1.
   static constexpr int XV = (G > 8) ? 8 : 4;  // accumulator values per lane and m-tile
   static constexpr int XP = (M != Math::kSimt) ? 2 : 1;
   static constexpr int XN = (M != Math::kSimt) ? D / NDP / 16 : 1;
-  alignas(16) float xbuf[XP][NDP][XN][32][XV];
+  alignas(16) float xbuf[XP][NDP][NPAR][XN][32][XV];
   // CUDA-core consumer only: per-group broadcast of p and the rescale factor.
   static constexpr int PG = (M == Math::kSimt) ? G : 1;
   static constexpr int PT = (M == Math::kSimt) ? TPG : 1;
@@ -587,9 +598,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   // Independent QK^T accumulator chains per query n-tile: k-step i feeds
   // chain i mod kQAcc (each MMA waits on the one before it in its chain).
   constexpr int kQAcc = (kMma && G <= 8) ? 4 : 2;
-  static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / (NCW / 2)) % 16 == 0),
+  constexpr int NPAR = S::NPAR;
+  static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / S::NDP) % 16 == 0),
                 "mma consumer shape");
-  static_assert(!kFp8 || (D % 128 == 0 && (D / (NCW / 2)) % 32 == 0), "fp8 consumer shape");
+  static_assert(!kFp8 || (D % 128 == 0 && (D / S::NDP) % 32 == 0), "fp8 consumer shape");
+  static_assert(NSTAGE % NPAR == 0, "alternate-page pairs need an even ring");
   static_assert(kMma || (S::GS <= 32 && (32 % S::GS) == 0 && S::NG * S::TPG == kPageTokens &&
                          G <= S::GS && (S::GS % G) == 0), "CUDA-core consumer shape");
 
@@ -623,7 +636,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   if (tid == 0) {
     for (int st = 0; st < NSTAGE; ++st) {
       mbar_init(&s.full[st], 1);
-      mbar_init(&s.empty[st], NCW);
+      mbar_init(&s.empty[st], NCW / NPAR);  // the warps of the stage's pair
     }
     mbar_init(&s.csync, NCW);  // one arrival per consumer warp
     mbar_init(&s.comb, 1);
@@ -748,6 +761,73 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         const int qr0 = sub * G;  // first query row of this subgroup
         const int gq = min(G, a.rows - qr0);
         const int* bt_row = a.block_tables + static_cast<size_t>(b) * a.max_blocks + sp.p_lo;
+        // Segment stages: the item's pages, plus a kPad stage when NPAR = 2
+        // and the count is odd.  The first NPAR stages carry the query rows
+        // (kFirst) and the last NPAR close the segment (kLast), one of each
+        // per warp pair.
+        const int nst = (pb - pa + NPAR - 1) / NPAR * NPAR;
+        auto put = [&](int pid, int p, bool pad) -> bool {
+          if (static_cast<int>(blockIdx.x) == a.withhold_cta && issued == a.withhold_tile) {
+            withheld = true;  // test hook: this tile never arrives
+            return false;
+          }
+          bool live = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty, a.wait_limit);
+          live = __all_sync(0xffffffffu, live);
+          if (!live) return false;
+          const int i = p - pa;  // stage of the segment
+          const bool first = i < NPAR;
+          const bool bad = !pad && (pid < 0 || pid >= a.num_blocks);
+          if (lane == 0) {
+            const int first_tok = (sp.p_lo + p) * kPageTokens;
+            StageHeader& hd = s.hdr[stage];
+            hd.b = b;
+            hd.vh = vh;
+            hd.lo = pad ? 0 : max(sp.t0 - first_tok, 0);
+            hd.hi = pad ? 0 : min(sp.L - first_tok, kPageTokens);
+            hd.rel_end = pad ? 0 : sp.L - first_tok;
+            hd.flags = (first ? kFirst : 0) | (i >= nst - NPAR ? kLast : 0) | (nsplit > 1 ? kSplit : 0) |
+                       (bad ? kBadPage : 0) | (pad ? kPad : 0);
+            hd.gq = gq;
+            hd.nsplit = nsplit;
+            hd.slot = slot;
+            hd.c_first = c_first;
+            hd.item_u = item_u;
+            uint32_t bytes = (bad || pad) ? 0u : 2u * kTileBytes;
+            if (first) bytes += static_cast<uint32_t>(gq) * D * sizeof(T);
+            mbar_arrive_expect_tx(&s.full[stage], bytes);
+          }
+          __syncwarp();
+          // One tensor copy per K (or V) tile, each issued by its own lane.
+          // bf16 boxes cover (64 columns, 32 tokens, D/64 column blocks) of one
+          // head, landing as D/64 swizzled [token][64] sub-tiles; fp8 boxes
+          // the same with 128-code column blocks.
+          if (!bad && !pad && lane < 2) {
+            const bool is_v = lane == 1;
+            KV* dst = is_v ? s.v[stage] : s.k[stage];
+            if constexpr (kMma)
+              tma_load_4d(dst, is_v ? &tmap_v : &tmap_k, 0, pid * kPageTokens, 0, h, &s.full[stage]);
+            else
+              tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, 0, h, pid * kPageTokens, &s.full[stage]);
+          }
+          if (first && lane >= 16) {
+            // The subgroup's rows, one bulk copy per new token they cover
+            // (one copy in all for single-token decode).
+            const int j = qr0 / a.group + (lane - 16);
+            const int lo = max(j * a.group, qr0), hi = min(j * a.group + a.group, qr0 + gq);
+            if (hi > lo) {
+              const T* qsrc = static_cast<const T*>(a.q) + q_row(a, b, h, lo) * D;
+              bulk_load(s.q[stage] + (lo - qr0) * D, qsrc, static_cast<uint32_t>(hi - lo) * D * sizeof(T),
+                        &s.full[stage]);
+            }
+          }
+          __syncwarp();
+          ++issued;
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          return true;
+        };
         for (int p0 = pa; ok && p0 < pb; p0 += 32) {
           const int my_p = p0 + lane;
           const int my_id = (my_p < pb) ? __ldg(bt_row + my_p) : 0;
@@ -774,67 +854,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           const int n = min(32, pb - p0);
           for (int jj = 0; jj < n; ++jj) {
             const int pid = __shfl_sync(0xffffffffu, my_id, jj);
-            const int p = p0 + jj;
-            if (static_cast<int>(blockIdx.x) == a.withhold_cta && issued == a.withhold_tile) {
-              withheld = true;  // test hook: this tile never arrives
-              ok = false;
-              break;
-            }
-            ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty, a.wait_limit);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = put(pid, p0 + jj, false);
             if (!ok) break;
-            const bool bad = pid < 0 || pid >= a.num_blocks;
-            if (lane == 0) {
-              const int first_tok = (sp.p_lo + p) * kPageTokens;
-              StageHeader& hd = s.hdr[stage];
-              hd.b = b;
-              hd.vh = vh;
-              hd.lo = max(sp.t0 - first_tok, 0);
-              hd.hi = min(sp.L - first_tok, kPageTokens);
-              hd.rel_end = sp.L - first_tok;
-              hd.flags = (p == pa ? kFirst : 0) | (p == pb - 1 ? kLast : 0) | (nsplit > 1 ? kSplit : 0) |
-                         (bad ? kBadPage : 0);
-              hd.gq = gq;
-              hd.nsplit = nsplit;
-              hd.slot = slot;
-              hd.c_first = c_first;
-              hd.item_u = item_u;
-              uint32_t bytes = bad ? 0u : 2u * kTileBytes;
-              if (p == pa) bytes += static_cast<uint32_t>(gq) * D * sizeof(T);
-              mbar_arrive_expect_tx(&s.full[stage], bytes);
-            }
-            __syncwarp();
-            // One tensor copy per K (or V) tile, each issued by its own lane.
-            // bf16 boxes cover (64 columns, 32 tokens, D/64 column blocks) of one
-            // head, landing as D/64 swizzled [token][64] sub-tiles; fp8 boxes
-            // the same with 128-code column blocks.
-            if (!bad && lane < 2) {
-              const bool is_v = lane == 1;
-              KV* dst = is_v ? s.v[stage] : s.k[stage];
-              if constexpr (kMma)
-                tma_load_4d(dst, is_v ? &tmap_v : &tmap_k, 0, pid * kPageTokens, 0, h, &s.full[stage]);
-              else
-                tma_load_3d(dst, is_v ? &tmap_v : &tmap_k, 0, h, pid * kPageTokens, &s.full[stage]);
-            }
-            if (p == pa && lane >= 16) {
-              // The subgroup's rows, one bulk copy per new token they cover
-              // (one copy in all for single-token decode).
-              const int j = qr0 / a.group + (lane - 16);
-              const int lo = max(j * a.group, qr0), hi = min(j * a.group + a.group, qr0 + gq);
-              if (hi > lo) {
-                const T* qsrc = static_cast<const T*>(a.q) + q_row(a, b, h, lo) * D;
-                bulk_load(s.q[stage] + (lo - qr0) * D, qsrc, static_cast<uint32_t>(hi - lo) * D * sizeof(T),
-                          &s.full[stage]);
-              }
-            }
-            __syncwarp();
-            ++issued;
-            if (++stage == NSTAGE) {
-              stage = 0;
-              phase ^= 1u;
-            }
           }
         }
+        // An odd segment gets one more stage, without tiles, for the second pair.
+        if (NPAR == 2 && ok && ((pb - pa) & 1)) ok = put(0, pb, true);
       }
       u = cum + off_end;
       cum += ub;
@@ -852,20 +877,27 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
     // The consumers learn that the work is over from one more stage that
     // carries no tiles (how many pages the slice holds depends on the items
     // it crosses).
-    bool end_sent = false;
+    int n_end = 0;  // end stages sent, one per warp pair
     if (ok && __all_sync(0xffffffffu, !s.abort_flag)) {
-      ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty, a.wait_limit);
-      end_sent = __all_sync(0xffffffffu, ok);
-      if (end_sent && lane == 0) {
-        s.hdr[stage].flags = kEnd;
-        mbar_arrive(&s.full[stage]);
+      for (int e = 0; e < NPAR; ++e) {
+        ok = wait_phase(&s.empty[stage], phase ^ 1u, &s.abort_flag, a.status, kStatusEmpty, a.wait_limit);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0) {
+          s.hdr[stage].flags = kEnd;
+          mbar_arrive(&s.full[stage]);
+        }
+        ++n_end;
+        if (++stage == NSTAGE) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
-    // Let every copy this warp issued land before the CTA can exit.  Once the
+    // Let every copy this warp issued land before the CTA can exit.  Once an
     // end stage went out, its own stage's last tile had been released, and
     // its full barrier has moved on a phase: drain only the others.
     if (lane == 0) {
-      const long long cap = end_sent ? NSTAGE - 1 : NSTAGE;
+      const long long cap = NSTAGE - n_end;
       const long long n_drain = issued < cap ? issued : cap;
       for (long long k = 1; k <= n_drain; ++k) {
         const long long idx = issued - k;  // stage index of the k-th most recent copy
@@ -918,12 +950,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int kKSteps = D / 16;        // k-steps of S^T over head_dim
   constexpr int kMt = kDPart / 16;       // 16-row m-tiles of O^T per warp
   constexpr int NQT = (G > 8) ? 2 : 1;   // 8-query n-tiles
-  const int tg = warp & 1, dp = warp >> 1;
+  const int tg = warp & 1, par = (warp >> 1) % NPAR, dp = warp / (2 * NPAR);
   const int gid = lane >> 2, tig = lane & 3;
 
-  int stage = 0;
+  int stage = kMma ? par : 0;  // a warp pair walks its own stages of the ring
   uint32_t phase = 0;
-  int par = 0, seg_par = 0;
+  int pbuf_par = 0, seg_par = 0;
   bool alive = true, more = true;
   // One iteration per (sequence, virtual head) segment: the query fragments
   // and accumulators are scoped to it, so they are dead in the epilogue.
@@ -983,7 +1015,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       }
       if (hd.flags & kBadPage) {
         poison = true;
-      } else {
+      } else if (!(hd.flags & kPad)) {
         const int end_q = hd.rel_end - qoff[0][0];                      // keys t < end_q
         const int beg_q = a.window > 0 ? end_q - a.window : -(1 << 30);  // and t >= beg_q
         const T* ks = s.k[stage];
@@ -1022,14 +1054,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         m_run = m_new;
         if (owner) {
 #pragma unroll
-          for (int tt = 0; tt < TPG; ++tt) s.pbuf[par][j][iq][tt] = p[tt];
-          s.abuf[par][j][iq] = alpha;
+          for (int tt = 0; tt < TPG; ++tt) s.pbuf[pbuf_par][j][iq][tt] = p[tt];
+          s.abuf[pbuf_par][j][iq] = alpha;
         }
         __syncwarp();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
           for (int i = 0; i < G; ++i) {
-            const float ai = s.abuf[par][j][i];
+            const float ai = s.abuf[pbuf_par][j][i];
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[i][e] *= ai;
           }
@@ -1042,13 +1074,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             Map::load(vs + t * D, c, vx);
 #pragma unroll
             for (int i = 0; i < G; ++i) {
-              const float pi = s.pbuf[par][j][i][tt];
+              const float pi = s.pbuf[pbuf_par][j][i][tt];
 #pragma unroll
               for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pi, vx[e], acc[i][e]);
             }
           }
         }
-        par ^= 1;
+        pbuf_par ^= 1;
       }
     } else {
       // ======================== tensor-core consumer ==========================
@@ -1162,7 +1194,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       }
       if (hd.flags & kBadPage) {
         poison = true;
-      } else {
+      } else if (!(hd.flags & kPad)) {
         // S3: S^T = K Q^T for this warp's 16 tokens of the page; even and odd
         // k-steps accumulate separately (two short MMA chains instead of one).
         auto qk = [&](const uint32_t kbase, float (&sc)[NQT][kQAcc][4]) {
@@ -1340,41 +1372,39 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             pb[n][0] = hi;
             pb[n][1] = f16x2_to_e4m3x2(r0) | (f16x2_to_e4m3x2(r1) << 16);
           }
-          // V^T A fragments: each lane reads the 4-byte codes of columns
-          // c0 + 4gid .. +3 for tokens 2tig, 2tig + 1, 2tig + 8, 2tig + 9
-          // (bank-conflict free under the swizzle) and transposes the 4x4
-          // bytes with byte permutes: one register per column, four tokens
-          // each.  A 32-column block makes two m-tiles whose rows are columns
-          // c0 + 4gid + {0, 1} and c0 + 4gid + {2, 3} (gid, gid + 8).  Codes
-          // of tokens outside the page's range are cleared (they may be NaN).
+          // V^T A fragments by ldmatrix.trans over byte pairs: an 8x8 matrix of
+          // 16-bit elements is 8 tokens x 16 codes, and transposed a lane gets
+          // codes 2gid, 2gid + 1 of tokens 2tig and 2tig + 1.  With the
+          // matrices of tokens 0-7 and 8-15 of the warp's 16, two byte
+          // permutes give one register per code column holding tokens 2tig,
+          // 2tig + 1, 2tig + 8, 2tig + 9 (the order of the P^T codes).  So
+          // rows gid and gid + 8 of m-tile mt are columns 16mt + 2gid and
+          // 16mt + 2gid + 1 of the warp's part.  Codes of tokens outside the
+          // page's range are cleared (they may be NaN).
           const uint32_t m8 = ((tl >= h.lo && tl < h.hi) ? 0x000000ffu : 0u) |
                               ((tl + 1 >= h.lo && tl + 1 < h.hi) ? 0x0000ff00u : 0u) |
                               ((tl + 8 >= h.lo && tl + 8 < h.hi) ? 0x00ff0000u : 0u) |
                               ((tl + 9 >= h.lo && tl + 9 < h.hi) ? 0xff000000u : 0u);
+          const int mi = lane >> 3, r = lane & 7;
+          const int t = 16 * tg + ((mi & 1) << 3) + r;  // token row this lane addresses
+          const uint32_t vrow = smem_addr(s.v[st]) + t * 128;
 #pragma unroll
-          for (int cb = 0; cb < kDPart / 32; ++cb) {
-            const int byte = dp * kDPart + cb * 32 + 4 * gid;
-            const int sb = byte >> 7, chunk = (byte & 127) >> 4, within = byte & 15;
-            uint32_t w[4];
+          for (int mp = 0; mp < kMt / 2; ++mp) {  // two 16-code blocks per ldmatrix.x4
+            const int byte = dp * kDPart + mp * 32 + ((mi >> 1) << 4);
+            const int sb = byte >> 7, chunk = (byte & 127) >> 4;
+            uint32_t w[4];  // (tokens 0-7, 8-15) of block 2mp, then of block 2mp + 1
+            ldmatrix_x4_trans(vrow + sb * (kPageTokens * 128) + ((chunk ^ (t & 7)) << 4), w);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int t = tl + (u & 1) + ((u >> 1) << 3);  // 2tig, +1, +8, +9
-              w[u] = *reinterpret_cast<const uint32_t*>(&s.v[st][0] + sb * (kPageTokens * 128) + t * 128 +
-                                                        ((chunk ^ (t & 7)) << 4) + within);
-            }
-            const uint32_t x01 = __byte_perm(w[0], w[1], 0x5140u), x23 = __byte_perm(w[2], w[3], 0x5140u);
-            const uint32_t y01 = __byte_perm(w[0], w[1], 0x7362u), y23 = __byte_perm(w[2], w[3], 0x7362u);
-            uint32_t col[4] = {__byte_perm(x01, x23, 0x5410u), __byte_perm(x01, x23, 0x7632u),
-                               __byte_perm(y01, y23, 0x5410u), __byte_perm(y01, y23, 0x7632u)};
-            if (!full_page) {
+            for (int hb = 0; hb < 2; ++hb) {
+              uint32_t c0 = __byte_perm(w[2 * hb], w[2 * hb + 1], 0x6420u);  // column 2gid
+              uint32_t c1 = __byte_perm(w[2 * hb], w[2 * hb + 1], 0x7531u);  // column 2gid + 1
+              if (!full_page) {
+                c0 &= m8;
+                c1 &= m8;
+              }
+              const uint32_t av[4] = {c0, c1, c0, c1};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) col[e] &= m8;
-            }
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {  // columns {0, 1} then {2, 3} of the lane's four
-              const uint32_t av[4] = {col[2 * half], col[2 * half + 1], col[2 * half], col[2 * half + 1]};
-#pragma unroll
-              for (int n = 0; n < NQT; ++n) mma_e4m3(oacc[2 * cb + half][n], av, pb[n][0], pb[n][1]);
+              for (int n = 0; n < NQT; ++n) mma_e4m3(oacc[2 * mp + hb][n], av, pb[n][0], pb[n][1]);
             }
           }
         } else {
@@ -1428,8 +1458,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       hold_stage = stage;
     else if (lane == 0)
       mbar_arrive(&s.empty[stage]);
-    if (++stage == NSTAGE) {
-      stage = 0;
+    stage += NPAR;
+    if (stage >= NSTAGE) {
+      stage -= NSTAGE;
       phase ^= 1u;
     }
   } while (!(hd.flags & kLast));
@@ -1542,7 +1573,58 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         lfull[n][jq] = l;
       }
-    if (dp == 0 && gid == 0) {
+    if constexpr (NPAR == 2) {
+      // ---- the second warp pair hands its partial to the first ----
+      float* xa = &s.xbuf[xp][dp][tg][0][0][0];
+      if (par == 1) {
+        if (dp == 0 && gid == 0) {
+#pragma unroll
+          for (int n = 0; n < NQT; ++n)
+#pragma unroll
+            for (int jq = 0; jq < 2; ++jq) {
+              const int q = 8 * n + 2 * tig + jq;
+              rm[2 + tg][q] = mq[n][jq];
+              rl[2 + tg][q] = poison ? kNaN : lfull[n][jq];
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+          for (int n = 0; n < NQT; ++n)
+            *reinterpret_cast<float4*>(xa + (mt * 32 + lane) * S::XV + 4 * n) =
+                make_float4(oacc[mt][n][0], oacc[mt][n][1], oacc[mt][n][2], oacc[mt][n][3]);
+      }
+      if (!cons_sync()) break;
+      if (par == 0) {
+        // (m, l, O) of both pairs against their larger maximum; a pair that
+        // saw no key of a row (m = -inf) weighs nothing
+        float f0[NQT][2], f1[NQT][2];
+#pragma unroll
+        for (int n = 0; n < NQT; ++n)
+#pragma unroll
+          for (int jq = 0; jq < 2; ++jq) {
+            const int q = 8 * n + 2 * tig + jq;
+            const float m1 = rm[2 + tg][q];
+            const float Mx = fmaxf(mq[n][jq], m1);
+            const float Ms = (Mx == kNegInf) ? 0.f : Mx;
+            f0[n][jq] = exp2f(mq[n][jq] - Ms);
+            f1[n][jq] = exp2f(m1 - Ms);
+            lfull[n][jq] = lfull[n][jq] * f0[n][jq] + rl[2 + tg][q] * f1[n][jq];
+            mq[n][jq] = Mx;
+          }
+#pragma unroll
+        for (int mt = 0; mt < kMt; ++mt)
+#pragma unroll
+          for (int n = 0; n < NQT; ++n) {
+            const float4 x = *reinterpret_cast<const float4*>(xa + (mt * 32 + lane) * S::XV + 4 * n);
+            oacc[mt][n][0] = oacc[mt][n][0] * f0[n][0] + x.x * f1[n][0];
+            oacc[mt][n][1] = oacc[mt][n][1] * f0[n][1] + x.y * f1[n][1];
+            oacc[mt][n][2] = oacc[mt][n][2] * f0[n][0] + x.z * f1[n][0];
+            oacc[mt][n][3] = oacc[mt][n][3] * f0[n][1] + x.w * f1[n][1];
+          }
+      }
+    }
+    if (par == 0 && dp == 0 && gid == 0) {
 #pragma unroll
       for (int n = 0; n < NQT; ++n)
 #pragma unroll
@@ -1554,8 +1636,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           }
         }
     }
-    float* xb = &s.xbuf[xp][dp][0][0][0];  // this dp's slice: kMt * 32 * XV floats
-    if (tg == 1) {
+    // this dp's slice (kMt * 32 * XV floats); with two pairs, slot 1, which
+    // only token half 1 of the first pair touched since the last rendezvous
+    float* xb = &s.xbuf[xp][dp][NPAR - 1][0][0][0];
+    if (par == 0 && tg == 1) {
 #pragma unroll
       for (int mt = 0; mt < kMt; ++mt)
 #pragma unroll
@@ -1564,7 +1648,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               make_float4(oacc[mt][n][0], oacc[mt][n][1], oacc[mt][n][2], oacc[mt][n][3]);
     }
     if (!cons_sync()) break;
-    if (tg == 0) {
+    if (par == 0 && tg == 0) {
       // merge the two token halves for this warp's queries and O^T rows
       float f0[NQT][2], f1[NQT][2], inv[NQT][2];
 #pragma unroll
@@ -1610,9 +1694,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int q = 8 * n + 2 * tig + (e & 1);
-            // bf16: m-tile rows are 16 consecutive head_dim columns; fp8: the
-            // columns of a 32-column block interleave (see S6)
-            const int dl = kFp8 ? 32 * (mt >> 1) + 4 * gid + 2 * (mt & 1) + (e >> 1) : mt * 16 + gid + ((e >> 1) << 3);
+            // bf16: m-tile rows are 16 consecutive head_dim columns; fp8: rows
+            // gid and gid + 8 are neighbouring columns (see S6)
+            const int dl = kFp8 ? mt * 16 + 2 * gid + (e >> 1) : mt * 16 + gid + ((e >> 1) << 3);
             xb[q * kDPart + dl] = o[mt][n][e];
           }
       __syncwarp();

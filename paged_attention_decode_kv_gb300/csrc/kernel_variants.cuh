@@ -24,12 +24,14 @@ struct VariantInfo {
 constexpr size_t kSmemPerSm = 233472;
 constexpr size_t kSmemReservedPerCta = 1024;
 
-// Deepest ring (<= ST stages) whose CTA still fits MINB times on an SM.
+// Deepest ring (<= ST stages) whose CTA still fits MINB times on an SM; a
+// multiple of the alternate-page pairs (Smem::NPAR).
 template <int D, typename T, int G, int NCW, int MINB, Math M, int ST>
 struct StagePick {
   static constexpr size_t bytes = sizeof(Smem<D, T, G, NCW, ST, M>) + 1024;
-  static constexpr int value =
-      (bytes + kSmemReservedPerCta) * MINB <= kSmemPerSm ? ST : StagePick<D, T, G, NCW, MINB, M, ST - 1>::value;
+  static constexpr bool fits =
+      (bytes + kSmemReservedPerCta) * MINB <= kSmemPerSm && ST % Smem<D, T, G, NCW, ST, M>::NPAR == 0;
+  static constexpr int value = fits ? ST : StagePick<D, T, G, NCW, MINB, M, ST - 1>::value;
 };
 template <int D, typename T, int G, int NCW, int MINB, Math M>
 struct StagePick<D, T, G, NCW, MINB, M, 0> {
