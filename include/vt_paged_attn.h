@@ -162,12 +162,13 @@ VT_API vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const vo
  *   k_scale, v_scale  device float32 [num_kv_heads], 4-byte aligned; NULL is
  *                     VT_ERR_INVALID_ARG.
  *   head_dim          128 or 256 (64 is VT_ERR_UNSUPPORTED).
- * Arithmetic: the K and V codes enter E4M3 tensor-core MMAs (fp32
- * accumulation) as they are.  Each query row is scaled by a power of two and
- * split into two E4M3 terms (about 8 significant bits, like bf16; rows below
- * 2^-100 in magnitude count as zero), and so are the softmax weights, times
- * 256 (weights below 2^-17 of their row's largest drop out).  k_scale folds
- * into the score scale and v_scale into the final normalisation.
+ * Arithmetic: the K and V codes are widened exactly to f16 and enter f16
+ * tensor-core MMAs with fp32 accumulation.  Each query row is scaled by a
+ * power of two that puts its largest magnitude in [2^14, 2^15) and rounded
+ * to f16, which holds the bf16 values exactly down to 2^-28 of that largest
+ * (rows below 2^-100 in magnitude count as zero); the softmax weights enter
+ * PV as f16 (11 significant bits).  k_scale folds into the score scale and
+ * v_scale into the final normalisation.
  * Workspace, plan, status and errors are those of vt_paged_attn_decode.
  */
 VT_API vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache,
@@ -273,8 +274,9 @@ VT_API vt_status vt_paged_attn_set_overlap(int enabled);
  * `tiles` tiles in the split: CTAs whose share crosses many short sequences
  * get fewer pages.  The weight applies when the batch gives every CTA at
  * least 4 pages (below that the split is latency-bound and weights only add
- * partial results).  tiles < 0 restores the default (2); 0 balances pages
- * alone.  Results are the same within rounding (split points move, and with
+ * partial results).  tiles < 0 restores the default: 2 for bf16 and fp32
+ * K/V, 6 for an FP8 cache or several new tokens per sequence (their tiles
+ * take less time per segment boundary); 0 balances pages alone.  Results are the same within rounding (split points move, and with
  * them the order of the log-sum-exp merge).  Returns VT_ERR_INVALID_ARG for
  * tiles > 64.
  */

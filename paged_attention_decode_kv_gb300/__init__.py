@@ -179,7 +179,7 @@ def vt_paged_attn_set_overlap(enabled: bool) -> None:
 
 
 def vt_paged_attn_set_segment_cost(tiles: int = -1) -> None:
-    """Partition weight of a (sequence, kv head) boundary in tiles (-1: default 2)."""
+    """Partition weight of a (sequence, kv head) boundary in tiles (-1: default, 2; 6 for FP8 or multi-token)."""
     _check(library().vt_paged_attn_set_segment_cost(tiles), "vt_paged_attn_set_segment_cost")
 
 

@@ -16,7 +16,8 @@
 //                        together, so every K/V byte is read from HBM once
 //                        per kv head.  bf16 storage: tensor cores
 //                        (mma.sync m16n8k16, the page's tokens as M and the
-//                        query group as N); fp32 storage: CUDA-core FMAs;
+//                        query group as N); FP8 E4M3 codes: the same on f16
+//                        after exact widening; fp32 storage: CUDA-core FMAs;
 //   S4  mask             tail slots past the context and tokens before the
 //                        window are excluded; pages wholly outside the window
 //                        are never loaded;
@@ -24,7 +25,8 @@
 //                        scores, warp-shuffle reductions;
 //   S6  PV               fp32 accumulation of p * v (tensor cores for bf16,
 //                        with p split into two bf16 terms, hi + lo, so the
-//                        weights keep ~16 significant bits);
+//                        weights keep ~16 significant bits; f16 weights for
+//                        FP8 codes);
 //   S7  split partials   a (sequence, kv head) whose tiles span several CTAs
 //                        leaves one normalised partial (o, m, l) per CTA;
 //   S8  LSE combine      the last CTA to finish such an item (found through
@@ -47,7 +49,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -61,9 +62,6 @@ constexpr int kSwizzleCols = 64; // bf16 columns per 128-byte swizzled sub-tile 
 // GB300's 2.07 GHz maximum, 2^31 cycles is about 1 s and 2^28 about 0.13 s).
 constexpr long long kWaitLimitCycles = 1ll << 31;
 constexpr long long kDrainLimitCycles = 1ll << 28;
-// FP8 consumer: the softmax weights (at most 1) enter PV times this power of
-// two, so that weights down to 2^-17 of the row's largest stay E4M3 numbers.
-constexpr float kPScale = 256.f;
 
 // Page tiles of its slice a CTA prefetches into L2 before its dependency wait.
 constexpr int kPrefetchTiles = 8;
@@ -137,8 +135,10 @@ struct StageHeader {
 };
 
 // Consumer kinds: CUDA cores (fp32 storage); tensor cores on bf16 K/V
-// (mma.sync bf16); tensor cores on FP8 E4M3 K/V codes (mma.sync e4m3, the
-// codes used as they are; bf16 queries and output).
+// (mma.sync bf16); tensor cores on FP8 E4M3 K/V codes (widened exactly to f16
+// in registers for mma.sync f16, with f16 queries and weights; bf16 queries
+// and output in memory).  An e4m3 mma.sync is no cheaper here: on this GPU it
+// issues two f16 MMAs plus the operand widening for every k32 step.
 enum class Math { kSimt, kMma, kMma8 };
 
 // Element type of the K/V page tiles for a consumer kind.
@@ -348,45 +348,36 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 codes (low byte: element 0) widened to an f16 pair, exactly: every
-// E4M3 value (at most 448 in magnitude, at least 2^-9 apart from zero) is an
-// f16 normal number or zero; the NaN codes give NaN.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
-
-// An f16 pair (low half: element 0) rounded to two E4M3 codes (low byte:
-// element 0), saturating to +-448.
-__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
-  __half2_raw r;
-  r.x = static_cast<unsigned short>(h & 0xffffu);
-  r.y = static_cast<unsigned short>(h >> 16);
-  return __nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
-}
-
-// Two floats rounded to two E4M3 codes (low byte: lo), saturating to +-448.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
-  return __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// D = A * B + D, E4M3 inputs (four codes per register), fp32 accumulators,
-// m16n8k32.
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// D = A * B + D, f16 inputs, fp32 accumulators, m16n8k16.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four E4M3 codes (byte i: element i) widened exactly to two f16 pairs,
+// lo = (e0, e1) and hi = (e2, e3) (every E4M3 value is an f16 normal number
+// or zero; the NaN codes give NaN).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
+}
+
 // 2^e as a float, e in [-126, 127].
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22; results below 2^-126 flush to 0, 2^-inf = 0): the softmax weights,
+// which enter the sums against weights of at least 1.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -1042,12 +1033,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         for (int tt = 1; tt < TPG; ++tt) mloc = fmaxf(mloc, sc[tt]);
         const float m_new = fmaxf(m_run, mloc);
         const float m_use = (m_new == kNegInf) ? 0.f : m_new;
-        const float alpha = exp2f(m_run - m_use);
+        const float alpha = ex2(m_run - m_use);
         float p[TPG];
         float psum = 0.f;
 #pragma unroll
         for (int tt = 0; tt < TPG; ++tt) {
-          p[tt] = exp2f(sc[tt] - m_use);
+          p[tt] = ex2(sc[tt] - m_use);
           psum += p[tt];
         }
         l_run = l_run * alpha + psum;
@@ -1090,55 +1081,40 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         // group are zero.
         const uint32_t* q32 = reinterpret_cast<const uint32_t*>(s.q[stage]);
         if constexpr (kFp8) {
-          // E4M3 operands of mma.sync m16n8k32: the lane holds query 8n + gid,
-          // columns 32kp + 4tig .. +3 (b0) and 32kp + 16 + 4tig .. +3 (b1) of
-          // k-step kp.  Each query row is scaled by a power of two 2^e that
-          // puts its largest magnitude in [128, 256) and split into two E4M3
-          // terms, hi = e4m3(q 2^e) and lo = e4m3(q 2^e - hi): about 8
-          // significant bits of q, like its bf16 storage (rows below 2^-100
-          // count as zero).  qb[2kp] holds hi, qb[2kp + 1] lo; the score of
-          // a query column is scaled back by 2^-e with the softmax factor.
+          // f16 operands of mma.sync m16n8k16 (the codes are widened to f16
+          // exactly): the lane holds query 8n + gid, columns 16ks + 4tig,
+          // +1 (b0) and 16ks + 4tig + 2, +3 (b1) of k-step ks -- the columns
+          // its K codes sit in (S3).  Each query row is scaled by a power of
+          // two 2^e that puts its largest magnitude in [2^14, 2^15), so f16
+          // holds the bf16 values exactly down to 2^-28 of the largest (rows
+          // below 2^-100 count as zero); the score of a query column is
+          // scaled back by 2^-e with the softmax factor.
           const int h = hd.vh / a.subgroups;
           const float sk = a.scale_log2 * __ldg(a.k_scale + h);
-          vsc = __ldg(a.v_scale + h) * (1.f / kPScale);
+          vsc = __ldg(a.v_scale + h);
 #pragma unroll
           for (int n = 0; n < NQT; ++n) {
             const int qr = 8 * n + gid;
             const bool ok = qr < hd.gq;
+            uint2 w[kKSteps];
             float mx = 0.f;
 #pragma unroll
-            for (int kp = 0; kp < kKSteps / 2; ++kp)
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const uint2 w = ok ? *reinterpret_cast<const uint2*>(q32 + ((qr * D + kp * 32 + hf * 16 + 4 * tig) >> 1))
-                                   : make_uint2(0u, 0u);
-                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_lo_f(w.x)), fabsf(bf16_hi_f(w.x))),
-                                     fmaxf(fabsf(bf16_lo_f(w.y)), fabsf(bf16_hi_f(w.y)))));
-              }
+            for (int ks = 0; ks < kKSteps; ++ks) {
+              w[ks] = ok ? *reinterpret_cast<const uint2*>(q32 + ((qr * D + ks * 16 + 4 * tig) >> 1))
+                         : make_uint2(0u, 0u);
+              mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_lo_f(w[ks].x)), fabsf(bf16_hi_f(w[ks].x))),
+                                   fmaxf(fabsf(bf16_lo_f(w[ks].y)), fabsf(bf16_hi_f(w[ks].y)))));
+            }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127;  // floor(log2 mx)
-            const int e = (mx >= 0x1p-100f && mx <= 0x1p+100f) ? 7 - ex : 0;
+            const int e = (mx >= 0x1p-100f && mx <= 0x1p+100f) ? 14 - ex : 0;
             const float sc = pow2f(e);
 #pragma unroll
-            for (int kp = 0; kp < kKSteps / 2; ++kp)
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const uint2 w = ok ? *reinterpret_cast<const uint2*>(q32 + ((qr * D + kp * 32 + hf * 16 + 4 * tig) >> 1))
-                                   : make_uint2(0u, 0u);
-                const float x0 = bf16_lo_f(w.x) * sc, x1 = bf16_hi_f(w.x) * sc;
-                const float x2 = bf16_lo_f(w.y) * sc, x3 = bf16_hi_f(w.y) * sc;
-                const uint32_t hi = f32x2_to_e4m3x2(x0, x1) | (f32x2_to_e4m3x2(x2, x3) << 16);
-                const uint32_t b01 = e4m3x2_to_f16x2(hi), b23 = e4m3x2_to_f16x2(hi >> 16);
-                const uint32_t lo =
-                    f32x2_to_e4m3x2(x0 - __half2float(__ushort_as_half(static_cast<unsigned short>(b01 & 0xffffu))),
-                                    x1 - __half2float(__ushort_as_half(static_cast<unsigned short>(b01 >> 16)))) |
-                    (f32x2_to_e4m3x2(x2 - __half2float(__ushort_as_half(static_cast<unsigned short>(b23 & 0xffffu))),
-                                     x3 - __half2float(__ushort_as_half(static_cast<unsigned short>(b23 >> 16))))
-                     << 16);
-                qb[2 * kp][n][hf] = hi;
-                qb[2 * kp + 1][n][hf] = lo;
-              }
+            for (int ks = 0; ks < kKSteps; ++ks) {
+              qb[ks][n][0] = pack_f16(bf16_lo_f(w[ks].x) * sc, bf16_hi_f(w[ks].x) * sc);
+              qb[ks][n][1] = pack_f16(bf16_lo_f(w[ks].y) * sc, bf16_hi_f(w[ks].y) * sc);
+            }
             // the factor of this lane's score columns, queries 8n + 2tig (+1),
             // whose exponents sit with the lanes of gid 2tig (+1)
 #pragma unroll
@@ -1205,12 +1181,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 #pragma unroll
               for (int e = 0; e < 4; ++e) sc[n][hh][e] = 0.f;
         if constexpr (kFp8) {
-          // K codes, [token][head_dim] bytes in 128-byte swizzled rows, feed
-          // the e4m3 MMA as they are: one ldmatrix.x4 gives the A fragment of
-          // a 32-column k-step for the warp's 16 tokens (lane (gid, tig):
-          // codes of columns 4tig .. +3 and 16 + 4tig .. +3 for tokens gid and
-          // gid + 8).  Two MMAs per k-step, Q hi and Q lo, into separate
-          // accumulators.
+          // K codes, [token][head_dim] bytes in 128-byte swizzled rows: one
+          // ldmatrix.x4 gives, for the warp's 16 tokens, the codes of columns
+          // 4tig .. +3 of two 16-column chunks (tokens gid and gid + 8); each
+          // register widens to the f16 pairs of k-slots 2tig, +1 (columns
+          // 4tig, +1) and 2tig + 8, +9 (columns 4tig + 2, +3).
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;
 #pragma unroll
@@ -1220,9 +1195,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             uint32_t ak[4];
             ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
-            for (int n = 0; n < NQT; ++n) {
-              mma_e4m3(sc[n][(2 * kp) % kQAcc], ak, qb[2 * kp][n][0], qb[2 * kp][n][1]);
-              mma_e4m3(sc[n][(2 * kp + 1) % kQAcc], ak, qb[2 * kp + 1][n][0], qb[2 * kp + 1][n][1]);
+            for (int hf = 0; hf < 2; ++hf) {
+              uint32_t af[4];
+              e4m3x4_to_f16(ak[2 * hf], af[0], af[2]);
+              e4m3x4_to_f16(ak[2 * hf + 1], af[1], af[3]);
+              const int ks = 2 * kp + hf;
+#pragma unroll
+              for (int n = 0; n < NQT; ++n) mma_f16(sc[n][ks % kQAcc], af, qb[ks][n][0], qb[ks][n][1]);
             }
           }
         } else if constexpr (kQSmem) {
@@ -1276,6 +1255,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         // single-token decode exactly [lo, hi)).
         const int t_lo = 16 * tg + gid, t_hi = t_lo + 8;
         const int wlim = a.window > 0 ? a.window : (1 << 30);
+        // Interior page: every token is live for every query row (rows past
+        // the live group have zero queries, so finite scores that no output
+        // reads), and the masks are skipped.
+        const bool interior = hd.rel_end - (a.q_len - 1) >= kPageTokens && hd.rel_end <= wlim;
         float sv[NQT][2][2];
         bool up = false;  // some score above its column's running maximum
 #pragma unroll
@@ -1292,8 +1275,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               s0 += sacc[n][c][jq];
               s1 += sacc[n][c][jq + 2];
             }
-            sv[n][jq][0] = (qok && t_lo >= beg && t_lo < end) ? s0 * f : kNegInf;
-            sv[n][jq][1] = (qok && t_hi >= beg && t_hi < end) ? s1 * f : kNegInf;
+            if (interior) {
+              sv[n][jq][0] = s0 * f;
+              sv[n][jq][1] = s1 * f;
+            } else {
+              sv[n][jq][0] = (qok && t_lo >= beg && t_lo < end) ? s0 * f : kNegInf;
+              sv[n][jq][1] = (qok && t_hi >= beg && t_hi < end) ? s1 * f : kNegInf;
+            }
             up |= fmaxf(sv[n][jq][0], sv[n][jq][1]) > mq[n][jq];
           }
         }
@@ -1312,9 +1300,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
               const float mn = fmaxf(mq[n][jq], mx);
               const float mu = (mn == kNegInf) ? 0.f : mn;
-              al[n][jq] = exp2f(mq[n][jq] - mu);
-              pr[n][jq] = exp2f(sv[n][jq][0] - mu);
-              pr[n][jq + 2] = exp2f(sv[n][jq][1] - mu);
+              al[n][jq] = ex2(mq[n][jq] - mu);
+              pr[n][jq] = ex2(sv[n][jq][0] - mu);
+              pr[n][jq + 2] = ex2(sv[n][jq][1] - mu);
               lq[n][jq] = lq[n][jq] * al[n][jq] + pr[n][jq] + pr[n][jq + 2];
               mq[n][jq] = mn;
             }
@@ -1336,8 +1324,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
 #pragma unroll
             for (int jq = 0; jq < 2; ++jq) {
               const float mu = (mq[n][jq] == kNegInf) ? 0.f : mq[n][jq];
-              pr[n][jq] = exp2f(sv[n][jq][0] - mu);
-              pr[n][jq + 2] = exp2f(sv[n][jq][1] - mu);
+              pr[n][jq] = ex2(sv[n][jq][0] - mu);
+              pr[n][jq + 2] = ex2(sv[n][jq][1] - mu);
               lq[n][jq] += pr[n][jq] + pr[n][jq + 2];
             }
           }
@@ -1355,36 +1343,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
                                ((tl + 9 >= h.lo && tl + 9 < h.hi) ? 0xffff0000u : 0u);
           const bool full_page = h.lo == 0 && h.hi == kPageTokens;  // no token to clear
         if constexpr (kFp8) {
-          // P^T for the e4m3 MMA: the weights times kPScale, split into two
-          // E4M3 terms hi + lo (about 8 significant bits).  After movmatrix a
-          // lane holds, for query gid, the weights of tokens 2tig, 2tig + 1
-          // (from the first 8x8 block) and 2tig + 8, 2tig + 9 (the second):
-          // the four codes of one B register, in that token order.  k = 0..15
-          // carries hi and k = 16..31 lo over the same tokens, and the V^T
-          // fragment repeats for both halves, so one MMA adds V (P_hi + P_lo).
+          // P^T as f16 B fragments (11 significant bits of the weights): the
+          // S^T accumulator layout transposed per 8x8 block with movmatrix, so a
+          // lane holds, for query gid, tokens 2tig, 2tig + 1 and 2tig + 8, +9.
           uint32_t pb[NQT][2];
 #pragma unroll
           for (int n = 0; n < NQT; ++n) {
-            const uint32_t h0 = movmatrix_trans(pack_f16(p[n][0] * kPScale, p[n][1] * kPScale));
-            const uint32_t h1 = movmatrix_trans(pack_f16(p[n][2] * kPScale, p[n][3] * kPScale));
-            const uint32_t hi = f16x2_to_e4m3x2(h0) | (f16x2_to_e4m3x2(h1) << 16);
-            const uint32_t r0 = hsub2_u32(h0, e4m3x2_to_f16x2(hi)), r1 = hsub2_u32(h1, e4m3x2_to_f16x2(hi >> 16));
-            pb[n][0] = hi;
-            pb[n][1] = f16x2_to_e4m3x2(r0) | (f16x2_to_e4m3x2(r1) << 16);
+            pb[n][0] = movmatrix_trans(pack_f16(p[n][0], p[n][1]));
+            pb[n][1] = movmatrix_trans(pack_f16(p[n][2], p[n][3]));
           }
           // V^T A fragments by ldmatrix.trans over byte pairs: an 8x8 matrix of
           // 16-bit elements is 8 tokens x 16 codes, and transposed a lane gets
-          // codes 2gid, 2gid + 1 of tokens 2tig and 2tig + 1.  With the
-          // matrices of tokens 0-7 and 8-15 of the warp's 16, two byte
-          // permutes give one register per code column holding tokens 2tig,
-          // 2tig + 1, 2tig + 8, 2tig + 9 (the order of the P^T codes).  So
-          // rows gid and gid + 8 of m-tile mt are columns 16mt + 2gid and
-          // 16mt + 2gid + 1 of the warp's part.  Codes of tokens outside the
-          // page's range are cleared (they may be NaN).
-          const uint32_t m8 = ((tl >= h.lo && tl < h.hi) ? 0x000000ffu : 0u) |
-                              ((tl + 1 >= h.lo && tl + 1 < h.hi) ? 0x0000ff00u : 0u) |
-                              ((tl + 8 >= h.lo && tl + 8 < h.hi) ? 0x00ff0000u : 0u) |
-                              ((tl + 9 >= h.lo && tl + 9 < h.hi) ? 0xff000000u : 0u);
+          // codes 2gid, 2gid + 1 (bytes 0, 1) of token 2tig and the same of
+          // token 2tig + 1 (bytes 2, 3).  A byte permute pairs the two tokens
+          // per code, and widening gives f16 pairs (tokens 2tig, +1) of
+          // columns 2gid and 2gid + 1: rows gid and gid + 8 of m-tile mt are
+          // columns 16mt + 2gid and 16mt + 2gid + 1 of the warp's part.  Codes
+          // of tokens outside the page's range are cleared (they may be NaN).
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;  // token row this lane addresses
           const uint32_t vrow = smem_addr(s.v[st]) + t * 128;
@@ -1394,17 +1369,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const int sb = byte >> 7, chunk = (byte & 127) >> 4;
             uint32_t w[4];  // (tokens 0-7, 8-15) of block 2mp, then of block 2mp + 1
             ldmatrix_x4_trans(vrow + sb * (kPageTokens * 128) + ((chunk ^ (t & 7)) << 4), w);
+            if (!full_page) {
+              w[0] &= mlo;
+              w[1] &= mhi;
+              w[2] &= mlo;
+              w[3] &= mhi;
+            }
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-              uint32_t c0 = __byte_perm(w[2 * hb], w[2 * hb + 1], 0x6420u);  // column 2gid
-              uint32_t c1 = __byte_perm(w[2 * hb], w[2 * hb + 1], 0x7531u);  // column 2gid + 1
-              if (!full_page) {
-                c0 &= m8;
-                c1 &= m8;
-              }
-              const uint32_t av[4] = {c0, c1, c0, c1};
+              uint32_t av[4];
+              e4m3x4_to_f16(__byte_perm(w[2 * hb], 0u, 0x3120u), av[0], av[1]);
+              e4m3x4_to_f16(__byte_perm(w[2 * hb + 1], 0u, 0x3120u), av[2], av[3]);
 #pragma unroll
-              for (int n = 0; n < NQT; ++n) mma_e4m3(oacc[2 * mp + hb][n], av, pb[n][0], pb[n][1]);
+              for (int n = 0; n < NQT; ++n) mma_f16(oacc[2 * mp + hb][n], av, pb[n][0], pb[n][1]);
             }
           }
         } else {

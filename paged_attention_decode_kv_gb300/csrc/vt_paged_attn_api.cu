@@ -31,7 +31,11 @@ using vt::VariantInfo;
 constexpr int kVersion = 10100;  // 1.1.0
 constexpr int kMaxGroupTile = 8;
 constexpr int kDefaultMinUnits = 2;
-constexpr int kDefaultSegCost = 2;  // a segment boundary weighs about two tiles of streaming
+// A segment boundary weighs about two tiles of bf16 or fp32 streaming; an FP8
+// tile (half the bytes) or a multi-token one (a longer epilogue per boundary)
+// is worth less against it: measured best at six.
+constexpr int kDefaultSegCost = 2;
+constexpr int kDefaultSegCostFp8OrMulti = 6;
 constexpr size_t kStatusBytes = 256;
 
 thread_local int g_override_grid = 0;
@@ -437,7 +441,9 @@ vt_status launch(const Call& c, const Plan& p, char* base, size_t counters_regio
   args.window = c.window > 0 ? c.window : 0;
   args.scale_log2 = c.scale * 1.4426950408889634f;
   args.min_units = p.min_units;
-  args.seg_cost = g_seg_cost < 0 ? kDefaultSegCost : g_seg_cost;
+  args.seg_cost = g_seg_cost >= 0 ? g_seg_cost
+                 : (c.dtype == VT_E4M3 || c.q_len > 1) ? kDefaultSegCostFp8OrMulti
+                                                       : kDefaultSegCost;
   args.wait_limit = g_test_wait_limit > 0 ? g_test_wait_limit : vt::kWaitLimitCycles;
   args.withhold_cta = g_test_withhold_tile >= 0 ? g_test_withhold_cta : -1;
   args.withhold_tile = g_test_withhold_tile;

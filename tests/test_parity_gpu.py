@@ -317,6 +317,20 @@ def test_default_plan(dev):
     assert plan["workspace_bytes"] > 0
 
 
+def test_default_segment_cost(dev):
+    """The partition's default segment weight: 2 tiles for bf16 K/V, 6 for an
+    FP8 cache or several new tokens per sequence; each result is the oracle's."""
+    cases = ((W.make_case(W.QWEN3_1P7B, 0), 2), (W.make_case(W.QWEN3_1P7B_FP8, 0), 6),
+             (W.make_case(W.custom("segdef_multi", [100, 40, 1200], 8, 2, 128, q_len=3), 0), 6))
+    for case, cost in cases:
+        _, plan = gpu_run(case, dev)
+        assert plan["segment_cost"] == cost, case.workload.name
+        if case.workload.q_len == 1:
+            check_case(case, dev)
+        else:
+            check_multi(case, dev)
+
+
 def test_side_stream_and_reuse(dev):
     """Calls on a non-default stream, back to back with different shapes, share
     the library workspace correctly."""
