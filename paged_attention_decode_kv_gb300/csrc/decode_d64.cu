@@ -8,7 +8,7 @@ namespace vt {
 
 const VariantInfo* variants_d64_bf16(int* count) {
   static const VariantInfo table[] = {
-      Variant<64, __nv_bfloat16, 8, 4, 2, 8, Math::kMma>::info(),
+      Variant<64, __nv_bfloat16, 8, 4, 3, 8, Math::kMma>::info(),
       Variant<64, __nv_bfloat16, 16, 4, 2, 8, Math::kMma>::info(),
   };
   *count = 2;

@@ -163,12 +163,14 @@ struct Smem {
   // mma layout: warps split the page into (token half tg) x (head_dim part
   // dp).  With NPAR = 2 the warps also form two pairs of alternate pages:
   // pair par takes the ring stages s with s mod 2 = par, so two pages are in
-  // flight per CTA and no head_dim part repeats another's QK^T and softmax
-  // (FP8 K/V with four consumer warps: its per-tile instruction count, not
-  // the bytes, bounds it).  The producer gives every segment an even number
-  // of stages (closing odd ones with a kPad stage), so segments start on even
-  // stages.
-  static constexpr int NPAR = (M == Math::kMma8 && G <= 8 && NCW == 4) ? 2 : 1;
+  // flight per CTA and no head_dim part repeats another's QK^T and softmax:
+  // for the 8 KB tiles of FP8 K/V at head_dim 128 and 256 and of bf16 at
+  // head_dim 64, whose per-tile work, not the bytes, bounds them (bf16 at
+  // head_dim 128 and 256 measured no faster).  The producer gives every
+  // segment an even number of stages (closing odd ones with a kPad stage),
+  // so segments start on even stages.
+  static constexpr int NPAR =
+      ((M == Math::kMma8 || (M == Math::kMma && D == 64)) && G <= 8 && NCW == 4) ? 2 : 1;
   static constexpr int NDP = (M != Math::kSimt) ? NCW / (2 * NPAR) : 1;
   static constexpr int kRedRows = (M == Math::kSimt) ? NG : 2 * NPAR;
   alignas(128) T q[NSTAGE][G * D];
