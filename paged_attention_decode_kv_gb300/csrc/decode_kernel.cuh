@@ -189,6 +189,14 @@ struct Smem {
   static constexpr int XP = (M != Math::kSimt) ? 2 : 1;
   static constexpr int XN = (M != Math::kSimt) ? D / NDP / 16 : 1;
   alignas(16) float xbuf[XP][NDP][NPAR][XN][32][XV];
+  // bf16 at head_dim 512: the four head_dim parts split QK^T (SQK) and sum
+  // their partial scores through this buffer ([tile parity][tg][dp][lane],
+  // a float4 per query n-tile), one mbarrier per (tile parity, tg).  (With
+  // the two parts of head_dim 256 the exchange costs more than it saves.)
+  static constexpr bool SQK = (M == Math::kMma) && D >= 512 && NDP > 1;
+  static constexpr int QXN = (G > 8) ? 2 : 1;
+  alignas(16) float4 qx[SQK ? 2 : 1][SQK ? 2 : 1][SQK ? NDP : 1][SQK ? 32 : 1][SQK ? QXN : 1];
+  unsigned long long qx_bar[2][2];
   // CUDA-core consumer only: per-group broadcast of p and the rescale factor.
   static constexpr int PG = (M == Math::kSimt) ? G : 1;
   static constexpr int PT = (M == Math::kSimt) ? TPG : 1;
@@ -632,6 +640,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
       mbar_init(&s.empty[st], NCW / NPAR);  // the warps of the stage's pair
     }
     mbar_init(&s.csync, NCW);  // one arrival per consumer warp
+    for (int p2 = 0; p2 < 4; ++p2) mbar_init(&s.qx_bar[p2 >> 1][p2 & 1], S::NDP);  // the warps of one tg
     mbar_init(&s.comb, 1);
     s.abort_flag = 0;
     s.b_start_s = -1;
@@ -936,18 +945,25 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   // mma consumer (bf16): warp = (token half tg, head_dim part dp).  The
   // products are taken transposed, with the warp's 16 tokens as the M
   // dimension and the query group as N (8 or 16): S^T = K Q^T over the full
-  // head_dim (repeated by the dp warps), O^T = V^T P^T for the warp's
-  // D / NDP output rows of O^T.  No M padding for groups of up to 8.
+  // head_dim (repeated by the dp warps, or at head_dim 512 split over them
+  // and summed), O^T = V^T P^T for the warp's D / NDP output rows of O^T.
+  // No M padding for groups of up to 8.
   constexpr int NDP = S::NDP;
   constexpr int kDPart = D / NDP;        // O^T rows (head_dim columns of O) per warp
   constexpr int kKSteps = D / 16;        // k-steps of S^T over head_dim
   constexpr int kMt = kDPart / 16;       // 16-row m-tiles of O^T per warp
   constexpr int NQT = (G > 8) ? 2 : 1;   // 8-query n-tiles
+  constexpr bool kSplitQK = S::SQK;
+  constexpr int kQKS = kSplitQK ? kKSteps / NDP : kKSteps;  // k-steps of this warp's share of S^T
+  static_assert(!kSplitQK || (kQKS % 2 == 0 && NQT == S::QXN), "split QK^T shape");
   const int tg = warp & 1, par = (warp >> 1) % NPAR, dp = warp / (2 * NPAR);
+  const int kq0 = kSplitQK ? dp * kQKS : 0;  // first k-step of the share
   const int gid = lane >> 2, tig = lane & 3;
 
   int stage = kMma ? par : 0;  // a warp pair walks its own stages of the ring
   uint32_t phase = 0;
+  int qx_t = 0;          // split QK^T: tiles exchanged so far (buffer parity)
+  uint32_t qx_ph = 0u;   // and the phase bit of each parity's barrier
   int pbuf_par = 0, seg_par = 0;
   bool alive = true, more = true;
   // One iteration per (sequence, virtual head) segment: the query fragments
@@ -955,7 +971,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   while (alive && more) {
   float qf[kMma ? 1 : G][8];
   float acc[kMma ? 1 : G][8];
-  uint32_t qb[kMma && !kQSmem ? kKSteps : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
+  uint32_t qb[kMma && !kQSmem ? kQKS : 1][NQT][2];  // Q^T as the B operand of S^T = K Q^T
   float oacc[kMma ? kMt : 1][NQT][4];       // O^T accumulators
   float m_run = kNegInf, l_run = 0.f;       // simt: the lane's query
   float sl2 = a.scale_log2;                 // score factor into the log2 domain
@@ -1147,8 +1163,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const int qr = 8 * n + gid;
             const bool ok = qr < hd.gq;
 #pragma unroll
-            for (int ks = 0; ks < kKSteps; ++ks) {
-              const int col = ks * 16 + 2 * tig;
+            for (int ks = 0; ks < kQKS; ++ks) {
+              const int col = (kq0 + ks) * 16 + 2 * tig;
               qb[ks][n][0] = ok ? q32[(qr * D + col) >> 1] : 0u;
               qb[ks][n][1] = ok ? q32[(qr * D + col + 8) >> 1] : 0u;
             }
@@ -1214,7 +1230,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           const int t = 16 * tg + ((mi & 1) << 3) + r;
           const uint32_t qbase = smem_addr(s.qs);
 #pragma unroll 4
-          for (int ks = 0; ks < kKSteps; ks += 2) {
+          for (int kk = 0; kk < kQKS; kk += 2) {
+            const int ks = kq0 + kk;
             uint32_t qf[NQT][4];
 #pragma unroll
             for (int n = 0; n < NQT; ++n) {
@@ -1230,15 +1247,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
               uint32_t ak[4];
               ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
 #pragma unroll
-              for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][(ks + h2) % kQAcc], ak, qf[n][2 * h2], qf[n][2 * h2 + 1]);
+              for (int n = 0; n < NQT; ++n) mma_bf16(sc[n][(kk + h2) % kQAcc], ak, qf[n][2 * h2], qf[n][2 * h2 + 1]);
             }
           }
         } else {
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;  // token row this lane addresses
 #pragma unroll
-          for (int ks = 0; ks < kKSteps; ++ks) {
-            const int d = ks * 16 + ((mi >> 1) << 3);
+          for (int ks = 0; ks < kQKS; ++ks) {
+            const int d = (kq0 + ks) * 16 + ((mi >> 1) << 3);
             const int sb = d / kSwizzleCols, chunk = (d % kSwizzleCols) >> 3;
             uint32_t ak[4];
             ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
@@ -1249,6 +1266,51 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
         };
         float sacc[NQT][kQAcc][4];
         qk(smem_addr(s.k[stage]), sacc);
+        if constexpr (kSplitQK) {
+          // The dp warps of this token half add their partial scores in dp
+          // order, so each gets the same bits.  A warp is at most one tile
+          // ahead of the others (it cannot pass the next tile's barrier
+          // before they reach it), hence two buffers.
+          const int xq = qx_t & 1;
+#pragma unroll
+          for (int n = 0; n < NQT; ++n) {
+            float v4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float x = sacc[n][0][e];
+#pragma unroll
+              for (int c2 = 1; c2 < kQAcc; ++c2) x += sacc[n][c2][e];
+              v4[e] = x;
+            }
+            s.qx[xq][tg][dp][lane][n] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.qx_bar[xq][tg]);
+          const bool xok = wait_phase(&s.qx_bar[xq][tg], (qx_ph >> xq) & 1u, &s.abort_flag, a.status, kStatusSync,
+                                      a.wait_limit);
+          if (!__all_sync(0xffffffffu, xok)) {
+            alive = false;
+            break;
+          }
+          qx_ph ^= 1u << xq;
+          ++qx_t;
+#pragma unroll
+          for (int n = 0; n < NQT; ++n) {
+            float4 tot = s.qx[xq][tg][0][lane][n];
+#pragma unroll
+            for (int d2 = 1; d2 < NDP; ++d2) {
+              const float4 x = s.qx[xq][tg][d2][lane][n];
+              tot.x += x.x;
+              tot.y += x.y;
+              tot.z += x.z;
+              tot.w += x.w;
+            }
+            sacc[n][0][0] = tot.x;
+            sacc[n][0][1] = tot.y;
+            sacc[n][0][2] = tot.z;
+            sacc[n][0][3] = tot.w;
+          }
+        }
         // S4 + S5: mask and scale; online softmax per query column.  Lane
         // holds tokens 16tg + gid (values 0, 1) and + 8 (values 2, 3) of
         // queries 8n + 2tig (values 0, 2) and + 1 (values 1, 3).  Query row q
@@ -1273,7 +1335,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
             const float f = kFp8 ? sq[kFp8 ? n : 0][jq] : sl2;
             float s0 = sacc[n][0][jq], s1 = sacc[n][0][jq + 2];
 #pragma unroll
-            for (int c = 1; c < kQAcc; ++c) {
+            for (int c = 1; c < (kSplitQK ? 1 : kQAcc); ++c) {
               s0 += sacc[n][c][jq];
               s1 += sacc[n][c][jq + 2];
             }
