@@ -249,6 +249,34 @@ def test_fp8_invalid_device_data_and_empty(dev):
         compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16)
 
 
+@pytest.mark.parametrize("d,dtype", [(128, "e4m3"), (256, "e4m3"), (64, "bf16")], ids=lambda x: str(x))
+def test_alternate_page_pairs(dev, d, dtype):
+    """The arms whose warps form two pairs taking alternate ring stages: odd
+    and even page counts (an odd segment is closed by a stage without tiles,
+    which for a one-page segment is also the second pair's first), split
+    items at many grids, windows, and a bad page id seen by either pair
+    poisoning only its sequence.  Repeated calls give the same bits."""
+    lens = [1, 32, 33, 64, 65, 95, 96, 97, 700, 1500, 0, 31]
+    case = W.make_case(W.custom(f"pairs_{dtype}_d{d}", lens, 8, 2, d, dtype=dtype), 31)
+    for window in (0, 40, 333):
+        for grid in (0, 3, 13, 301):
+            (_, _), plan = check_case(case, dev, window=window, grid=grid, min_units=1 if grid else 0)
+            assert plan["group_tile"] == 8
+    bt = case.block_tables.clone()
+    bt[4, 1] = case.num_blocks + 2   # second page of a three-page context: the second pair's
+    bt[5, 2] = -1                    # third page of another: the first pair's
+    ok_rows = [(b, i) for b in (0, 1, 2, 3, 6, 7, 8, 9, 11) for i in range(8)]
+    for grid in (0, 7):
+        out, _ = gpu_run(case, dev, tables=bt, grid=grid, min_units=1)
+        assert torch.isnan(out[4].float()).all() and torch.isnan(out[5].float()).all()
+        assert torch.count_nonzero(out[10]) == 0
+        idx, ref = oracle_rows(case, ok_rows)
+        compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, case.q.dtype, "pairs with bad pages")
+    a, _ = gpu_run(case, dev, grid=13, min_units=1)
+    b, _ = gpu_run(case, dev, grid=13, min_units=1)
+    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_head_dim_64_windows_and_boundaries(dev, dtype):
     """The head_dim 64 arm on the straddling contexts, with and without a
