@@ -45,6 +45,7 @@ SWEEP = ["batch1_ctx32768_gqa4_d128", "large_gqa8_b64_d128", "d256_gqa4_b16", "d
          "d64_gqa4_b32_f32", "skewed_b128_gqa4_d128_fp8", "batch1_ctx32768_gqa4_d128_fp8",
          "large_gqa8_b64_d128_fp8", "d256_gqa4_b16_fp8", "d512_gqa4_b16", "d512_gqa4_b16_w1024", "multi_q4_b64_gqa4_d128"]
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy rate is the roofline peak)
 KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "vt_paged_attn_api.cu"]  # shared by every variant
 
 
@@ -537,6 +538,7 @@ def run_ours(args, rank, world, dist):
             sweep.append({"workload": name, "us_per_call": m * 1e6, "eager_per_call": summarize(ts),
                           "kv_gbs": case_s.kv_bytes() / m / 1e9,
                           "achieved_gbs": a_bytes / m / 1e9, "frac": a_bytes / m / 1e9 / peak,
+                          "frac_of_nominal": a_bytes / m / 1e9 / NOMINAL_HBM_GBS,
                           "algorithmic_bytes": a_bytes, "ideal_us_at_peak": a_bytes / (peak * 1e9) * 1e6,
                           "traffic": tr, "traffic_over_algorithmic": (tr / a_bytes) if tr else None,
                           "plan": vt.vt_paged_attn_last_plan()})
@@ -567,7 +569,8 @@ def run_ours(args, rank, world, dist):
         "eager_per_call": summarize(times),
         "kv_gbs": kv / mean_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS, "traffic": traffic,
                      "traffic_over_algorithmic": (traffic / algo) if traffic else None,
                      "ideal_us_at_peak": algo / (peak * 1e9) * 1e6,
                      "algorithmic_bytes_per_launch": algo, "peak_source": peak_src,
