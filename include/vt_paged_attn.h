@@ -341,7 +341,8 @@ VT_API vt_status vt_paged_attn_set_workspace(void* dev_ptr, size_t bytes, vt_str
  * sets a status bit and lets the CTA exit; this hook shortens the limit to
  * wait_limit_cycles (<= 0: the default) and, when withhold_tile >= 0, makes
  * CTA withhold_cta stop feeding its consumers before its withhold_tile-th
- * tile.  The consumers' wait for that tile then runs out, the kernel returns
+ * ring stage (counting from 0; stages that only close a segment count too).
+ * The consumers' wait for that stage then runs out, the kernel returns
  * without faulting, and vt_paged_attn_device_status reports
  * VT_ERR_DEVICE_TIMEOUT (bit 0); the output of that call is incomplete.
  * vt_paged_attn_set_test_wait(0, -1, -1) restores normal operation.

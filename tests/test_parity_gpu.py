@@ -595,6 +595,34 @@ def test_bounded_wait_gives_up_and_reports(dev, path):
             vt.vt_paged_attn_set_workspace(0, 0)
 
 
+@pytest.mark.parametrize("tile", [1, 2])
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "e4m3")], ids=lambda x: str(x))
+def test_bounded_wait_gives_up_alternate_pairs(dev, d, dtype, tile):
+    """The give-up path on the arms whose warp pairs take alternate stages:
+    CTA 0 withholds a tile of the second pair (tile 1) or of the first
+    (tile 2); the waits run out, the status reports a page-tile timeout by a
+    consumer thread of CTA 0, and the next call is exact."""
+    case = W.make_case(W.custom(f"giveup_pairs_{dtype}_d{d}", [100, 700], 16, 4, d, dtype=dtype), 29)
+    w = case.workload
+    k, v = case.pool(dev)
+    q, bt, cl = case.q.to(dev), case.block_tables.to(dev), case.context_lens.to(dev)
+    vt.vt_paged_attn_set_override(1, 1)
+    vt.vt_paged_attn_set_test_wait(1 << 22, 0, tile)
+    try:
+        run_decode(case, q, k, v, bt, cl)
+    finally:
+        vt.vt_paged_attn_set_test_wait(0, -1, -1)
+        vt.vt_paged_attn_set_override(0, 0)
+    torch.cuda.synchronize()
+    detail = vt.vt_paged_attn_device_status_detail(n_words=5)
+    status = vt.vt_paged_attn_device_status()
+    assert status & 1, f"status {status:#x}"
+    assert detail[1] == 1 and detail[2] & 0xFF == 1 and (detail[2] >> 8) < 128, detail
+    assert vt.vt_paged_attn_device_status() == 0
+    for grid in (0, 3):
+        check_case(case, dev, grid=grid, min_units=1 if grid else 0)
+
+
 # ---------------------------------------------------------------------------
 # Multi-token decode (q_len new tokens per sequence, causal within them)
 # ---------------------------------------------------------------------------
