@@ -43,7 +43,8 @@ DEFAULT_WORKLOAD = "skewed_b128_gqa4_d128"
 SWEEP = ["batch1_ctx32768_gqa4_d128", "large_gqa8_b64_d128", "d256_gqa4_b16", "d256_gqa4_b16_w1024",
          "d256_gqa4_b16_f32", "d256_gqa4_b16_f32_w1024", "qwen3_1p7b_b8_gqa2_d128", "d64_gqa4_b32",
          "d64_gqa4_b32_f32", "skewed_b128_gqa4_d128_fp8", "batch1_ctx32768_gqa4_d128_fp8",
-         "large_gqa8_b64_d128_fp8", "d256_gqa4_b16_fp8", "d512_gqa4_b16", "d512_gqa4_b16_w1024", "multi_q4_b64_gqa4_d128"]
+         "large_gqa8_b64_d128_fp8", "d256_gqa4_b16_fp8", "d512_gqa4_b16", "d512_gqa4_b16_w1024", "multi_q4_b64_gqa4_d128",
+         "multi_q4_b64_gqa4_d128_fp8"]
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy rate is the roofline peak)
 KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "vt_paged_attn_api.cu"]  # shared by every variant
@@ -365,6 +366,13 @@ def oracle_baseline(case, budget_s: float, threads: int = 1):
     w = case.workload
     k, v, bt = case.compact()
     qa, ka, va = W.to_oracle_array(case.q), W.to_oracle_array(k), W.to_oracle_array(v)
+    if case.fp8 and w.q_len > 1:
+        # the oracle's multi-token rows take the FP8 cache as its fp64 values
+        import torch
+        ks, vs = case.scales()
+        ka = (k.view(torch.float8_e4m3fn).to(torch.float64) * ks.double()[None, None, :, None]).numpy()
+        va = (v.view(torch.float8_e4m3fn).to(torch.float64) * vs.double()[None, None, :, None]).numpy()
+        qa = case.q.to(torch.float64).numpy()  # bf16 -> fp64 is exact; one storage type for all three
     tail = (bt.numpy(), case.context_lens.numpy(), w.scale, w.window)
 
     def decode_rows(rows, threads=1):

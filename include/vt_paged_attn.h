@@ -200,7 +200,8 @@ VT_API vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* 
  * The query rows of one kv head (q_len tokens x its group of query heads)
  * share every page the head's kv tile is read for, so the cache is read once
  * per kv head for the whole chunk.  A sequence with L < q_len gets NaN rows
- * for all its new tokens.  dtype VT_E4M3 is VT_ERR_INVALID_ARG.
+ * for all its new tokens.  dtype VT_E4M3 is VT_ERR_INVALID_ARG (an FP8 cache
+ * takes vt_paged_attn_decode_multi_fp8).
  */
 VT_API vt_status vt_paged_attn_decode_multi(void* out, const void* q, const void* k_cache,
                                             const void* v_cache, const int32_t* block_tables,
@@ -209,6 +210,27 @@ VT_API vt_status vt_paged_attn_decode_multi(void* out, const void* q, const void
                                             int block_size, float scale, int window,
                                             vt_stream_t stream, int max_blocks_per_seq,
                                             int num_blocks, vt_dtype dtype);
+
+/*
+ * vt_paged_attn_decode_multi_fp8 -- several new tokens per sequence over an
+ * FP8 (E4M3) cache: the operation of vt_paged_attn_decode_multi on the cache
+ * that vt_paged_attn_decode_fp8 reads (codes times per-kv-head scales).
+ *
+ * Arguments as for vt_paged_attn_decode_fp8, plus q_len after num_seqs:
+ *   q, out   bf16 [num_seqs][q_len][num_q_heads][head_dim].
+ *   q_len    >= 1 (1 is vt_paged_attn_decode_fp8); q_len * group <= 4096.
+ * Arithmetic as for vt_paged_attn_decode_fp8; causal limits, windows and the
+ * NaN rows of L < q_len as for vt_paged_attn_decode_multi.  NULL scales are
+ * VT_ERR_INVALID_ARG.
+ */
+VT_API vt_status vt_paged_attn_decode_multi_fp8(void* out, const void* q, const void* k_cache,
+                                                const void* v_cache, const float* k_scale,
+                                                const float* v_scale, const int32_t* block_tables,
+                                                const int32_t* context_lens, int num_seqs, int q_len,
+                                                int num_q_heads, int num_kv_heads, int head_dim,
+                                                int block_size, float scale, int window,
+                                                vt_stream_t stream, int max_blocks_per_seq,
+                                                int num_blocks);
 
 /* What the last successful decode call on this host thread launched. */
 typedef struct {

@@ -21,7 +21,7 @@ VT_BF16, VT_F32, VT_E4M3 = 0, 1, 2
 BLOCK_SIZE = 32
 
 EXPORTED = ("vt_paged_attn_decode", "vt_paged_attn_decode_noalloc", "vt_paged_attn_decode_fp8",
-            "vt_paged_attn_decode_multi",
+            "vt_paged_attn_decode_multi", "vt_paged_attn_decode_multi_fp8",
             "vt_paged_attn_last_plan",
             "vt_paged_attn_set_override", "vt_paged_attn_set_overlap", "vt_paged_attn_set_segment_cost",
             "vt_paged_attn_set_workspace", "vt_paged_attn_set_test_wait",
@@ -80,6 +80,9 @@ def library() -> ctypes.CDLL:
             lib.vt_paged_attn_decode_multi.argtypes = [c_void] * 6 + [c_int] * 6 + [c_float, c_int, c_void, c_int,
                                                                                     c_int, c_int]
             lib.vt_paged_attn_decode_multi.restype = c_int
+            lib.vt_paged_attn_decode_multi_fp8.argtypes = [c_void] * 8 + [c_int] * 6 + [c_float, c_int, c_void,
+                                                                                         c_int, c_int]
+            lib.vt_paged_attn_decode_multi_fp8.restype = c_int
             lib.vt_paged_attn_last_plan.argtypes = [ctypes.POINTER(vt_plan)]
             lib.vt_paged_attn_last_plan.restype = c_int
             lib.vt_paged_attn_set_override.argtypes = [c_int, c_int]
@@ -149,6 +152,17 @@ def vt_paged_attn_decode_multi(out, q, k_cache, v_cache, block_tables, context_l
     return library().vt_paged_attn_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                                                 q_len, num_q_heads, num_kv_heads, head_dim, block_size, float(scale),
                                                 int(window), stream, max_blocks_per_seq, num_blocks, dtype)
+
+
+def vt_paged_attn_decode_multi_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                   num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, scale, window,
+                                   stream, max_blocks_per_seq, num_blocks) -> int:
+    """Raw call of the multi-token decode over an FP8 (E4M3) KV cache; returns
+    the status code."""
+    return library().vt_paged_attn_decode_multi_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                                    context_lens, num_seqs, q_len, num_q_heads, num_kv_heads,
+                                                    head_dim, block_size, float(scale), int(window), stream,
+                                                    max_blocks_per_seq, num_blocks)
 
 
 def vt_paged_attn_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
@@ -289,12 +303,18 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
                out=None, stream=None):
     """Decode attention over an FP8 (E4M3) KV cache, for torch CUDA tensors.
 
-    q [B][Hq][D] bf16; k_codes, v_codes [num_blocks][32][Hkv][D] uint8 E4M3
-    codes (or torch.float8_e4m3fn); k_scale, v_scale [Hkv] float32.  Returns
-    out [B][Hq][D] bf16 (allocated unless given).  Asynchronous on ``stream``.
+    q [B][Hq][D] bf16, or [B][q_len][Hq][D] for several new tokens per
+    sequence (vt_paged_attn_decode_multi_fp8); k_codes, v_codes
+    [num_blocks][32][Hkv][D] uint8 E4M3 codes (or torch.float8_e4m3fn);
+    k_scale, v_scale [Hkv] float32.  Returns out shaped like q, bf16
+    (allocated unless given).  Asynchronous on ``stream``.
     """
     import torch
-    B, Hq, D = q.shape
+    if q.dim() == 4:
+        B, q_len, Hq, D = q.shape
+    else:
+        B, Hq, D = q.shape
+        q_len = 0
     if k_codes.dtype == torch.float8_e4m3fn:
         k_codes = k_codes.view(torch.uint8)
     if v_codes.dtype == torch.float8_e4m3fn:
@@ -321,11 +341,18 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens
         raise ValueError("out must be a contiguous CUDA tensor shaped and typed like q")
     if scale is None:
         scale = D ** -0.5
-    st = vt_paged_attn_decode_fp8(out.data_ptr(), q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
-                                  k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
-                                  context_lens.data_ptr(), B, Hq, Hkv, D, P, scale, window, _stream_handle(stream),
-                                  block_tables.shape[1], nb)
-    _check(st, "vt_paged_attn_decode_fp8")
+    if q_len:
+        st = vt_paged_attn_decode_multi_fp8(out.data_ptr(), q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                                            k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
+                                            context_lens.data_ptr(), B, q_len, Hq, Hkv, D, P, scale, window,
+                                            _stream_handle(stream), block_tables.shape[1], nb)
+        _check(st, "vt_paged_attn_decode_multi_fp8")
+    else:
+        st = vt_paged_attn_decode_fp8(out.data_ptr(), q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                                      k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
+                                      context_lens.data_ptr(), B, Hq, Hkv, D, P, scale, window,
+                                      _stream_handle(stream), block_tables.shape[1], nb)
+        _check(st, "vt_paged_attn_decode_fp8")
     return out
 
 

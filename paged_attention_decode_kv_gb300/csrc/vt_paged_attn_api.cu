@@ -677,6 +677,20 @@ vt_status vt_paged_attn_decode_fp8(void* out, const void* q, const void* k_cache
   return decode_on_workspace(c);
 }
 
+vt_status vt_paged_attn_decode_multi_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                         const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                         const int32_t* context_lens, int num_seqs, int q_len, int num_q_heads,
+                                         int num_kv_heads, int head_dim, int block_size, float scale, int window,
+                                         vt_stream_t stream, int max_blocks_per_seq, int num_blocks) {
+  Call c = make_call(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, scale, window, stream, max_blocks_per_seq, num_blocks, VT_E4M3);
+  if (!k_scale || !v_scale) return VT_ERR_INVALID_ARG;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  c.q_len = q_len;
+  return decode_on_workspace(c);
+}
+
 vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,

@@ -450,6 +450,30 @@ def pin_e4m3_rows_over_threads(oracle):
         assert np.array_equal(one[r], single), (r, pair)
 
 
+def pin_e4m3_multi_token_is_truncated_decode(oracle):
+    """Several new tokens over an FP8 cache, computed as the multi-token rows
+    on the cache's fp64 values (codes decoded by torch times the scales):
+    new token j of a sequence with L cached tokens equals the FP8 decode of
+    the same query over the first L - q_len + 1 + j tokens, with and without
+    a window (the causal reading of a chunk, on the FP8 reading of a cache)."""
+    rng = np.random.default_rng(41)
+    lens, hq, hkv, d, q_len = [3, 33, 70, 40], 6, 2, 32, 3
+    _, ck, cv, ks, vs, _, _ = _e4m3_case(rng, lens, hq, hkv, d)
+    kc, vc, bt, cl = paginate(ck, cv, 32, rng)
+    q = _rand(rng, (len(lens), q_len, hq, d), "bf16")
+    k64 = _e4m3_value(kc) * ks[None, None, :, None]
+    v64 = _e4m3_value(vc) * vs[None, None, :, None]
+    rows = _all_multi_rows(len(lens), q_len, hq)
+    for window in (0, 20):
+        multi = oracle.decode_multi_rows(rows, widen(q), k64, v64, bt, cl, 0.25, window)
+        for r, (b, j, i) in enumerate(rows):
+            cl_j = cl.copy()
+            cl_j[b] = cl[b] - q_len + 1 + j
+            ref = oracle.decode_rows_e4m3([(b, i)], np.ascontiguousarray(q[:, j]), kc, vc, ks, vs, bt, cl_j, 0.25,
+                                          window)[0]
+            assert np.allclose(multi[r], ref, rtol=0, atol=1e-12), (window, b, j, i)
+
+
 def _multi_case(rng, lens, q_len, hq, hkv, d, kind, block_size):
     q = _rand(rng, (len(lens), q_len, hq, d), kind)
     dk = [_rand(rng, (L, hkv, d), kind) for L in lens]

@@ -76,6 +76,41 @@ def test_host_validation(lib, over, status):
     assert _call(**over) == status
 
 
+def _fp8_call(multi, **over):
+    args = dict(out=0x1000, q=0x2000, k_cache=0x3000, v_cache=0x4000, k_scale=0x7000, v_scale=0x7100,
+                block_tables=0x5000, context_lens=0x6000, num_seqs=2, num_q_heads=16, num_kv_heads=8, head_dim=128,
+                block_size=32, scale=0.088, window=0, stream=None, max_blocks_per_seq=4, num_blocks=16)
+    if multi:
+        args["q_len"] = 3
+    args.update(over)
+    return (vt.vt_paged_attn_decode_multi_fp8 if multi else vt.vt_paged_attn_decode_fp8)(**args)
+
+
+@pytest.mark.parametrize("multi", [False, True])
+@pytest.mark.parametrize("over,status", [
+    (dict(num_seqs=0, out=None, q=None), vt.VT_OK),
+    (dict(k_scale=None), vt.VT_ERR_INVALID_ARG),
+    (dict(v_scale=None), vt.VT_ERR_INVALID_ARG),
+    (dict(k_scale=0x7002), vt.VT_ERR_INVALID_ARG),             # 4-byte alignment
+    (dict(head_dim=64), vt.VT_ERR_UNSUPPORTED),
+    (dict(head_dim=512), vt.VT_ERR_UNSUPPORTED),
+    (dict(q=0x2008), vt.VT_ERR_INVALID_ARG),
+])
+def test_fp8_host_validation(lib, multi, over, status):
+    """The FP8 entry points, single- and multi-token, check their scales and
+    shapes on the host."""
+    assert _fp8_call(multi, **over) == status
+
+
+def test_multi_token_host_validation(lib):
+    base = dict(out=0x1000, q=0x2000, k_cache=0x3000, v_cache=0x4000, block_tables=0x5000, context_lens=0x6000,
+                num_seqs=2, q_len=2, num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=32, scale=0.088,
+                window=0, stream=None, max_blocks_per_seq=4, num_blocks=16, dtype=vt.VT_BF16)
+    assert vt.vt_paged_attn_decode_multi(**dict(base, q_len=0)) == vt.VT_ERR_INVALID_ARG
+    assert vt.vt_paged_attn_decode_multi(**dict(base, dtype=vt.VT_E4M3)) == vt.VT_ERR_INVALID_ARG
+    assert _fp8_call(True, q_len=0) == vt.VT_ERR_INVALID_ARG
+
+
 def test_override_validation(lib):
     assert lib.vt_paged_attn_set_override(-1, 0) == vt.VT_ERR_INVALID_ARG
     assert lib.vt_paged_attn_set_override(0, -5) == vt.VT_ERR_INVALID_ARG

@@ -627,14 +627,23 @@ def test_bounded_wait_gives_up_alternate_pairs(dev, d, dtype, tile):
 # Multi-token decode (q_len new tokens per sequence, causal within them)
 # ---------------------------------------------------------------------------
 def oracle_multi_rows(case, rows=None, window=None, lens=None):
+    """The oracle's multi-token rows; an FP8 cache enters as its values in
+    fp64 (codes decoded by torch's float8_e4m3fn, the decoder the oracle's own
+    E4M3 decoding is pinned against, times the per-kv-head scales)."""
     import oracle
     o = oracle.default_oracle()
     w = case.workload
     k, v, bt = case.compact()
+    q = case.q
+    if case.fp8:
+        ks, vs = case.scales()
+        k = k.view(torch.float8_e4m3fn).to(torch.float64) * ks.double()[None, None, :, None]
+        v = v.view(torch.float8_e4m3fn).to(torch.float64) * vs.double()[None, None, :, None]
+        q = q.to(torch.float64)  # exact; the oracle takes one storage type for q and the caches
     cl = case.context_lens if lens is None else lens
     if rows is None:
         rows = [(b, j, i) for b in range(w.num_seqs) for j in range(w.q_len) for i in range(w.num_q_heads)]
-    ref = o.decode_multi_rows(rows, W.to_oracle_array(case.q), W.to_oracle_array(k), W.to_oracle_array(v),
+    ref = o.decode_multi_rows(rows, W.to_oracle_array(q), W.to_oracle_array(k), W.to_oracle_array(v),
                               bt.numpy(), cl.numpy(), w.scale, w.window if window is None else window,
                               threads=THREADS)
     return np.asarray(rows), ref
@@ -697,10 +706,39 @@ def test_multi_token_short_context_is_nan(dev):
     compare(out[idx[:, 0], idx[:, 1], idx[:, 2]].double().numpy(), ref, torch.bfloat16)
 
 
-def test_multi_token_full_size_sampled(dev):
-    """The multi-token benchmark batch in the benchmark's launch plan, all rows
-    of sampled sequences."""
-    case = W.make_case(W.MULTI_Q4, 0)
+@pytest.mark.parametrize("q_len", [2, 3, 4, 7])
+@pytest.mark.parametrize("hq,hkv,d", [(16, 8, 128), (32, 8, 128), (8, 8, 128), (12, 4, 128), (16, 4, 256)])
+def test_multi_token_fp8(dev, q_len, hq, hkv, d):
+    """Several new tokens over an FP8 cache (vt_paged_attn_decode_multi_fp8):
+    every row against the oracle on the dequantised cache, with windows, split
+    and unsplit, query rows in one or several tensor-core tiles."""
+    lens = [q_len, q_len + 1, 31, 33, 100, 685]
+    case = W.make_case(W.custom(f"multi_fp8_q{q_len}_d{d}", lens, hq, hkv, d, dtype="e4m3", q_len=q_len),
+                       40 + q_len)
+    for window in (0, 5, 64):
+        (_, _), plan = check_multi(case, dev, window=window)
+        assert plan["dtype"] == vt.VT_E4M3
+        check_multi(case, dev, window=window, grid=9, min_units=1)
+
+
+def test_multi_token_fp8_q_len_one_is_decode(dev):
+    """q_len = 1 through the FP8 multi-token entry gives the FP8 decode's bits."""
+    case = W.make_case(W.QWEN3_1P7B_FP8, 34)
+    single, _ = gpu_run(case, dev)
+    k, v = case.pool(dev)
+    ks, vs = case.scales(dev)
+    q = case.q.to(dev)[:, None]
+    out = vt.decode_fp8(q, k, v, ks, vs, case.block_tables.to(dev), case.context_lens.to(dev), case.workload.scale)
+    torch.cuda.synchronize()
+    assert vt.vt_paged_attn_last_plan()["q_len"] == 1
+    assert torch.equal(out[:, 0].cpu().view(torch.int16), single.view(torch.int16))
+
+
+@pytest.mark.parametrize("w", [W.MULTI_Q4, W.MULTI_Q4_FP8], ids=lambda w: w.name)
+def test_multi_token_full_size_sampled(dev, w):
+    """The multi-token benchmark batches in the benchmark's launch plan, all
+    rows of sampled sequences."""
+    case = W.make_case(w, 0)
     L = case.context_lens.numpy()
     pick = sorted({int(np.argmin(L)), int(np.argmax(L)), 7, 30, 55})
     rows = [(b, j, i) for b in pick for j in range(4) for i in range(32)]
