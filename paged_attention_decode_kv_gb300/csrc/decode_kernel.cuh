@@ -942,8 +942,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int kSpread = (GS / G) > 0 ? GS / G : 1;
   const int iq = c / kSpread;
   const bool owner = (c % kSpread) == 0;
-  // mma consumer (bf16): warp = (token half tg, head_dim part dp).  The
-  // products are taken transposed, with the warp's 16 tokens as the M
+  // mma consumer (bf16, FP8): warp = (token half tg, page pair par, head_dim
+  // part dp); par is 0 unless the pairs take alternate stages (NPAR = 2).
+  // The products are taken transposed, with the warp's 16 tokens as the M
   // dimension and the query group as N (8 or 16): S^T = K Q^T over the full
   // head_dim (repeated by the dp warps, or at head_dim 512 split over them
   // and summed), O^T = V^T P^T for the warp's D / NDP output rows of O^T.
