@@ -743,3 +743,53 @@ def test_multi_token_full_size_sampled(dev, w):
     pick = sorted({int(np.argmin(L)), int(np.argmax(L)), 7, 30, 55})
     rows = [(b, j, i) for b in pick for j in range(4) for i in range(32)]
     check_multi(case, dev, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# Seeded random configurations across the whole surface
+# ---------------------------------------------------------------------------
+_RANDOM_ARMS = [(64, "bf16"), (64, "bf16"), (64, "f32"), (128, "bf16"), (128, "f32"), (128, "e4m3"),
+                (128, "e4m3"), (128, "e4m3"), (256, "bf16"), (256, "f32"), (256, "e4m3"), (256, "e4m3"),
+                (512, "bf16")]
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_random_configurations(dev, seed):
+    """A seeded draw of head_dim and storage, group size, new tokens per
+    sequence, window, context mix (empty, one-token, page-straddling and long
+    contexts) and a forced or default grid; sampled rows of every sequence
+    against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    d, dtype = _RANDOM_ARMS[int(rng.integers(len(_RANDOM_ARMS)))]
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16]))
+    q_len = int(rng.choice([1, 1, 1, 2, 4]))
+    if q_len * g > 64:
+        q_len = 1
+    B = int(rng.integers(1, 9))
+    pool = [0, 1, 2, 31, 32, 33, 63, 64, 65, 95, 97, 129, 300, 777, 1500]
+    lens = [int(rng.choice(pool)) for _ in range(B)]
+    lens = [max(L, q_len) if L > 0 else 0 for L in lens]
+    if max(lens) == 0:
+        lens[0] = 40
+    window = int(rng.choice([0, 0, 1, 17, 64, 333]))
+    grid = int(rng.choice([0, 0, 1, 3, 17, 200]))
+    case = W.make_case(W.custom(f"rand{seed}", lens, hkv * g, hkv, d, dtype=dtype, q_len=q_len), 2000 + seed)
+    out, plan = gpu_run(case, dev, window=window, grid=grid, min_units=1 if grid else 0)
+    w = case.workload
+    heads = sorted({0, w.num_q_heads - 1, int(rng.integers(w.num_q_heads))})
+    live = [b for b in range(B) if lens[b] > 0]
+    for b in range(B):
+        if lens[b] == 0:  # decode: a zero row; several new tokens need L >= q_len: NaN rows
+            if q_len == 1:
+                assert torch.count_nonzero(out[b]) == 0
+            else:
+                assert torch.isnan(out[b].float()).all()
+    if q_len == 1:
+        idx, ref = oracle_rows(case, [(b, i) for b in live for i in heads], window=window)
+        got = out[idx[:, 0], idx[:, 1]].to(torch.float64).numpy()
+    else:
+        rows = [(b, j, i) for b in live for j in range(q_len) for i in heads]
+        idx, ref = oracle_multi_rows(case, rows, window=window)
+        got = out[idx[:, 0], idx[:, 1], idx[:, 2]].to(torch.float64).numpy()
+    compare(got, ref, case.q.dtype, f"seed {seed}: d{d} {dtype} g{g} q_len{q_len} W{window} grid{grid}")
