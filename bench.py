@@ -44,7 +44,7 @@ SWEEP = ["batch1_ctx32768_gqa4_d128", "large_gqa8_b64_d128", "d256_gqa4_b16", "d
          "d256_gqa4_b16_f32", "d256_gqa4_b16_f32_w1024", "qwen3_1p7b_b8_gqa2_d128", "d64_gqa4_b32",
          "d64_gqa4_b32_f32", "skewed_b128_gqa4_d128_fp8", "batch1_ctx32768_gqa4_d128_fp8",
          "large_gqa8_b64_d128_fp8", "d256_gqa4_b16_fp8", "d512_gqa4_b16", "d512_gqa4_b16_w1024", "multi_q4_b64_gqa4_d128",
-         "multi_q4_b64_gqa4_d128_fp8"]
+         "multi_q4_b64_gqa4_d128_fp8", "d64_gqa4_b32_fp8"]
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy rate is the roofline peak)
 KERNEL_SOURCES = ["decode_kernel.cuh", "kernel_variants.cuh", "vt_paged_attn_api.cu"]  # shared by every variant

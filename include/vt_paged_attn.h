@@ -161,7 +161,7 @@ VT_API vt_status vt_paged_attn_decode_noalloc(void* out, const void* q, const vo
  *                     [head_dim] (NHD), 16-byte aligned.
  *   k_scale, v_scale  device float32 [num_kv_heads], 4-byte aligned; NULL is
  *                     VT_ERR_INVALID_ARG.
- *   head_dim          128 or 256 (64 is VT_ERR_UNSUPPORTED).
+ *   head_dim          64, 128 or 256 (512 is VT_ERR_UNSUPPORTED).
  * Arithmetic: the K and V codes are widened exactly to f16 and enter f16
  * tensor-core MMAs with fp32 accumulation.  Each query row is scaled by a
  * power of two that puts its largest magnitude in [2^14, 2^15) and rounded

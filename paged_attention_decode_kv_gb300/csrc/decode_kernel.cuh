@@ -602,7 +602,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
   constexpr int NPAR = S::NPAR;
   static_assert(!kMma || (sizeof(T) == 2 && (NCW == 4 || NCW == 8) && G <= 16 && (D / S::NDP) % 16 == 0),
                 "mma consumer shape");
-  static_assert(!kFp8 || (D % 128 == 0 && (D / S::NDP) % 32 == 0), "fp8 consumer shape");
+  static_assert(!kFp8 || ((D % 128 == 0 || D == 64) && (D / S::NDP) % 32 == 0), "fp8 consumer shape");
+  // FP8 tiles in shared memory: rows of kF8Row code bytes per column block,
+  // swizzled as the tensor map writes them (128-byte rows: 16-byte chunk
+  // XOR row mod 8; the 64-byte rows of head_dim 64: chunk XOR (row / 2) mod 4).
+  constexpr int kF8Row = (D >= 128) ? 128 : 64;
+  auto f8_off = [&](int t, int byte) -> uint32_t {
+    const int sb = byte / kF8Row, chunk = (byte % kF8Row) >> 4;
+    const int sw = (kF8Row == 128) ? (chunk ^ (t & 7)) : (chunk ^ ((t >> 1) & 3));
+    return static_cast<uint32_t>(sb * (kPageTokens * kF8Row) + t * kF8Row + (sw << 4));
+  };
   static_assert(NSTAGE % NPAR == 0, "alternate-page pairs need an even ring");
   static_assert(kMma || (S::GS <= 32 && (32 % S::GS) == 0 && S::NG * S::TPG == kPageTokens &&
                          G <= S::GS && (S::GS % G) == 0), "CUDA-core consumer shape");
@@ -1209,10 +1218,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           const int t = 16 * tg + ((mi & 1) << 3) + r;
 #pragma unroll
           for (int kp = 0; kp < kKSteps / 2; ++kp) {
-            const int byte = kp * 32 + ((mi >> 1) << 4);
-            const int sb = byte >> 7, chunk = (byte & 127) >> 4;
             uint32_t ak[4];
-            ldmatrix_x4(kbase + sb * (kPageTokens * 128) + t * 128 + ((chunk ^ (t & 7)) << 4), ak);
+            ldmatrix_x4(kbase + f8_off(t, kp * 32 + ((mi >> 1) << 4)), ak);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               uint32_t af[4];
@@ -1427,13 +1434,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, MINB)
           // of tokens outside the page's range are cleared (they may be NaN).
           const int mi = lane >> 3, r = lane & 7;
           const int t = 16 * tg + ((mi & 1) << 3) + r;  // token row this lane addresses
-          const uint32_t vrow = smem_addr(s.v[st]) + t * 128;
+          const uint32_t vbase = smem_addr(s.v[st]);
 #pragma unroll
           for (int mp = 0; mp < kMt / 2; ++mp) {  // two 16-code blocks per ldmatrix.x4
-            const int byte = dp * kDPart + mp * 32 + ((mi >> 1) << 4);
-            const int sb = byte >> 7, chunk = (byte & 127) >> 4;
             uint32_t w[4];  // (tokens 0-7, 8-15) of block 2mp, then of block 2mp + 1
-            ldmatrix_x4_trans(vrow + sb * (kPageTokens * 128) + ((chunk ^ (t & 7)) << 4), w);
+            ldmatrix_x4_trans(vbase + f8_off(t, dp * kDPart + mp * 32 + ((mi >> 1) << 4)), w);
             if (!full_page) {
               w[0] &= mlo;
               w[1] &= mhi;

@@ -100,6 +100,7 @@ const VariantInfo* variants_d256_bf16(int* count);
 const VariantInfo* variants_d512_bf16(int* count);
 const VariantInfo* variants_d128_f32(int* count);
 const VariantInfo* variants_d256_f32(int* count);
+const VariantInfo* variants_d64_e4m3(int* count);
 const VariantInfo* variants_d128_e4m3(int* count);
 const VariantInfo* variants_d256_e4m3(int* count);
 

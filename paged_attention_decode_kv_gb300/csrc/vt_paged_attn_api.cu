@@ -67,6 +67,7 @@ const VariantInfo* find_variant(int head_dim, vt_dtype dtype, int group_tile) {
   if (head_dim == 512 && dtype == VT_BF16) table = vt::variants_d512_bf16(&n);
   if (head_dim == 128 && dtype == VT_F32) table = vt::variants_d128_f32(&n);
   if (head_dim == 256 && dtype == VT_F32) table = vt::variants_d256_f32(&n);
+  if (head_dim == 64 && dtype == VT_E4M3) table = vt::variants_d64_e4m3(&n);
   if (head_dim == 128 && dtype == VT_E4M3) table = vt::variants_d128_e4m3(&n);
   if (head_dim == 256 && dtype == VT_E4M3) table = vt::variants_d256_e4m3(&n);
   for (int k = 0; k < n; ++k)
@@ -278,16 +279,17 @@ vt_status tensor_map(const MapKey& k, CUtensorMap* out) {
   CUresult r;
   if (k.dtype == VT_E4M3) {
     // FP8 consumer: the same 4-D view as bf16 over bytes, column blocks of
-    // 128 codes (one 128-byte swizzle row), head_dim 128 or 256.
-    constexpr cuuint64_t kCols = 128;
+    // 128 codes (one 128-byte swizzle row) at head_dim 128 or 256, one block
+    // of 64 codes with the 64-byte swizzle at head_dim 64.
+    const cuuint64_t kCols = k.head_dim >= 128 ? 128 : 64;
     const cuuint64_t dims[4] = {kCols, tokens, static_cast<cuuint64_t>(k.head_dim) / kCols,
                                 static_cast<cuuint64_t>(k.num_kv_heads)};
     const cuuint64_t strides[3] = {row, kCols, static_cast<cuuint64_t>(k.head_dim)};
     const cuuint32_t box[4] = {static_cast<cuuint32_t>(kCols), static_cast<cuuint32_t>(vt::kPageTokens),
                                static_cast<cuuint32_t>(k.head_dim / kCols), 1u};
     r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(k.ptr), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+           CU_TENSOR_MAP_INTERLEAVE_NONE, kCols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else if (k.dtype == VT_BF16) {
     // Tensor-core consumer: a 4-D view (64 columns, token, column block, kv
     // head) so one box brings a whole [32 tokens][head_dim] tile of one head,
@@ -375,7 +377,7 @@ vt_status validate(const Call& c) {
       !aligned(c.block_tables, 4) || !aligned(c.context_lens, 4))
     return VT_ERR_INVALID_ARG;
   if (c.head_dim != 64 && c.head_dim != 128 && c.head_dim != 256 && c.head_dim != 512) return VT_ERR_UNSUPPORTED;
-  if (c.dtype == VT_E4M3 && (c.head_dim == 64 || c.head_dim == 512)) return VT_ERR_UNSUPPORTED;
+  if (c.dtype == VT_E4M3 && c.head_dim == 512) return VT_ERR_UNSUPPORTED;
   if (c.dtype == VT_F32 && c.head_dim == 512) return VT_ERR_UNSUPPORTED;
   if (c.block_size != vt::kPageTokens) return VT_ERR_UNSUPPORTED;
   if (static_cast<long long>(c.num_blocks) * vt::kPageTokens > 0x7fffffffLL) return VT_ERR_UNSUPPORTED;

@@ -195,6 +195,8 @@ BATCH1_LONG_FP8 = _register(BATCH1_LONG.with_(name="batch1_ctx32768_gqa4_d128_fp
                                              description=BATCH1_LONG.description + _FP8))
 MULTI_Q4_FP8 = _register(MULTI_Q4.with_(name="multi_q4_b64_gqa4_d128_fp8", dtype="e4m3",
                                        description=MULTI_Q4.description + _FP8))
+D64_GQA4_FP8 = _register(D64_GQA4.with_(name="d64_gqa4_b32_fp8", dtype="e4m3",
+                                       description=D64_GQA4.description + _FP8))
 
 
 def custom(name: str, contexts, num_q_heads: int, num_kv_heads: int, head_dim: int,

@@ -92,8 +92,8 @@ def _fp8_call(multi, **over):
     (dict(k_scale=None), vt.VT_ERR_INVALID_ARG),
     (dict(v_scale=None), vt.VT_ERR_INVALID_ARG),
     (dict(k_scale=0x7002), vt.VT_ERR_INVALID_ARG),             # 4-byte alignment
-    (dict(head_dim=64), vt.VT_ERR_UNSUPPORTED),
     (dict(head_dim=512), vt.VT_ERR_UNSUPPORTED),
+    (dict(head_dim=96), vt.VT_ERR_UNSUPPORTED),
     (dict(q=0x2008), vt.VT_ERR_INVALID_ARG),
 ])
 def test_fp8_host_validation(lib, multi, over, status):

@@ -120,7 +120,7 @@ def check_case(case, dev, rows=None, **kw):
 # ---------------------------------------------------------------------------
 SMALL = [W.TINY, W.QWEN3_1P7B, W.D256_GQA4, W.D256_GQA4_W1024, W.D256_GQA4_F32, W.D256_GQA4_F32_W1024,
          W.D64_GQA4, W.D64_GQA4_F32, W.QWEN3_1P7B_FP8, W.D256_GQA4_FP8, W.D256_GQA4_W1024_FP8,
-         W.D512_GQA4, W.D512_GQA4_W1024]
+         W.D512_GQA4, W.D512_GQA4_W1024, W.D64_GQA4_FP8]
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -173,7 +173,7 @@ def test_page_boundary_contexts(dev, ctx):
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (12, 4), (16, 4), (20, 4), (32, 4), (48, 4), (64, 4), (6, 2)])
 @pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (128, "f32"), (64, "bf16"), (64, "f32"),
-                                     (128, "e4m3"), (256, "e4m3"), (512, "bf16")])
+                                     (64, "e4m3"), (128, "e4m3"), (256, "e4m3"), (512, "bf16")])
 def test_group_sizes(dev, hq, hkv, d, dtype):
     """GQA groups 1..16 including ones that pad the group tile (3, 5) or need
     several query subgroups per kv head (12, 16)."""
@@ -200,7 +200,7 @@ def test_head_dim_512_page_boundary_contexts(dev, d):
         check_case(case, dev, window=window, grid=13, min_units=1)
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_fp8_page_boundary_contexts(dev, d):
     """The FP8 arm on the contexts straddling the 32-token page, with and
     without a window, split and unsplit."""
@@ -249,7 +249,7 @@ def test_fp8_invalid_device_data_and_empty(dev):
         compare(out[idx[:, 0], idx[:, 1]].double().numpy(), ref, torch.bfloat16)
 
 
-@pytest.mark.parametrize("d,dtype", [(128, "e4m3"), (256, "e4m3"), (64, "bf16")], ids=lambda x: str(x))
+@pytest.mark.parametrize("d,dtype", [(64, "e4m3"), (128, "e4m3"), (256, "e4m3"), (64, "bf16")], ids=lambda x: str(x))
 def test_alternate_page_pairs(dev, d, dtype):
     """The arms whose warps form two pairs taking alternate ring stages: odd
     and even page counts (an odd segment is closed by a stage without tiles,
@@ -707,7 +707,8 @@ def test_multi_token_short_context_is_nan(dev):
 
 
 @pytest.mark.parametrize("q_len", [2, 3, 4, 7])
-@pytest.mark.parametrize("hq,hkv,d", [(16, 8, 128), (32, 8, 128), (8, 8, 128), (12, 4, 128), (16, 4, 256)])
+@pytest.mark.parametrize("hq,hkv,d", [(16, 8, 128), (32, 8, 128), (8, 8, 128), (12, 4, 128), (16, 4, 256),
+                                      (16, 4, 64)])
 def test_multi_token_fp8(dev, q_len, hq, hkv, d):
     """Several new tokens over an FP8 cache (vt_paged_attn_decode_multi_fp8):
     every row against the oracle on the dequantised cache, with windows, split
@@ -748,7 +749,7 @@ def test_multi_token_full_size_sampled(dev, w):
 # ---------------------------------------------------------------------------
 # Seeded random configurations across the whole surface
 # ---------------------------------------------------------------------------
-_RANDOM_ARMS = [(64, "bf16"), (64, "bf16"), (64, "f32"), (128, "bf16"), (128, "f32"), (128, "e4m3"),
+_RANDOM_ARMS = [(64, "bf16"), (64, "e4m3"), (64, "f32"), (128, "bf16"), (128, "f32"), (128, "e4m3"),
                 (128, "e4m3"), (128, "e4m3"), (256, "bf16"), (256, "f32"), (256, "e4m3"), (256, "e4m3"),
                 (512, "bf16")]
 
