@@ -55,7 +55,7 @@ typedef enum {
 } vt_status;
 
 /* Storage types.  VT_E4M3 is an FP8 K/V cache (with bf16 q and out) and is
- * taken only by vt_paged_attn_decode_fp8. */
+ * taken only by vt_paged_attn_decode_fp8 and vt_paged_attn_decode_multi_fp8. */
 typedef enum { VT_BF16 = 0, VT_F32 = 1, VT_E4M3 = 2 } vt_dtype;
 
 /*
