@@ -20,7 +20,7 @@ const VariantInfo* variants_d64_f32(int* count) {
       Variant<64, float, 1, 4, 2, 6, Math::kSimt>::info(),
       Variant<64, float, 2, 4, 2, 6, Math::kSimt>::info(),
       Variant<64, float, 4, 4, 2, 6, Math::kSimt>::info(),
-      Variant<64, float, 8, 4, 2, 6, Math::kSimt>::info(),
+      Variant<64, float, 8, 4, 1, 6, Math::kSimt>::info(),
   };
   *count = 4;
   return table;
